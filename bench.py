@@ -1,0 +1,353 @@
+#!/usr/bin/env python
+"""GPT-2 124M training throughput on B300: tokens/s and MFU of the full training step
+(forward, backward, global-norm clip, AdamW) through the libgpt2 C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = the GPT-2 124M optimiser step: 40 micro-batches of 12 x 1024 tokens
+(forward + backward each, gradients accumulated with scale 1/40), global-norm clip 1.0 and
+AdamW (lr from the 6e-4 warmup-cosine schedule, betas 0.9/0.95, wd 0.1). Tokens are
+seeded synthetic Zipf(1.0) ids over the GPT-2 vocabulary (no dataset is available) and
+weights are the N(0, 0.02) initialisation. Under torchrun each rank runs an independent
+replica on its own GPU and its own token stream (no collective on the data path), so
+the throughput is weak-scaled. Prints one JSON line on rank 0.
+"""
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from decoder_only_transformer_05_b300 import synthetic as S  # noqa: E402
+
+METRIC = "GPT-2 124M training tokens/sec on 1 B300; MFU vs dense BF16 tensor peak"
+WORKLOAD = "gpt2-124m-step"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"],
+                    bf16_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
+
+
+def lr_at(it):
+    # linear warmup over 2000 steps to 6e-4, cosine to 6e-5 at 600000 steps
+    if it < 2000:
+        return 6e-4 * (it + 1) / 2000
+    r = (it - 2000) / (600000 - 2000)
+    return 6e-5 + 0.5 * (1 + math.cos(math.pi * min(r, 1.0))) * (6e-4 - 6e-5)
+
+
+def flops_per_token(n_model, L, T, C):
+    return 6.0 * n_model + 6.0 * L * T * C
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.rows, self.proc = index, [], None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        if not self.rows:
+            return None
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if r[3 + i].lower() in ("active", "1")})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_sample(w, params_seed, seq_index, steps_label):
+    """The CPU oracle on a bounded sample of the workload: one 1024-token sequence,
+    forward + backward, then AdamW over every parameter. Returns (tokens, seconds)."""
+    from oracle import gpt2_oracle as O
+    cfg = O.Config(w["V"], w["Vp"], w["T"], w["L"], w["H"], w["C"], w["bias"])
+    params = oracle_sample.params
+    if params is None:
+        params = S.init_params(params_seed, w["V"], w["Vp"], w["T"], w["L"], w["C"], w["bias"],
+                               dtype=np.float64)
+        oracle_sample.params = params
+    tok, tgt = S.batch(w["tok_seed"], seq_index, 1, w["T"], w["V"], w["dist"], w["s"])
+    t0 = time.perf_counter()
+    out = O.forward(params, cfg, tok, tgt)
+    g = O.backward(params, cfg, out["cache"], 1.0)
+    del out
+    _, coef = O.clip_coefficient(g, 1.0)
+    for k in params:
+        O.adamw_update(params[k], g[k], np.zeros_like(params[k]), np.zeros_like(params[k]), 1,
+                       6e-4, 0.9, 0.95, 1e-8, 0.1, coef)
+    return w["T"], time.perf_counter() - t0
+
+
+oracle_sample.params = None
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i["num_threads"] for i in threadpool_info() if i.get("internal_api") in
+             ("openblas", "mkl", "blis")]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+SAMPLE_DESC = ("one 1024-token sequence of the GPT-2 124M step (forward, backward, "
+               "global-norm clip and AdamW over all 124M parameters) in float64 numpy")
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    for i in range(args.warmup):
+        oracle_sample(w, w["w_seed"], i, "warmup")
+    toks, secs = 0, 0.0
+    for i in range(args.steps):
+        t, s = oracle_sample(w, w["w_seed"], args.warmup + i, "timed")
+        toks += t
+        secs += s
+    value = toks / secs
+    cores = blas_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * secs / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(w),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": SAMPLE_DESC + " per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block(w):
+    return {"workload": f"{WORKLOAD}: GPT-2 124M (L=12, H=12, C=768, T=1024, V=50257 "
+                        "padded to 50304), 40 micro-batches of 12 x 1024 tokens, clip 1.0, "
+                        "AdamW",
+            "batch": w["B"], "seq_len": w["T"], "grad_accum": w["accum"],
+            "tokens_per_step": w["B"] * w["T"] * w["accum"],
+            "l2": "working set (weights, activations, 1.2 GB logits) far larger than L2"}
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+    from decoder_only_transformer_05_b300 import build as b
+    from decoder_only_transformer_05_b300 import gpt2 as G
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    b.build()
+    G.load_library()
+    B, T, accum = w["B"], w["T"], w["accum"]
+    m = G.GPT2(vocab_size=w["V"], padded_vocab_size=w["Vp"], block_size=T, n_layer=w["L"],
+               n_head=w["H"], n_embd=w["C"], batch_size=B, bias=w["bias"], precision="bf16",
+               init=True, seed=w["w_seed"])
+    stream = torch.cuda.current_stream()
+    m.set_stream(stream)
+
+    # token batches for every step, generated up front and resident in HBM
+    W, K = args.warmup, args.steps
+    nb = (W + K) * accum
+    ids = np.stack([S.token_stream(w["tok_seed"], rank * 1_000_000 + i, B, T, w["V"], w["dist"],
+                                   w["s"]) for i in range(nb)])
+    dtok = torch.tensor(ids[:, :, :T]).cuda().contiguous()
+    dtgt = torch.tensor(ids[:, :, 1:]).cuda().contiguous()
+
+    def step(si):
+        m.zero_grad()
+        for a in range(accum):
+            i = si * accum + a
+            m.forward(dtok[i], dtgt[i], B, T)
+            m.backward(1.0 / accum)
+        m.adamw_step(lr_at(si), 0.9, 0.95, 1e-8, 0.1, grad_clip=1.0)
+
+    for si in range(W):
+        step(si)
+    torch.cuda.synchronize()
+    m.sync()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---------------- timed region: inputs already in HBM
+    m.profile_enable(("gemm",), capacity=160 * accum * K + 64)
+    m.profile_read("gemm", reset=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    launches0 = G.kernel_launches()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for si in range(W, W + K):
+        step(si)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clock_info = clocks.stop()
+    launches = G.kernel_launches() - launches0
+    elapsed_ms = ev0.elapsed_time(ev1)
+    loss = m.get_loss()
+    g_n, g_ms, g_flops = m.profile_read("gemm", reset=True)
+    m.profile_enable((), capacity=0)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    tokens = world * K * B * T * accum
+    value = tokens / (elapsed_ms / 1000.0)
+
+    # ---------------- end to end: host (pinned) tokens copied in, loss read back, per step
+    e2e = None
+    if not args.no_e2e:
+        htok = torch.tensor(ids[:, :, :T]).pin_memory()
+        htgt = torch.tensor(ids[:, :, 1:]).pin_memory()
+        stok = torch.empty(B, T, dtype=torch.int32, device="cuda")
+        stgt = torch.empty(B, T, dtype=torch.int32, device="cuda")
+
+        def step_e2e(si):
+            m.zero_grad()
+            for a in range(accum):
+                i = si * accum + a
+                stok.copy_(htok[i], non_blocking=True)
+                stgt.copy_(htgt[i], non_blocking=True)
+                m.forward(stok, stgt, B, T)
+                m.backward(1.0 / accum)
+            m.adamw_step(lr_at(si), 0.9, 0.95, 1e-8, 0.1, grad_clip=1.0)
+            return m.get_loss()
+
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for si in range(W, W + K):
+            step_e2e(si)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_s = time.perf_counter() - t0
+        if world > 1:
+            t = torch.tensor([e2e_s], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": tokens / e2e_s, "unit": "tokens/s",
+               "h2d_bytes_per_step": int(accum * 2 * B * T * 4), "d2h_bytes_per_step": 4}
+
+    pk = peaks()
+    fpt = flops_per_token(m.num_params, w["L"], T, w["C"])
+    gemm_tflops = g_flops / (g_ms / 1000.0) / 1e12 if g_ms > 0 else None
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        toks, secs = oracle_sample(w, w["w_seed"], 0, "baseline")
+        cpu = {"value": toks / secs, "unit": "tokens/s", "cores": blas_threads(),
+               "kind": "oracle", "sample": SAMPLE_DESC}
+    m.close()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_block(w),
+            "mfu": {"flops_per_token": fpt, "value": value / world * fpt / (pk["bf16"] * 1e12),
+                    "peak_tflops": pk["bf16"],
+                    "vs_sustained": value / world * fpt / (pk["bf16_sustained"] * 1e12),
+                    "peak_source": pk["source"]},
+            "loss": loss,
+            "clocks": clock_info,
+            "e2e": e2e,
+            "gpu_launches": int(launches),
+            "roofline": {"kernel": "tcgen05 GEMM (all Linear layers, forward/dgrad/wgrad)",
+                         "bound": "tensor", "achieved": gemm_tflops,
+                         "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
+                         "frac": gemm_tflops / pk["bf16_sustained"] if gemm_tflops else None,
+                         "peak_kind": f"bf16 sustained ({pk['source']})",
+                         "launches": g_n, "avg_launch_ms": g_ms / g_n if g_n else None,
+                         "traffic": None},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--accum", type=int, default=None, help="override micro-batches per step")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = dict(S.WORKLOADS[WORKLOAD])
+    if args.accum:
+        w["accum"] = args.accum
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,623 @@
+// Causal multi-head self-attention, forward and backward.
+//
+// Math (「从零实现一个最小GPT：代码讲解 + 知识点全解」 三.3-三.4): for head h, q, k, v are
+// columns [h*hs, (h+1)*hs) of the Q, K, V thirds of qkv [B, T, 3C];
+// s_ij = q_i . k_j / sqrt(hs) for j <= i, p = softmax_j(s), o_i = sum_j p_ij v_j, heads
+// concatenated in head order into out [B, T, C]. The T x T weights are never stored:
+// the forward keeps lse_i = log sum_j exp(s_ij) per row and the backward recomputes p.
+// Backward: D_i = dO_i . O_i; dp_ij = dO_i . v_j; ds_ij = p_ij (dp_ij - D_i);
+// dq_i = sum_j ds_ij k_j / sqrt(hs); dk_j = sum_i ds_ij q_i / sqrt(hs); dv_j = sum_i p_ij dO_i.
+// dQ and dK/dV come from separate kernels, so no float atomics are needed and the result
+// is deterministic.
+//
+// Two implementations:
+//  * fp32: one warp per (batch, head, row), plain FMA (parity path).
+//  * bf16, head size 64: flash-attention tiles of 64 queries x 64 keys on mma.sync
+//    tensor-core instructions, online softmax in registers.
+#include "common.cuh"
+#include "launch.h"
+
+namespace gpt2k {
+
+// =====================================================================================
+// fp32 path
+__global__ void attn_fwd_f32_kernel(float* __restrict__ out, float* __restrict__ lse,
+                                    const float* __restrict__ qkv, int B, int T, int C, int H) {
+  extern __shared__ float sc_f32[];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + wid;
+  if (gw >= (long long)B * H * T) return;
+  const int i = (int)(gw % T);
+  const int h = (int)((gw / T) % H);
+  const int b = (int)(gw / ((long long)T * H));
+  const int hs = C / H;
+  const float scale = 1.0f / sqrtf((float)hs);
+  float* s = sc_f32 + (size_t)wid * T;
+  const float* base = qkv + (size_t)b * T * 3 * C;
+  const float* q = base + (size_t)i * 3 * C + h * hs;
+  float mx = -INFINITY;
+  for (int j = lane; j <= i; j += 32) {
+    const float* k = base + (size_t)j * 3 * C + C + h * hs;
+    float d = 0.f;
+    for (int e = 0; e < hs; ++e) d = fmaf(q[e], k[e], d);
+    s[j] = d * scale;
+    mx = fmaxf(mx, s[j]);
+  }
+  mx = warp_max(mx);
+  float sum = 0.f;
+  for (int j = lane; j <= i; j += 32) { float p = expf(s[j] - mx); s[j] = p; sum += p; }
+  sum = warp_sum(sum);
+  __syncwarp();
+  for (int d = lane; d < hs; d += 32) {
+    float o = 0.f;
+    for (int j = 0; j <= i; ++j) o = fmaf(s[j], base[(size_t)j * 3 * C + 2 * C + h * hs + d], o);
+    out[((size_t)b * T + i) * C + h * hs + d] = o / sum;
+  }
+  if (lane == 0) lse[((size_t)b * H + h) * T + i] = mx + logf(sum);
+}
+
+// D_i = dO_i . O_i per (b, h, i)
+__global__ void attn_bwd_D_f32_kernel(float* __restrict__ Dbuf, const float* __restrict__ dout,
+                                      const float* __restrict__ out, int B, int T, int C, int H) {
+  const int lane = threadIdx.x & 31;
+  const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (gw >= (long long)B * H * T) return;
+  const int i = (int)(gw % T), h = (int)((gw / T) % H), b = (int)(gw / ((long long)T * H));
+  const int hs = C / H;
+  size_t o = ((size_t)b * T + i) * C + h * hs;
+  float d = 0.f;
+  for (int e = lane; e < hs; e += 32) d = fmaf(dout[o + e], out[o + e], d);
+  d = warp_sum(d);
+  if (lane == 0) Dbuf[((size_t)b * H + h) * T + i] = d;
+}
+
+__global__ void attn_bwd_dq_f32_kernel(float* __restrict__ dqkv, const float* __restrict__ Dbuf,
+                                       const float* __restrict__ dout, const float* __restrict__ qkv,
+                                       const float* __restrict__ lse, int B, int T, int C, int H) {
+  extern __shared__ float sc_f32[];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + wid;
+  if (gw >= (long long)B * H * T) return;
+  const int i = (int)(gw % T), h = (int)((gw / T) % H), b = (int)(gw / ((long long)T * H));
+  const int hs = C / H;
+  const float scale = 1.0f / sqrtf((float)hs);
+  float* ds = sc_f32 + (size_t)wid * T;
+  const float* base = qkv + (size_t)b * T * 3 * C;
+  const float* q = base + (size_t)i * 3 * C + h * hs;
+  const float* dO = dout + ((size_t)b * T + i) * C + h * hs;
+  const size_t ri = ((size_t)b * H + h) * T + i;
+  const float L = lse[ri], Di = Dbuf[ri];
+  for (int j = lane; j <= i; j += 32) {
+    const float* k = base + (size_t)j * 3 * C + C + h * hs;
+    const float* v = base + (size_t)j * 3 * C + 2 * C + h * hs;
+    float s = 0.f, dp = 0.f;
+    for (int e = 0; e < hs; ++e) { s = fmaf(q[e], k[e], s); dp = fmaf(dO[e], v[e], dp); }
+    float p = expf(s * scale - L);
+    ds[j] = p * (dp - Di);
+  }
+  __syncwarp();
+  for (int d = lane; d < hs; d += 32) {
+    float a = 0.f;
+    for (int j = 0; j <= i; ++j) a = fmaf(ds[j], base[(size_t)j * 3 * C + C + h * hs + d], a);
+    dqkv[((size_t)b * T + i) * 3 * C + h * hs + d] = a * scale;
+  }
+}
+
+__global__ void attn_bwd_dkv_f32_kernel(float* __restrict__ dqkv, const float* __restrict__ Dbuf,
+                                        const float* __restrict__ dout,
+                                        const float* __restrict__ qkv,
+                                        const float* __restrict__ lse, int B, int T, int C, int H) {
+  extern __shared__ float sc_f32[];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + wid;
+  if (gw >= (long long)B * H * T) return;
+  const int j = (int)(gw % T), h = (int)((gw / T) % H), b = (int)(gw / ((long long)T * H));
+  const int hs = C / H;
+  const float scale = 1.0f / sqrtf((float)hs);
+  float* P = sc_f32 + (size_t)wid * 2 * T;
+  float* dS = P + T;
+  const float* base = qkv + (size_t)b * T * 3 * C;
+  const float* k = base + (size_t)j * 3 * C + C + h * hs;
+  const float* v = base + (size_t)j * 3 * C + 2 * C + h * hs;
+  for (int i = j + lane; i < T; i += 32) {
+    const float* q = base + (size_t)i * 3 * C + h * hs;
+    const float* dO = dout + ((size_t)b * T + i) * C + h * hs;
+    const size_t ri = ((size_t)b * H + h) * T + i;
+    float s = 0.f, dp = 0.f;
+    for (int e = 0; e < hs; ++e) { s = fmaf(q[e], k[e], s); dp = fmaf(dO[e], v[e], dp); }
+    float p = expf(s * scale - lse[ri]);
+    P[i] = p;
+    dS[i] = p * (dp - Dbuf[ri]);
+  }
+  __syncwarp();
+  for (int d = lane; d < hs; d += 32) {
+    float av = 0.f, ak = 0.f;
+    for (int i = j; i < T; ++i) {
+      av = fmaf(P[i], dout[((size_t)b * T + i) * C + h * hs + d], av);
+      ak = fmaf(dS[i], base[(size_t)i * 3 * C + h * hs + d], ak);
+    }
+    size_t o = ((size_t)b * T + j) * 3 * C;
+    dqkv[o + C + h * hs + d] = ak * scale;
+    dqkv[o + 2 * C + h * hs + d] = av;
+  }
+}
+
+// =====================================================================================
+// bf16 flash path, head size 64, tiles of 64 rows; 4 warps per block, 16 rows per warp.
+namespace fa {
+
+constexpr int D = 64;
+constexpr int BR = 64;             // rows per tile
+constexpr int THREADS = 128;
+constexpr int TILE_BYTES = BR * D * 2;   // 8 KB, 128 B per row
+constexpr float LOG2E = 1.4426950408889634f;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+// byte offset of 16-byte chunk `ch` of row `r` in a swizzled 64x64 bf16 tile
+__device__ __forceinline__ uint32_t swz(int r, int ch) {
+  return (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
+  int sz = pred ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz));
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N> __device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+// async copy of rows [r0, r0+64) (predicated on r < T) of a row-major bf16 matrix with
+// row stride `ld` elements, columns [col, col+64), into a swizzled tile
+__device__ __forceinline__ void load_tile(uint32_t tile, const bf16* g, int r0, int T, long long ld,
+                                          int col) {
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    int idx = it * THREADS + threadIdx.x;
+    int r = idx >> 3, ch = idx & 7;
+    bool ok = (r0 + r) < T;
+    const bf16* src = g + (size_t)(ok ? r0 + r : 0) * ld + col + ch * 8;
+    cp_async16(tile + swz(r, ch), src, ok);
+  }
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c,
+                                        uint32_t& d) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c,
+                                          uint32_t& d) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// A fragments (16 rows x 64 cols, 4 k-steps) of rows [row0, row0+16) of a tile
+__device__ __forceinline__ void load_a_frags(uint32_t tile, int row0, uint32_t (&a)[4][4]) {
+  const int l = threadIdx.x & 31;
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    int r = row0 + (l & 15), ch = kk * 2 + (l >> 4);
+    ldsm_x4(tile + swz(r, ch), a[kk][0], a[kk][1], a[kk][2], a[kk][3]);
+  }
+}
+
+// acc[8][4] (16 x 64) += A (16 x 64, fragments) * X^T where X is a 64x64 tile stored
+// [n][k] (the B operand's n index is the tile row): "non-transposed" B
+__device__ __forceinline__ void mma_abt(float (&acc)[8][4], const uint32_t (&a)[4][4],
+                                        uint32_t tile) {
+  const int l = threadIdx.x & 31;
+#pragma unroll
+  for (int np = 0; np < 4; ++np) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      int r = np * 16 + ((l >> 4) << 3) + (l & 7), ch = kk * 2 + ((l >> 3) & 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(tile + swz(r, ch), b0, b1, b2, b3);
+      mma16816(acc[2 * np], a[kk], b0, b1);
+      mma16816(acc[2 * np + 1], a[kk], b2, b3);
+    }
+  }
+}
+
+// acc[8][4] (16 x 64) += A (16 x 64 over k = tile rows) * X where X is a 64x64 tile
+// stored [k][n]: "transposed" B
+__device__ __forceinline__ void mma_ab(float (&acc)[8][4], const uint32_t (&a)[4][4],
+                                       uint32_t tile) {
+  const int l = threadIdx.x & 31;
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+    for (int dp = 0; dp < 4; ++dp) {
+      int r = kk * 16 + (((l >> 3) & 1) << 3) + (l & 7), ch = dp * 2 + (l >> 4);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(tile + swz(r, ch), b0, b1, b2, b3);
+      mma16816(acc[2 * dp], a[kk], b0, b1);
+      mma16816(acc[2 * dp + 1], a[kk], b2, b3);
+    }
+  }
+}
+
+// convert a 16x64 fp32 accumulator (C layout) into bf16 A fragments
+__device__ __forceinline__ void acc_to_a(const float (&s)[8][4], uint32_t (&a)[4][4]) {
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    a[kk][0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
+    a[kk][1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
+    a[kk][2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+    a[kk][3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+  }
+}
+
+__device__ __forceinline__ void zero(float (&a)[8][4]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) a[i][j] = 0.f;
+}
+
+__global__ void __launch_bounds__(THREADS)
+fwd_kernel(bf16* __restrict__ out, float* __restrict__ lse, const bf16* __restrict__ qkv, int T,
+           int C, int H) {
+  __shared__ __align__(1024) uint8_t sm[5 * TILE_BYTES];
+  const uint32_t Qs = smem_u32(sm), Ks0 = Qs + TILE_BYTES, Vs0 = Qs + 3 * TILE_BYTES;
+  const int nq = gridDim.x;
+  const int qb = nq - 1 - blockIdx.x;              // heavy (late) blocks first
+  const int bh = blockIdx.y, b = bh / H, h = bh % H;
+  const long long ld = 3LL * C;
+  const bf16* base = qkv + (size_t)b * T * ld;
+  const int l = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int g = l >> 2, tq = l & 3;
+  const float sl2 = rsqrtf((float)D) * LOG2E;
+
+  load_tile(Qs, base, qb * BR, T, ld, h * D);
+  load_tile(Ks0, base, 0, T, ld, C + h * D);
+  load_tile(Vs0, base, 0, T, ld, 2 * C + h * D);
+  cp_commit();
+
+  uint32_t qa[4][4];
+  float o[8][4];
+  zero(o);
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+  const int r0 = qb * BR + w * 16 + g;   // this thread's rows r0 and r0 + 8
+  const int nkv = qb + 1;
+  for (int kb = 0; kb < nkv; ++kb) {
+    const int buf = kb & 1;
+    if (kb + 1 < nkv) {
+      load_tile(Ks0 + (buf ^ 1) * TILE_BYTES, base, (kb + 1) * BR, T, ld, C + h * D);
+      load_tile(Vs0 + (buf ^ 1) * TILE_BYTES, base, (kb + 1) * BR, T, ld, 2 * C + h * D);
+      cp_commit();
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
+    }
+    __syncthreads();
+    if (kb == 0) load_a_frags(Qs, w * 16, qa);
+    const uint32_t Ks = Ks0 + buf * TILE_BYTES, Vs = Vs0 + buf * TILE_BYTES;
+    float s[8][4];
+    zero(s);
+    mma_abt(s, qa, Ks);
+    // scale into the log2 domain, mask the future on the diagonal tile
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        int key = kb * BR + nt * 8 + tq * 2 + (e & 1);
+        int row = r0 + (e >> 1) * 8;
+        float v = s[nt][e] * sl2;
+        if (kb == qb && key > row) v = -INFINITY;
+        s[nt][e] = v;
+        mx[e >> 1] = fmaxf(mx[e >> 1], v);
+      }
+    float alpha[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+      float mn = fmaxf(mrow[r], mx[r]);
+      alpha[r] = fast_exp2(mrow[r] - mn);
+      mrow[r] = mn;
+      lrow[r] *= alpha[r];
+    }
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float p = fast_exp2(s[nt][e] - mrow[e >> 1]);
+        s[nt][e] = p;
+        lrow[e >> 1] += p;
+        o[nt][e] *= alpha[e >> 1];
+      }
+    uint32_t pa[4][4];
+    acc_to_a(s, pa);
+    mma_ab(o, pa, Vs);
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
+    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int row = r0 + r * 8;
+    if (row >= T) continue;
+    const float inv = 1.0f / lrow[r];
+    bf16* dst = out + ((size_t)b * T + row) * C + h * D;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      uint32_t v = pack_bf16(o[nt][2 * r] * inv, o[nt][2 * r + 1] * inv);
+      *reinterpret_cast<uint32_t*>(dst + nt * 8 + tq * 2) = v;
+    }
+    if (tq == 0) lse[((size_t)b * H + h) * T + row] = (mrow[r] + __log2f(lrow[r])) * (1.0f / LOG2E);
+  }
+}
+
+// D_i = dO_i . O_i, one thread per (b, t, h)
+__global__ void bwd_D_kernel(float* __restrict__ Dbuf, const bf16* __restrict__ dout,
+                             const bf16* __restrict__ out, int B, int T, int C, int H) {
+  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)B * T * H) return;
+  int h = (int)(i % H);
+  long long bt = i / H;
+  int t = (int)(bt % T), b = (int)(bt / T);
+  const bf16* a = dout + (size_t)bt * C + h * D;
+  const bf16* c = out + (size_t)bt * C + h * D;
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < D; k += 8) {
+    Vec16<bf16> x = ld16(a + k), y = ld16(c + k);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s += to_f32(x.e[e]) * to_f32(y.e[e]);
+  }
+  Dbuf[((size_t)b * H + h) * T + t] = s;
+}
+
+// dK, dV for one block of 64 keys; loops over the query blocks at or after it.
+__global__ void __launch_bounds__(THREADS)
+bwd_dkv_kernel(bf16* __restrict__ dqkv, const float* __restrict__ Dbuf,
+               const bf16* __restrict__ dout, const bf16* __restrict__ qkv,
+               const float* __restrict__ lse, int T, int C, int H) {
+  extern __shared__ __align__(1024) uint8_t sm[];   // 6 tiles
+  __shared__ float s_lse[2][BR], s_D[2][BR];
+  const uint32_t Ks = smem_u32(sm), Vs = Ks + TILE_BYTES, Qs0 = Ks + 2 * TILE_BYTES,
+                 Os0 = Ks + 4 * TILE_BYTES;
+  const int nb = gridDim.x;
+  const int kb = blockIdx.x;   // key block; q blocks kb..nb-1
+  const int bh = blockIdx.y, b = bh / H, h = bh % H;
+  const long long ld = 3LL * C;
+  const bf16* base = qkv + (size_t)b * T * ld;
+  const bf16* dbase = dout + (size_t)b * T * C;
+  const float* lse_bh = lse + ((size_t)b * H + h) * T;
+  const float* D_bh = Dbuf + ((size_t)b * H + h) * T;
+  const int l = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int g = l >> 2, tq = l & 3;
+  const float sl2 = rsqrtf((float)D) * LOG2E;
+
+  load_tile(Ks, base, kb * BR, T, ld, C + h * D);
+  load_tile(Vs, base, kb * BR, T, ld, 2 * C + h * D);
+  load_tile(Qs0, base, kb * BR, T, ld, h * D);
+  load_tile(Os0, dbase, kb * BR, T, C, h * D);
+  if (threadIdx.x < BR) {
+    int r = kb * BR + threadIdx.x;
+    s_lse[0][threadIdx.x] = r < T ? lse_bh[r] * LOG2E : 0.f;
+    s_D[0][threadIdx.x] = r < T ? D_bh[r] : 0.f;
+  }
+  cp_commit();
+
+  uint32_t ka[4][4], va[4][4];
+  float dk[8][4], dv[8][4];
+  zero(dk);
+  zero(dv);
+  const int key0 = kb * BR + w * 16 + g;   // this thread's keys key0, key0 + 8
+  for (int qb = kb; qb < nb; ++qb) {
+    const int buf = (qb - kb) & 1;
+    if (qb + 1 < nb) {
+      load_tile(Qs0 + (buf ^ 1) * TILE_BYTES, base, (qb + 1) * BR, T, ld, h * D);
+      load_tile(Os0 + (buf ^ 1) * TILE_BYTES, dbase, (qb + 1) * BR, T, C, h * D);
+      if (threadIdx.x < BR) {
+        int r = (qb + 1) * BR + threadIdx.x;
+        s_lse[buf ^ 1][threadIdx.x] = r < T ? lse_bh[r] * LOG2E : 0.f;
+        s_D[buf ^ 1][threadIdx.x] = r < T ? D_bh[r] : 0.f;
+      }
+      cp_commit();
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
+    }
+    __syncthreads();
+    if (qb == kb) { load_a_frags(Ks, w * 16, ka); load_a_frags(Vs, w * 16, va); }
+    const uint32_t Qs = Qs0 + buf * TILE_BYTES, Os = Os0 + buf * TILE_BYTES;
+    // S^T = K Q^T (rows: keys, cols: queries)
+    float st[8][4];
+    zero(st);
+    mma_abt(st, ka, Qs);
+    // P^T = exp(S^T / sqrt(d) - lse[q]), zero where q < key
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        int qi = nt * 8 + tq * 2 + (e & 1);
+        int q = qb * BR + qi;
+        int key = key0 + (e >> 1) * 8;
+        float p = fast_exp2(st[nt][e] * sl2 - s_lse[buf][qi]);
+        st[nt][e] = (q >= key && q < T) ? p : 0.f;
+      }
+    uint32_t pa[4][4];
+    acc_to_a(st, pa);
+    mma_ab(dv, pa, Os);              // dV += P^T dO
+    float dpt[8][4];
+    zero(dpt);
+    mma_abt(dpt, va, Os);            // dP^T = V dO^T
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        int qi = nt * 8 + tq * 2 + (e & 1);
+        dpt[nt][e] = st[nt][e] * (dpt[nt][e] - s_D[buf][qi]);   // dS^T
+      }
+    uint32_t da[4][4];
+    acc_to_a(dpt, da);
+    mma_ab(dk, da, Qs);              // dK += dS^T Q
+    __syncthreads();
+  }
+  const float scale = rsqrtf((float)D);
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int key = key0 + r * 8;
+    if (key >= T) continue;
+    bf16* dst = dqkv + ((size_t)b * T + key) * ld;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      int d = nt * 8 + tq * 2;
+      *reinterpret_cast<uint32_t*>(dst + C + h * D + d) =
+          pack_bf16(dk[nt][2 * r] * scale, dk[nt][2 * r + 1] * scale);
+      *reinterpret_cast<uint32_t*>(dst + 2 * C + h * D + d) =
+          pack_bf16(dv[nt][2 * r], dv[nt][2 * r + 1]);
+    }
+  }
+}
+
+// dQ for one block of 64 queries; loops over the key blocks up to the diagonal.
+__global__ void __launch_bounds__(THREADS)
+bwd_dq_kernel(bf16* __restrict__ dqkv, const float* __restrict__ Dbuf,
+              const bf16* __restrict__ dout, const bf16* __restrict__ qkv,
+              const float* __restrict__ lse, int T, int C, int H) {
+  extern __shared__ __align__(1024) uint8_t sm[];   // 6 tiles
+  const uint32_t Qs = smem_u32(sm), Os = Qs + TILE_BYTES, Ks0 = Qs + 2 * TILE_BYTES,
+                 Vs0 = Qs + 4 * TILE_BYTES;
+  const int nb = gridDim.x;
+  const int qb = nb - 1 - blockIdx.x;
+  const int bh = blockIdx.y, b = bh / H, h = bh % H;
+  const long long ld = 3LL * C;
+  const bf16* base = qkv + (size_t)b * T * ld;
+  const bf16* dbase = dout + (size_t)b * T * C;
+  const int l = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int g = l >> 2, tq = l & 3;
+  const float sl2 = rsqrtf((float)D) * LOG2E;
+  const int r0 = qb * BR + w * 16 + g;
+  float lse2[2], Dr[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    int row = r0 + r * 8;
+    size_t ri = ((size_t)b * H + h) * T + (row < T ? row : 0);
+    lse2[r] = lse[ri] * LOG2E;
+    Dr[r] = Dbuf[ri];
+  }
+  load_tile(Qs, base, qb * BR, T, ld, h * D);
+  load_tile(Os, dbase, qb * BR, T, C, h * D);
+  load_tile(Ks0, base, 0, T, ld, C + h * D);
+  load_tile(Vs0, base, 0, T, ld, 2 * C + h * D);
+  cp_commit();
+  uint32_t qa[4][4], oa[4][4];
+  float dq[8][4];
+  zero(dq);
+  const int nkv = qb + 1;
+  for (int kb = 0; kb < nkv; ++kb) {
+    const int buf = kb & 1;
+    if (kb + 1 < nkv) {
+      load_tile(Ks0 + (buf ^ 1) * TILE_BYTES, base, (kb + 1) * BR, T, ld, C + h * D);
+      load_tile(Vs0 + (buf ^ 1) * TILE_BYTES, base, (kb + 1) * BR, T, ld, 2 * C + h * D);
+      cp_commit();
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
+    }
+    __syncthreads();
+    if (kb == 0) { load_a_frags(Qs, w * 16, qa); load_a_frags(Os, w * 16, oa); }
+    const uint32_t Ks = Ks0 + buf * TILE_BYTES, Vs = Vs0 + buf * TILE_BYTES;
+    float s[8][4], dp[8][4];
+    zero(s);
+    zero(dp);
+    mma_abt(s, qa, Ks);      // S = Q K^T
+    mma_abt(dp, oa, Vs);     // dP = dO V^T
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        int key = kb * BR + nt * 8 + tq * 2 + (e & 1);
+        int row = r0 + (e >> 1) * 8;
+        float p = fast_exp2(s[nt][e] * sl2 - lse2[e >> 1]);
+        p = (key <= row) ? p : 0.f;
+        s[nt][e] = p * (dp[nt][e] - Dr[e >> 1]);   // dS
+      }
+    uint32_t da[4][4];
+    acc_to_a(s, da);
+    mma_ab(dq, da, Ks);      // dQ += dS K
+    __syncthreads();
+  }
+  const float scale = rsqrtf((float)D);
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int row = r0 + r * 8;
+    if (row >= T) continue;
+    bf16* dst = dqkv + ((size_t)b * T + row) * ld + h * D;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+      *reinterpret_cast<uint32_t*>(dst + nt * 8 + tq * 2) =
+          pack_bf16(dq[nt][2 * r] * scale, dq[nt][2 * r + 1] * scale);
+  }
+}
+
+}  // namespace fa
+
+// =====================================================================================
+cudaError_t attention_forward(DType t, void* out, float* lse, const void* qkv, int B, int T, int C,
+                              int H, cudaStream_t s) {
+  if (t == DType::BF16) {
+    if (C / H != fa::D || C % H) return cudaErrorInvalidValue;
+    dim3 grid(ceil_div(T, fa::BR), B * H);
+    fa::fwd_kernel<<<grid, fa::THREADS, 0, s>>>((bf16*)out, lse, (const bf16*)qkv, T, C, H); count_launches(1);
+    return cudaGetLastError();
+  }
+  long long warps = (long long)B * H * T;
+  attn_fwd_f32_kernel<<<ceil_div(warps, 4), 128, 4 * T * sizeof(float), s>>>(
+      (float*)out, lse, (const float*)qkv, B, T, C, H); count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t attention_backward(DType t, void* dqkv, float* Dbuf, const void* dout,
+                               const void* out, const void* qkv, const float* lse, int B, int T,
+                               int C, int H, cudaStream_t s) {
+  if (t == DType::BF16) {
+    if (C / H != fa::D || C % H) return cudaErrorInvalidValue;
+    long long n = (long long)B * T * H;
+    fa::bwd_D_kernel<<<ceil_div(n, 256), 256, 0, s>>>(Dbuf, (const bf16*)dout, (const bf16*)out,
+                                                      B, T, C, H); count_launches(1);
+    dim3 grid(ceil_div(T, fa::BR), B * H);
+    const int sm = 6 * fa::TILE_BYTES;
+    static bool attr = false;
+    if (!attr) {
+      cudaFuncSetAttribute(fa::bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+      cudaFuncSetAttribute(fa::bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+      attr = true;
+    }
+    fa::bwd_dkv_kernel<<<grid, fa::THREADS, sm, s>>>((bf16*)dqkv, Dbuf, (const bf16*)dout,
+                                                     (const bf16*)qkv, lse, T, C, H); count_launches(1);
+    fa::bwd_dq_kernel<<<grid, fa::THREADS, sm, s>>>((bf16*)dqkv, Dbuf, (const bf16*)dout,
+                                                    (const bf16*)qkv, lse, T, C, H); count_launches(1);
+    return cudaGetLastError();
+  }
+  long long warps = (long long)B * H * T;
+  int blocks = ceil_div(warps, 4);
+  attn_bwd_D_f32_kernel<<<blocks, 128, 0, s>>>(Dbuf, (const float*)dout, (const float*)out, B, T,
+                                               C, H); count_launches(1);
+  attn_bwd_dq_f32_kernel<<<blocks, 128, 4 * T * sizeof(float), s>>>(
+      (float*)dqkv, Dbuf, (const float*)dout, (const float*)qkv, lse, B, T, C, H); count_launches(1);
+  attn_bwd_dkv_f32_kernel<<<blocks, 128, 8 * T * sizeof(float), s>>>(
+      (float*)dqkv, Dbuf, (const float*)dout, (const float*)qkv, lse, B, T, C, H); count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace gpt2k

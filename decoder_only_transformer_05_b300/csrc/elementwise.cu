@@ -1,0 +1,854 @@
+// Memory-bound kernels of the GPT-2 training step: embedding gather and its
+// deterministic scatter-add backward, LayerNorm forward/backward, the fused
+// softmax-cross-entropy classifier, bias-gradient column sums, split-K reduction,
+// global gradient norm and AdamW.
+//
+// Every reduction runs in a fixed order (fixed partitions, fixed combine order), so two
+// runs on the same inputs give bit-identical results.
+#include "common.cuh"
+#include "launch.h"
+
+namespace gpt2k {
+
+static inline cudaError_t last() { return cudaGetLastError(); }
+
+long long& launch_counter() {
+  static long long n = 0;
+  return n;
+}
+
+// =====================================================================================
+// Embedding: x[b, t] = wte[tok[b, t]] + wpe[t]
+// (「从零实现一个最小GPT：代码讲解 + 知识点全解」 二.7 MiniGPT.forward, step 1)
+template <typename T>
+__global__ void encoder_fwd_kernel(T* __restrict__ x, const int* __restrict__ tokens,
+                                   const T* __restrict__ wte, const T* __restrict__ wpe,
+                                   int M, int T_, int C, int V, int* err) {
+  constexpr int VE = 16 / sizeof(T);
+  const int vpr = C / VE;
+  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)M * vpr) return;
+  int p = (int)(i / vpr);
+  int c = (int)(i % vpr) * VE;
+  int tok = tokens[p];
+  if (tok < 0 || tok >= V) {
+    atomicOr(err, DEV_ERR_BAD_TOKEN);
+    tok = tok < 0 ? 0 : V - 1;
+  }
+  int t = p % T_;
+  Vec16<T> a = ld16(wte + (size_t)tok * C + c);
+  Vec16<T> b = ld16(wpe + (size_t)t * C + c);
+  Vec16<T> o;
+#pragma unroll
+  for (int e = 0; e < VE; ++e) o.e[e] = from_f32<T>(to_f32(a.e[e]) + to_f32(b.e[e]));
+  st16(x + (size_t)p * C + c, o);
+}
+
+cudaError_t encoder_forward(DType t, void* x, const int* tokens, const void* wte, const void* wpe,
+                            int B, int T_, int C, int V, int* err, cudaStream_t s) {
+  int M = B * T_;
+  if (t == DType::BF16) {
+    long long n = (long long)M * (C / 8);
+    encoder_fwd_kernel<bf16><<<ceil_div(n, 256), 256, 0, s>>>(
+        (bf16*)x, tokens, (const bf16*)wte, (const bf16*)wpe, M, T_, C, V, err); count_launches(1);
+  } else {
+    long long n = (long long)M * (C / 4);
+    encoder_fwd_kernel<float><<<ceil_div(n, 256), 256, 0, s>>>(
+        (float*)x, tokens, (const float*)wte, (const float*)wpe, M, T_, C, V, err); count_launches(1);
+  }
+  return last();
+}
+
+// -------------------------------------------------------------------------------------
+// Embedding backward.
+// Stage 1 (one block): stable LSD radix sort of the positions by token id, 8 bits per
+// pass. Each warp owns a contiguous slice of positions; within a warp, equal digits are
+// ranked by lane order (match.any), across warps by warp order, so the sort is stable
+// and the result does not depend on scheduling. Then segment starts (first position of
+// each distinct id) are found with a block scan.
+// Stage 2 (one block per segment): the rows of one id are summed in position order
+// (each warp a fixed contiguous share of the rows, warps combined in warp order) and
+// added, times scale, to dwte[id].
+// Stage 3: dwpe[t] += scale * sum_b dx[b, t], b in increasing order.
+constexpr int SORT_THREADS = 1024;
+constexpr int SORT_WARPS = SORT_THREADS / 32;
+
+struct EncScratch {
+  int* key0; int* pos0; int* key1; int* pos1; int* seg_start; int* nseg;
+};
+static EncScratch enc_scratch(void* base, int M) {
+  char* p = (char*)base;
+  auto take = [&](size_t bytes) { char* r = p; p += (bytes + 255) / 256 * 256; return (int*)r; };
+  EncScratch s;
+  s.key0 = take(sizeof(int) * M); s.pos0 = take(sizeof(int) * M);
+  s.key1 = take(sizeof(int) * M); s.pos1 = take(sizeof(int) * M);
+  s.seg_start = take(sizeof(int) * (M + 1)); s.nseg = take(sizeof(int) * 4);
+  return s;
+}
+size_t encoder_backward_scratch_bytes(int M, int Vp) {
+  (void)Vp;
+  size_t a = ((size_t)M * 4 + 255) / 256 * 256;
+  size_t b = ((size_t)(M + 1) * 4 + 255) / 256 * 256;
+  return 4 * a + b + 256;
+}
+
+// Exclusive scan of one int per thread over the block; returns the total in *total.
+__device__ int block_exclusive_scan(int v, int* sh, int* total) {
+  int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int s = lane < (int)(blockDim.x >> 5) ? sh[lane] : 0;
+    int xs = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, xs, o);
+      if (lane >= o) xs += y;
+    }
+    sh[lane] = xs - s;           // exclusive prefix of warp totals
+    if (lane == 31) sh[32] = xs; // block total
+  }
+  __syncthreads();
+  int r = sh[w] + x - v;
+  *total = sh[32];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(SORT_THREADS, 1)
+encoder_sort_kernel(const int* __restrict__ tokens, int M, int Vp, EncScratch sc) {
+  __shared__ int hist[256][SORT_WARPS + 1];
+  __shared__ int scan_sh[40];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int per_warp = (M + SORT_WARPS - 1) / SORT_WARPS;
+  const int lo = min(M, w * per_warp), hi = min(M, lo + per_warp);
+  // load keys (clamped ids) and positions
+  for (int i = threadIdx.x; i < M; i += blockDim.x) {
+    int t = tokens[i];
+    t = t < 0 ? 0 : (t >= Vp ? Vp - 1 : t);
+    sc.key0[i] = t;
+    sc.pos0[i] = i;
+  }
+  __syncthreads();
+  int bits = 0;
+  while ((1 << bits) < Vp) bits += 8;
+  int* kin = sc.key0; int* pin = sc.pos0; int* kout = sc.key1; int* pout = sc.pos1;
+  for (int shift = 0; shift < bits; shift += 8) {
+    for (int i = threadIdx.x; i < 256 * (SORT_WARPS + 1); i += blockDim.x)
+      (&hist[0][0])[i] = 0;
+    __syncthreads();
+    // per-warp digit counts
+    for (int base = lo; base < hi; base += 32) {
+      int i = base + lane;
+      bool valid = i < hi;
+      int d = valid ? (kin[i] >> shift) & 255 : -1 - lane;
+      unsigned peers = __match_any_sync(0xffffffffu, d);
+      if (valid && lane == __ffs(peers) - 1) hist[d][w] += __popc(peers);
+      __syncwarp();
+    }
+    __syncthreads();
+    // exclusive offsets in (digit, warp) order: each thread owns 8 (digit, warp) cells
+    {
+      const int cells = 256 * SORT_WARPS;   // 8192
+      const int per = cells / SORT_THREADS; // 8
+      int c0 = threadIdx.x * per;
+      int local = 0;
+      for (int j = 0; j < per; ++j) { int c = c0 + j; local += hist[c / SORT_WARPS][c % SORT_WARPS]; }
+      int total;
+      int run = block_exclusive_scan(local, scan_sh, &total);
+      for (int j = 0; j < per; ++j) {
+        int c = c0 + j;
+        int v = hist[c / SORT_WARPS][c % SORT_WARPS];
+        hist[c / SORT_WARPS][c % SORT_WARPS] = run;
+        run += v;
+      }
+    }
+    __syncthreads();
+    // stable scatter
+    for (int base = lo; base < hi; base += 32) {
+      int i = base + lane;
+      bool valid = i < hi;
+      int k = valid ? kin[i] : 0;
+      int d = valid ? (k >> shift) & 255 : -1 - lane;
+      unsigned peers = __match_any_sync(0xffffffffu, d);
+      int leader = __ffs(peers) - 1;
+      int basepos = valid ? hist[d][w] : 0;
+      int rank = __popc(peers & ((1u << lane) - 1u));
+      if (valid) { kout[basepos + rank] = k; pout[basepos + rank] = pin[i]; }
+      __syncwarp();
+      if (valid && lane == leader) hist[d][w] = basepos + __popc(peers);
+      __syncwarp();
+    }
+    __syncthreads();
+    int* t0 = kin; kin = kout; kout = t0;
+    int* t1 = pin; pin = pout; pout = t1;
+  }
+  // sorted keys/positions are now in kin/pin; make sure they sit in key0/pos0
+  if (kin != sc.key0) {
+    for (int i = threadIdx.x; i < M; i += blockDim.x) { sc.key0[i] = kin[i]; sc.pos0[i] = pin[i]; }
+    __syncthreads();
+  }
+  // segment starts: i where key changes
+  int nseg_total = 0;
+  for (int base = 0; base < M; base += blockDim.x) {
+    int i = base + threadIdx.x;
+    int flag = (i < M) && (i == 0 || sc.key0[i] != sc.key0[i - 1]);
+    int total;
+    int off = block_exclusive_scan(flag, scan_sh, &total);
+    if (flag) sc.seg_start[nseg_total + off] = i;
+    nseg_total += total;
+  }
+  if (threadIdx.x == 0) { sc.seg_start[nseg_total] = M; sc.nseg[0] = nseg_total; }
+}
+
+template <typename T, int MAXV>
+__global__ void __launch_bounds__(256)
+encoder_segsum_kernel(float* __restrict__ dwte, const T* __restrict__ dx, int C, float scale,
+                      EncScratch sc) {
+  constexpr int VE = 16 / sizeof(T);
+  __shared__ float part[MAXV * 32 * VE];   // warps' partial rows, combined in warp order
+  const int seg = blockIdx.x;
+  if (seg >= sc.nseg[0]) return;
+  const int start = sc.seg_start[seg], end = sc.seg_start[seg + 1];
+  const int id = sc.key0[start];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int n = end - start;
+  const int per = (n + 7) / 8;
+  const int r0 = start + min(n, w * per), r1 = start + min(n, (w + 1) * per);
+  float acc[MAXV][VE];
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j)
+#pragma unroll
+    for (int e = 0; e < VE; ++e) acc[j][e] = 0.f;
+  for (int r = r0; r < r1; ++r) {
+    const T* row = dx + (size_t)sc.pos0[r] * C;
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+      int c = (j * 32 + lane) * VE;
+      if (c < C) {
+        Vec16<T> v = ld16(row + c);
+#pragma unroll
+        for (int e = 0; e < VE; ++e) acc[j][e] += to_f32(v.e[e]);
+      }
+    }
+  }
+  for (int k = 0; k < 8; ++k) {
+    if (w == k) {
+#pragma unroll
+      for (int j = 0; j < MAXV; ++j)
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          int c = (j * 32 + lane) * VE + e;
+          part[c] = (k == 0 ? 0.f : part[c]) + acc[j][e];
+        }
+    }
+    __syncthreads();
+  }
+  for (int c = threadIdx.x; c < C; c += blockDim.x)
+    dwte[(size_t)id * C + c] += scale * part[c];
+}
+
+template <typename T>
+__global__ void encoder_wpe_kernel(float* __restrict__ dwpe, const T* __restrict__ dx, int B,
+                                   int T_, int C, float scale) {
+  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)T_ * C) return;
+  float s = 0.f;
+  for (int b = 0; b < B; ++b) s += to_f32(dx[(size_t)b * T_ * C + i]);
+  dwpe[i] += scale * s;
+}
+
+cudaError_t encoder_backward(DType t, float* dwte, float* dwpe, const void* dx, const int* tokens,
+                             int B, int T_, int C, int Vp, float scale, void* scratch,
+                             cudaStream_t s) {
+  int M = B * T_;
+  EncScratch sc = enc_scratch(scratch, M);
+  encoder_sort_kernel<<<1, SORT_THREADS, 0, s>>>(tokens, M, Vp, sc); count_launches(1);
+  if (t == DType::BF16) {
+    if (C > 2048 || C % 8) return cudaErrorInvalidValue;
+    if (C <= 256) { encoder_segsum_kernel<bf16, 1><<<M, 256, 0, s>>>(dwte, (const bf16*)dx, C, scale, sc); count_launches(1); }
+    else if (C <= 512) { encoder_segsum_kernel<bf16, 2><<<M, 256, 0, s>>>(dwte, (const bf16*)dx, C, scale, sc); count_launches(1); }
+    else if (C <= 1024) { encoder_segsum_kernel<bf16, 4><<<M, 256, 0, s>>>(dwte, (const bf16*)dx, C, scale, sc); count_launches(1); }
+    else { encoder_segsum_kernel<bf16, 8><<<M, 256, 0, s>>>(dwte, (const bf16*)dx, C, scale, sc); count_launches(1); }
+    encoder_wpe_kernel<bf16><<<ceil_div((long long)T_ * C, 256), 256, 0, s>>>(dwpe, (const bf16*)dx, B, T_, C, scale); count_launches(1);
+  } else {
+    if (C > 1024 || C % 4) return cudaErrorInvalidValue;
+    if (C <= 128) { encoder_segsum_kernel<float, 1><<<M, 256, 0, s>>>(dwte, (const float*)dx, C, scale, sc); count_launches(1); }
+    else if (C <= 256) { encoder_segsum_kernel<float, 2><<<M, 256, 0, s>>>(dwte, (const float*)dx, C, scale, sc); count_launches(1); }
+    else if (C <= 512) { encoder_segsum_kernel<float, 4><<<M, 256, 0, s>>>(dwte, (const float*)dx, C, scale, sc); count_launches(1); }
+    else { encoder_segsum_kernel<float, 8><<<M, 256, 0, s>>>(dwte, (const float*)dx, C, scale, sc); count_launches(1); }
+    encoder_wpe_kernel<float><<<ceil_div((long long)T_ * C, 256), 256, 0, s>>>(dwpe, (const float*)dx, B, T_, C, scale); count_launches(1);
+  }
+  return last();
+}
+
+// =====================================================================================
+// LayerNorm forward: y = (x - mean) * rstd * w + b, biased variance, eps 1e-5.
+// One warp per row; the row stays in registers (MAXV 16-byte vectors per lane).
+template <typename T, int MAXV>
+__global__ void ln_fwd_kernel(T* __restrict__ y, float* __restrict__ mean, float* __restrict__ rstd,
+                              const T* __restrict__ x, const T* __restrict__ w,
+                              const T* __restrict__ b, int M, int C) {
+  constexpr int VE = 16 / sizeof(T);
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const T* xr = x + (size_t)row * C;
+  float v[MAXV][VE];
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    int c = (j * 32 + lane) * VE;
+    if (c < C) {
+      Vec16<T> a = ld16(xr + c);
+#pragma unroll
+      for (int e = 0; e < VE; ++e) { v[j][e] = to_f32(a.e[e]); s += v[j][e]; }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VE; ++e) v[j][e] = 0.f;
+    }
+  }
+  const float mu = warp_sum(s) / C;
+  float q = 0.f;
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    int c = (j * 32 + lane) * VE;
+    if (c < C) {
+#pragma unroll
+      for (int e = 0; e < VE; ++e) { float d = v[j][e] - mu; q += d * d; }
+    }
+  }
+  const float rs = rsqrtf(warp_sum(q) / C + 1e-5f);
+  T* yr = y + (size_t)row * C;
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    int c = (j * 32 + lane) * VE;
+    if (c < C) {
+      Vec16<T> wv = ld16(w + c), bv = ld16(b + c), o;
+#pragma unroll
+      for (int e = 0; e < VE; ++e)
+        o.e[e] = from_f32<T>((v[j][e] - mu) * rs * to_f32(wv.e[e]) + to_f32(bv.e[e]));
+      st16(yr + c, o);
+    }
+  }
+  if (lane == 0) { mean[row] = mu; rstd[row] = rs; }
+}
+
+template <typename T>
+static cudaError_t ln_fwd_dispatch(T* y, float* mean, float* rstd, const T* x, const T* w,
+                                   const T* b, int M, int C, cudaStream_t s) {
+  constexpr int VE = 16 / sizeof(T);
+  int vpl = ceil_div(C, 32 * VE);
+  dim3 grid(ceil_div(M, 8)), block(256);
+  switch (vpl) {
+    case 1: ln_fwd_kernel<T, 1><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C); count_launches(1); break;
+    case 2: ln_fwd_kernel<T, 2><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C); count_launches(1); break;
+    case 3: ln_fwd_kernel<T, 3><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C); count_launches(1); break;
+    case 4: ln_fwd_kernel<T, 4><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C); count_launches(1); break;
+    case 5: case 6: ln_fwd_kernel<T, 6><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C); count_launches(1); break;
+    case 7: case 8: ln_fwd_kernel<T, 8><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C); count_launches(1); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return last();
+}
+
+cudaError_t layernorm_forward(DType t, void* y, float* mean, float* rstd, const void* x,
+                              const void* w, const void* b, int M, int C, cudaStream_t s) {
+  if (t == DType::BF16) {
+    if (C % 8) return cudaErrorInvalidValue;
+    return ln_fwd_dispatch<bf16>((bf16*)y, mean, rstd, (const bf16*)x, (const bf16*)w,
+                                 (const bf16*)b, M, C, s);
+  }
+  if (C % 4) return cudaErrorInvalidValue;
+  return ln_fwd_dispatch<float>((float*)y, mean, rstd, (const float*)x, (const float*)w,
+                                (const float*)b, M, C, s);
+}
+
+// -------------------------------------------------------------------------------------
+// LayerNorm backward (「手写训练脚本：不用框架，从零实现GPT训练流程」 二: LayerNorm's
+// backward derived by hand):
+//   xhat = (x - mean) rstd;  g = dy * w
+//   dx = rstd (g - mean(g) - xhat mean(g xhat));  dres = (accumulate ? dres : 0) + dx
+//   dw += sum_rows dy xhat;  db += sum_rows dy
+// Block c handles a fixed contiguous range of rows; its per-column sums go to
+// partials[c] and a second kernel adds them in block order.
+constexpr int LNB_THREADS = 256;
+int layernorm_backward_blocks(int M) { return std::min(ceil_div(M, 32), 2 * 148); }
+
+template <typename T, int MAXV>
+__global__ void __launch_bounds__(LNB_THREADS)
+ln_bwd_kernel(T* __restrict__ dres, int accumulate, float* __restrict__ partials,
+              const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ w,
+              const float* __restrict__ mean, const float* __restrict__ rstd, int M, int C,
+              int rows_per_block) {
+  constexpr int VE = 16 / sizeof(T);
+  constexpr int WARPS = LNB_THREADS / 32;
+  extern __shared__ float smem_lnb[];   // [2][C]
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int r_begin = blockIdx.x * rows_per_block;
+  const int r_end = min(M, r_begin + rows_per_block);
+  float dw[MAXV][VE], db[MAXV][VE], wv[MAXV][VE];
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    int c = (j * 32 + lane) * VE;
+#pragma unroll
+    for (int e = 0; e < VE; ++e) { dw[j][e] = 0.f; db[j][e] = 0.f; wv[j][e] = 0.f; }
+    if (c < C) {
+      Vec16<T> a = ld16(w + c);
+#pragma unroll
+      for (int e = 0; e < VE; ++e) wv[j][e] = to_f32(a.e[e]);
+    }
+  }
+  for (int row = r_begin + wid; row < r_end; row += WARPS) {
+    const float mu = mean[row], rs = rstd[row];
+    float g[MAXV][VE], xh[MAXV][VE];
+    float sg = 0.f, sgx = 0.f;
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+      int c = (j * 32 + lane) * VE;
+      if (c < C) {
+        Vec16<T> a = ld16(dy + (size_t)row * C + c), b = ld16(x + (size_t)row * C + c);
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          float d = to_f32(a.e[e]);
+          xh[j][e] = (to_f32(b.e[e]) - mu) * rs;
+          g[j][e] = d * wv[j][e];
+          sg += g[j][e];
+          sgx += g[j][e] * xh[j][e];
+          dw[j][e] += d * xh[j][e];
+          db[j][e] += d;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < VE; ++e) { g[j][e] = 0.f; xh[j][e] = 0.f; }
+      }
+    }
+    const float mg = warp_sum(sg) / C, mgx = warp_sum(sgx) / C;
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+      int c = (j * 32 + lane) * VE;
+      if (c < C) {
+        T* dr = dres + (size_t)row * C + c;
+        Vec16<T> o;
+        if (accumulate) o = ld16(dr);
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          float dx = rs * (g[j][e] - mg - xh[j][e] * mgx);
+          o.e[e] = from_f32<T>((accumulate ? to_f32(o.e[e]) : 0.f) + dx);
+        }
+        st16(dr, o);
+      }
+    }
+  }
+  // combine the warps' column sums in warp order
+  for (int k = 0; k < WARPS; ++k) {
+    if (wid == k) {
+#pragma unroll
+      for (int j = 0; j < MAXV; ++j) {
+        int c = (j * 32 + lane) * VE;
+        if (c < C) {
+#pragma unroll
+          for (int e = 0; e < VE; ++e) {
+            if (k == 0) { smem_lnb[c + e] = dw[j][e]; smem_lnb[C + c + e] = db[j][e]; }
+            else { smem_lnb[c + e] += dw[j][e]; smem_lnb[C + c + e] += db[j][e]; }
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  float* out = partials + (size_t)blockIdx.x * 2 * C;
+  for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) out[c] = smem_lnb[c];
+}
+
+// out0[c] += scale * sum_k partials[k][c], out1[c] += scale * sum_k partials[k][C + c]
+__global__ void column_partials_reduce_kernel(float* __restrict__ out0, float* __restrict__ out1,
+                                              const float* __restrict__ partials, int nparts,
+                                              int C, int stride, float scale) {
+  int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= C) return;
+  float s0 = 0.f, s1 = 0.f;
+  for (int k = 0; k < nparts; ++k) {
+    s0 += partials[(size_t)k * stride + c];
+    if (out1) s1 += partials[(size_t)k * stride + C + c];
+  }
+  out0[c] += scale * s0;
+  if (out1) out1[c] += scale * s1;
+}
+
+template <typename T>
+static cudaError_t ln_bwd_dispatch(T* dres, int acc, float* dw, float* db, const T* dy, const T* x,
+                                   const T* w, const float* mean, const float* rstd, int M, int C,
+                                   float scale, float* partials, cudaStream_t s) {
+  constexpr int VE = 16 / sizeof(T);
+  int blocks = layernorm_backward_blocks(M);
+  int rpb = ceil_div(M, blocks);
+  blocks = ceil_div(M, rpb);
+  size_t sm = sizeof(float) * 2 * C;
+  int vpl = ceil_div(C, 32 * VE);
+  switch (vpl) {
+#define LNB_CASE(N)                                                                           \
+  ln_bwd_kernel<T, N><<<blocks, LNB_THREADS, sm, s>>>(dres, acc, partials, dy, x, w, mean,   \
+                                                      rstd, M, C, rpb); count_launches(1);  \
+  break;
+    case 1: LNB_CASE(1)
+    case 2: LNB_CASE(2)
+    case 3: LNB_CASE(3)
+    case 4: LNB_CASE(4)
+    case 5: case 6: LNB_CASE(6)
+    case 7: case 8: LNB_CASE(8)
+#undef LNB_CASE
+    default: return cudaErrorInvalidValue;
+  }
+  column_partials_reduce_kernel<<<ceil_div(C, 256), 256, 0, s>>>(dw, db, partials, blocks, C,
+                                                                  2 * C, scale); count_launches(1);
+  return last();
+}
+
+cudaError_t layernorm_backward(DType t, void* dres, int accumulate, float* dw, float* db,
+                               const void* dy, const void* x, const void* w, const float* mean,
+                               const float* rstd, int M, int C, float scale, float* partials,
+                               cudaStream_t s) {
+  if (t == DType::BF16)
+    return ln_bwd_dispatch<bf16>((bf16*)dres, accumulate, dw, db, (const bf16*)dy,
+                                 (const bf16*)x, (const bf16*)w, mean, rstd, M, C, scale,
+                                 partials, s);
+  return ln_bwd_dispatch<float>((float*)dres, accumulate, dw, db, (const float*)dy,
+                                (const float*)x, (const float*)w, mean, rstd, M, C, scale,
+                                partials, s);
+}
+
+// =====================================================================================
+// Fused classifier (「从零实现一个最小GPT」 二.7 forward step 4, F.cross_entropy with mean
+// reduction): one block per row. Pass 1 reads the row once with a running (max, sum of
+// exp) per thread over the first V columns; the block combines them into lse and the
+// row loss lse - z[y]. Pass 2 re-reads the row (from L2) and writes, in place,
+// dlogits = (exp(z - lse) - [v == y]) / M, and 0 in the padded columns [V, Vp).
+constexpr int CLS_THREADS = 512;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+__device__ __forceinline__ void online_merge(float& m, float& s, float m2, float s2) {
+  float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) return;
+  s = s * fast_exp2(m - mn) + s2 * fast_exp2(m2 - mn);
+  m = mn;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(CLS_THREADS)
+classifier_kernel(T* __restrict__ logits, float* __restrict__ losses,
+                  const int* __restrict__ targets, int V, int Vp, float inv_M, int* err) {
+  constexpr int VE = 16 / sizeof(T);
+  __shared__ float sm_m[CLS_THREADS / 32], sm_s[CLS_THREADS / 32];
+  __shared__ float sh_lse;
+  const int row = blockIdx.x;
+  T* z = logits + (size_t)row * Vp;
+  int y = targets[row];
+  if (y < 0 || y >= V) {
+    if (threadIdx.x == 0) atomicOr(err, DEV_ERR_BAD_TARGET);
+    y = y < 0 ? 0 : V - 1;
+  }
+  // pass 1 (log2 domain): running max m and sum s of 2^(z*log2e - m)
+  float m = -INFINITY, s = 0.f;
+  const int nvec = Vp / VE;
+  for (int i = threadIdx.x; i < nvec; i += CLS_THREADS) {
+    Vec16<T> v = ld16(z + (size_t)i * VE);
+    float a[VE];
+    float lm = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < VE; ++e) {
+      a[e] = (i * VE + e < V) ? to_f32(v.e[e]) * LOG2E : -INFINITY;
+      lm = fmaxf(lm, a[e]);
+    }
+    if (lm == -INFINITY) continue;
+    float ls = 0.f;
+#pragma unroll
+    for (int e = 0; e < VE; ++e) ls += fast_exp2(a[e] - lm);
+    online_merge(m, s, lm, ls);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    online_merge(m, s, m2, s2);
+  }
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (lane == 0) { sm_m[wid] = m; sm_s[wid] = s; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M0 = sm_m[0], S0 = sm_s[0];
+    for (int k = 1; k < CLS_THREADS / 32; ++k) online_merge(M0, S0, sm_m[k], sm_s[k]);
+    float lse2 = M0 + __log2f(S0);     // log2-domain lse
+    sh_lse = lse2;
+    losses[row] = lse2 * LN2 - to_f32(z[y]);
+  }
+  __syncthreads();
+  const float lse2 = sh_lse;
+  for (int i = threadIdx.x; i < nvec; i += CLS_THREADS) {
+    Vec16<T> v = ld16(z + (size_t)i * VE), o;
+#pragma unroll
+    for (int e = 0; e < VE; ++e) {
+      int col = i * VE + e;
+      float d = 0.f;
+      if (col < V) {
+        d = fast_exp2(to_f32(v.e[e]) * LOG2E - lse2);
+        if (col == y) d -= 1.0f;
+        d *= inv_M;
+      }
+      o.e[e] = from_f32<T>(d);
+    }
+    st16_cs(z + (size_t)i * VE, o);
+  }
+}
+
+cudaError_t classifier(DType t, void* logits, float* losses, const int* targets, int M, int V,
+                       int Vp, int* err, cudaStream_t s) {
+  float inv = 1.0f / (float)M;
+  if (t == DType::BF16)
+    classifier_kernel<bf16><<<M, CLS_THREADS, 0, s>>>((bf16*)logits, losses, targets, V, Vp, inv, err);
+  else
+    classifier_kernel<float><<<M, CLS_THREADS, 0, s>>>((float*)logits, losses, targets, V, Vp, inv, err);
+  count_launches(1);
+  return last();
+}
+
+__global__ void mean_loss_kernel(float* out, const float* __restrict__ losses, int M) {
+  __shared__ double sh[1024];
+  double a = 0.0;
+  for (int i = threadIdx.x; i < M; i += blockDim.x) a += (double)losses[i];
+  sh[threadIdx.x] = a;
+  __syncthreads();
+  for (int o = blockDim.x / 2; o > 0; o >>= 1) {
+    if ((int)threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) out[0] = (float)(sh[0] / M);
+}
+
+cudaError_t mean_loss(float* loss_out, const float* losses, int M, cudaStream_t s) {
+  mean_loss_kernel<<<1, 1024, 0, s>>>(loss_out, losses, M); count_launches(1);
+  return last();
+}
+
+template <typename T>
+__global__ void argmax_kernel(int* out, const T* __restrict__ logits, int V, int Vp) {
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  const T* z = logits + (size_t)blockIdx.x * Vp;
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int c = threadIdx.x; c < V; c += blockDim.x) {
+    float v = to_f32(z[c]);
+    if (v > best) { best = v; bi = c; }   // c increases per thread: first max kept
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float v2 = __shfl_xor_sync(0xffffffffu, best, o);
+    int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (v2 > best || (v2 == best && i2 < bi)) { best = v2; bi = i2; }
+  }
+  int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (lane == 0) { sv[w] = best; si[w] = bi; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int k = 1; k < (int)(blockDim.x >> 5); ++k)
+      if (sv[k] > best || (sv[k] == best && si[k] < bi)) { best = sv[k]; bi = si[k]; }
+    out[blockIdx.x] = bi;
+  }
+}
+
+cudaError_t argmax_rows(DType t, int* out, const void* logits, int M, int V, int Vp,
+                        cudaStream_t s) {
+  if (t == DType::BF16) { argmax_kernel<bf16><<<M, 256, 0, s>>>(out, (const bf16*)logits, V, Vp); count_launches(1); }
+  else { argmax_kernel<float><<<M, 256, 0, s>>>(out, (const float*)logits, V, Vp); count_launches(1); }
+  return last();
+}
+
+// =====================================================================================
+// Bias gradient: db[n] += scale * sum_m dy[m, n]. Block (x, y) sums the rows of chunk y
+// for one strip of columns; the chunk sums are added in chunk order.
+constexpr int COLSUM_THREADS = 128;
+int colsum_blocks(int M) { return std::min(ceil_div(M, 64), 192); }
+
+template <typename T>
+__global__ void __launch_bounds__(COLSUM_THREADS)
+colsum_kernel(float* __restrict__ partials, const T* __restrict__ dy, int M, int N, int rpc) {
+  constexpr int VE = 16 / sizeof(T);
+  int c = (blockIdx.x * COLSUM_THREADS + threadIdx.x) * VE;
+  if (c >= N) return;
+  int r0 = blockIdx.y * rpc, r1 = min(M, r0 + rpc);
+  float acc[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) acc[e] = 0.f;
+  int r = r0;
+  for (; r + 4 <= r1; r += 4) {
+    Vec16<T> v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = ld16(dy + (size_t)(r + u) * N + c);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int e = 0; e < VE; ++e) acc[e] += to_f32(v[u].e[e]);
+  }
+  for (; r < r1; ++r) {
+    Vec16<T> v = ld16(dy + (size_t)r * N + c);
+#pragma unroll
+    for (int e = 0; e < VE; ++e) acc[e] += to_f32(v.e[e]);
+  }
+  float* out = partials + (size_t)blockIdx.y * N + c;
+#pragma unroll
+  for (int e = 0; e < VE; ++e) out[e] = acc[e];
+}
+
+cudaError_t bias_grad(DType t, float* db, const void* dy, int M, int N, float scale,
+                      float* partials, cudaStream_t s) {
+  int chunks = colsum_blocks(M);
+  int rpc = ceil_div(M, chunks);
+  chunks = ceil_div(M, rpc);
+  if (t == DType::BF16) {
+    dim3 grid(ceil_div(N, COLSUM_THREADS * 8), chunks);
+    colsum_kernel<bf16><<<grid, COLSUM_THREADS, 0, s>>>(partials, (const bf16*)dy, M, N, rpc); count_launches(1);
+  } else {
+    dim3 grid(ceil_div(N, COLSUM_THREADS * 4), chunks);
+    colsum_kernel<float><<<grid, COLSUM_THREADS, 0, s>>>(partials, (const float*)dy, M, N, rpc); count_launches(1);
+  }
+  column_partials_reduce_kernel<<<ceil_div(N, 256), 256, 0, s>>>(db, nullptr, partials, chunks, N,
+                                                                  N, scale); count_launches(1);
+  return last();
+}
+
+// =====================================================================================
+__global__ void splitk_reduce_kernel(float* __restrict__ accum, const float* __restrict__ ws,
+                                     int splits, long long n4, long long n, float scale) {
+  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  float4 a = reinterpret_cast<float4*>(accum)[i];
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < splits; ++k) {
+    float4 w = reinterpret_cast<const float4*>(ws + (size_t)k * n)[i];
+    s.x += w.x; s.y += w.y; s.z += w.z; s.w += w.w;
+  }
+  a.x += scale * s.x; a.y += scale * s.y; a.z += scale * s.z; a.w += scale * s.w;
+  reinterpret_cast<float4*>(accum)[i] = a;
+}
+
+cudaError_t splitk_reduce(float* accum, const float* ws, int splits, long long n, float scale,
+                          cudaStream_t s) {
+  if (n % 4) return cudaErrorInvalidValue;
+  long long n4 = n / 4;
+  splitk_reduce_kernel<<<ceil_div(n4, 256), 256, 0, s>>>(accum, ws, splits, n4, n, scale); count_launches(1);
+  return last();
+}
+
+// =====================================================================================
+// Global gradient norm and clip coefficient, on device (no host sync):
+// out[0] = ||g||_2, out[1] = max_norm > 0 ? min(1, max_norm / (||g|| + 1e-6)) : 1.
+constexpr int NORM_BLOCKS = 592;   // 4 x 148 SMs
+int norm_partials_count() { return NORM_BLOCKS; }
+
+__global__ void __launch_bounds__(256)
+sumsq_kernel(float* __restrict__ partials, const float* __restrict__ g, long long n) {
+  __shared__ float sh[8];
+  long long n4 = n / 4;
+  long long per = (n4 + gridDim.x - 1) / gridDim.x;
+  long long b0 = blockIdx.x * per, b1 = min(n4, b0 + per);
+  float a = 0.f;
+  for (long long i = b0 + threadIdx.x; i < b1; i += blockDim.x) {
+    float4 v = __ldcs(reinterpret_cast<const float4*>(g) + i);
+    a += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  if (blockIdx.x == gridDim.x - 1)
+    for (long long i = n4 * 4 + threadIdx.x; i < n; i += blockDim.x) a += g[i] * g[i];
+  a = warp_sum(a);
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int k = 0; k < 8; ++k) t += sh[k];
+    partials[blockIdx.x] = t;
+  }
+}
+
+__global__ void norm_finish_kernel(float* out, const float* __restrict__ partials, int np,
+                                   float max_norm) {
+  if (threadIdx.x != 0) return;
+  double s = 0.0;
+  for (int k = 0; k < np; ++k) s += (double)partials[k];
+  float nrm = (float)sqrt(s);
+  out[0] = nrm;
+  out[1] = max_norm > 0.f ? fminf(1.0f, max_norm / (nrm + 1e-6f)) : 1.0f;
+}
+
+cudaError_t grad_norm(float* out, float* partials, const float* g, long long n, float max_norm,
+                      cudaStream_t s) {
+  sumsq_kernel<<<NORM_BLOCKS, 256, 0, s>>>(partials, g, n); count_launches(1);
+  norm_finish_kernel<<<1, 32, 0, s>>>(out, partials, NORM_BLOCKS, max_norm); count_launches(1);
+  return last();
+}
+
+// AdamW, decoupled weight decay (「从零实现一个最小GPT」 三.9), PyTorch's formulation:
+// p *= 1 - lr wd; m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2;
+// p -= lr (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps)
+__global__ void __launch_bounds__(256)
+adamw_kernel(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
+             float* __restrict__ v, bf16* __restrict__ pb, long long n4, float lr, float b1,
+             float b2, float eps, float decay, float inv_bc1, float inv_bc2,
+             const float* __restrict__ coef) {
+  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const float c = coef ? coef[1] : 1.0f;
+  float4 pp = reinterpret_cast<float4*>(p)[i];
+  float4 gg = __ldcs(reinterpret_cast<const float4*>(g) + i);
+  float4 mm = reinterpret_cast<float4*>(m)[i];
+  float4 vv = reinterpret_cast<float4*>(v)[i];
+  float* P = &pp.x; float* G = &gg.x; float* Mv = &mm.x; float* Vv = &vv.x;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float gr = G[e] * c;
+    Mv[e] = b1 * Mv[e] + (1.0f - b1) * gr;
+    Vv[e] = b2 * Vv[e] + (1.0f - b2) * gr * gr;
+    float pv = P[e] * decay;
+    P[e] = pv - lr * (Mv[e] * inv_bc1) / (sqrtf(Vv[e] * inv_bc2) + eps);
+  }
+  reinterpret_cast<float4*>(p)[i] = pp;
+  reinterpret_cast<float4*>(m)[i] = mm;
+  reinterpret_cast<float4*>(v)[i] = vv;
+  if (pb) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(pp.x, pp.y), hi = __floats2bfloat162_rn(pp.z, pp.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(pb)[i] = u;
+  }
+}
+
+cudaError_t adamw(float* p, const float* g, float* m, float* v, void* p_bf16, long long n,
+                  float lr, float beta1, float beta2, float eps, float weight_decay, int t,
+                  const float* coef, cudaStream_t s) {
+  if (n % 4) return cudaErrorInvalidValue;
+  double bc1 = 1.0 - pow((double)beta1, (double)t), bc2 = 1.0 - pow((double)beta2, (double)t);
+  long long n4 = n / 4;
+  adamw_kernel<<<ceil_div(n4, 256), 256, 0, s>>>(p, g, m, v, (bf16*)p_bf16, n4, lr, beta1, beta2,
+                                                 eps, 1.0f - lr * weight_decay,
+                                                 (float)(1.0 / bc1), (float)(1.0 / bc2), coef); count_launches(1);
+  return last();
+}
+
+__global__ void to_bf16_kernel(bf16* __restrict__ dst, const float* __restrict__ src, long long n) {
+  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) dst[i] = __float2bfloat16_rn(src[i]);
+}
+
+cudaError_t to_bf16(void* dst, const float* src, long long n, cudaStream_t s) {
+  to_bf16_kernel<<<ceil_div(n, 256), 256, 0, s>>>((bf16*)dst, src, n); count_launches(1);
+  return last();
+}
+
+}  // namespace gpt2k

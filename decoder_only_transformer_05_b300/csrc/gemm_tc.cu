@@ -1,0 +1,515 @@
+// bf16 GEMM on the 5th-generation tensor cores (tcgen05) for sm_103a, with the training
+// step's fused epilogues (bias, residual add, tanh-GELU and its derivative, fp32
+// gradient accumulation).
+//
+// C(m, n) = sum_k A(m, k) B(n, k); each operand is K-major (k contiguous) or MN-major
+// (m or n contiguous). Forward GEMMs are K-major x K-major, dgrad GEMMs K-major x
+// MN-major, wgrad GEMMs MN-major x MN-major.
+//
+// Structure (one persistent block of 192 threads per SM):
+//   warp 0      TMA producer: 128x64 A and BNx64 B tiles, 128-byte swizzle, into a
+//               ring of shared-memory stages (mbarrier full/empty handshake)
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN, K=16) into a
+//               fp32 accumulator in tensor memory; two accumulators alternate so the
+//               epilogue of one tile overlaps the main loop of the next
+//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time (each warp owns the 32 TMEM
+//               lanes = rows its warp index selects), apply the epilogue, store
+// Every mbarrier wait is bounded: on timeout the block records DEV_ERR_TIMEOUT, stops
+// issuing work, waits for its own copies and MMAs and frees its tensor memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace gpt2k {
+namespace tc {
+
+constexpr int BM = 128, BK = 64;
+constexpr int THREADS = 192;
+constexpr unsigned long long TIMEOUT_NS = 2000000000ull;   // 2 s per wait
+
+template <int BN> struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;   // 16 KB
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int TMEM_COLS = 2 * BN;      // two accumulators
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = STAGES * STAGE + 1024 + BAR_BYTES;
+};
+
+struct Params {
+  int M, N, K;
+  int num_m, num_n, splits, kb_per_split, num_kb;
+  int epi;
+  void* out; long long ldo;
+  const bf16* bias; const bf16* resid; bf16* pre; const bf16* aux;
+  float* accum; float scale; float* workspace;
+  int* err;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded wait. Returns false if the block is aborting or this wait timed out.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       int* err, bool honour_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (honour_abort && *abort_flag) return false;
+    if (globaltimer() - t0 > TIMEOUT_NS) {
+      *abort_flag = 1;
+      if (err) atomicOr(err, DEV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"((unsigned long long)map), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+               "r"(ncols));
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+// 32 TMEM lanes x 32 consecutive 32-bit columns; thread i of the warp gets lane base+i.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: 128-byte swizzle, descriptor version 1.
+//   K-major tile: rows of 128 B (64 bf16 of k), 8-row groups 1024 B apart (SBO).
+//   MN-major tile: rows of 128 B (64 bf16 of m or n) per k, 8-k-row groups 1024 B
+//   apart (SBO), 64-wide m/n groups LBO bytes apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, majors, N, M.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ epilogue
+__device__ __forceinline__ void epilogue32(const Params& p, int row, int col0, int split,
+                                           const float (&v)[32]) {
+  const size_t o = (size_t)row * p.ldo + col0;
+  switch (p.epi) {
+    case EPI_STORE: {
+      bf16* out = (bf16*)p.out + o;
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        Vec16<bf16> r, b, w;
+        if (p.resid) r = ld16(p.resid + o + j);
+        if (p.bias) b = ld16(p.bias + col0 + j);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float x = v[j + e];
+          if (p.bias) x += to_f32(b.e[e]);
+          if (p.resid) x += to_f32(r.e[e]);
+          w.e[e] = __float2bfloat16_rn(x);
+        }
+        st16(out + j, w);
+      }
+      break;
+    }
+    case EPI_GELU_FWD: {
+      bf16* out = (bf16*)p.out + o;
+      bf16* pre = p.pre + o;
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        Vec16<bf16> b, u, a;
+        if (p.bias) b = ld16(p.bias + col0 + j);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float x = v[j + e];
+          if (p.bias) x += to_f32(b.e[e]);
+          u.e[e] = __float2bfloat16_rn(x);
+          a.e[e] = __float2bfloat16_rn(gelu_tanh(x));
+        }
+        st16(pre + j, u);
+        st16(out + j, a);
+      }
+      break;
+    }
+    case EPI_GELU_BWD: {
+      bf16* out = (bf16*)p.out + o;
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        Vec16<bf16> u = ld16(p.aux + o + j), w;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w.e[e] = __float2bfloat16_rn(v[j + e] * gelu_tanh_grad(to_f32(u.e[e])));
+        st16(out + j, w);
+      }
+      break;
+    }
+    case EPI_ACCUM: {
+      if (p.splits == 1) {
+        float* a = p.accum + o;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          float4 x = *reinterpret_cast<float4*>(a + j);
+          x.x += p.scale * v[j]; x.y += p.scale * v[j + 1];
+          x.z += p.scale * v[j + 2]; x.w += p.scale * v[j + 3];
+          *reinterpret_cast<float4*>(a + j) = x;
+        }
+      } else {
+        float* w = p.workspace + (size_t)split * p.M * p.N + (size_t)row * p.N + col0;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(w + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+      }
+      break;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int BN, bool AMN, bool BMN>
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+            const Params p) {
+  using Cf = Cfg<BN>;
+  constexpr uint32_t IDESC = make_idesc(BM, BN, AMN, BMN);
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bars = base + Cf::STAGES * Cf::STAGE;
+  uint8_t* bars_ptr = base_ptr + Cf::STAGES * Cf::STAGE;
+  // barrier layout: full[S] empty[S] tfull[2] tempty[2] final, then tmem slot, abort flag
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (Cf::STAGES + s); };
+  auto tfull = [&](int a) { return bars + 8u * (2 * Cf::STAGES + a); };
+  auto tempty = [&](int a) { return bars + 8u * (2 * Cf::STAGES + 2 + a); };
+  const uint32_t final_bar = bars + 8u * (2 * Cf::STAGES + 4);
+  const uint32_t slot = bars + 8u * (2 * Cf::STAGES + 5);
+  volatile uint32_t* slot_ptr = (volatile uint32_t*)(bars_ptr + 8 * (2 * Cf::STAGES + 5));
+  volatile int* abort_flag = (volatile int*)(bars_ptr + 8 * (2 * Cf::STAGES + 6));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cf::STAGES; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), 4); }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(slot, Cf::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *slot_ptr;
+
+  const int tiles = p.num_m * p.num_n * p.splits;
+  auto decode = [&](int tile, int& mb, int& nb, int& sp) {
+    mb = tile % p.num_m;
+    int r = tile / p.num_m;
+    nb = r % p.num_n;
+    sp = r / p.num_n;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+        int mb, nb, sp;
+        decode(tile, mb, nb, sp);
+        const int m0 = mb * BM, n0 = nb * BN;
+        const int kb0 = sp * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % Cf::STAGES;
+          const uint32_t ph = (uint32_t)(it / Cf::STAGES) & 1u;
+          if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          const uint32_t a_dst = base + s * Cf::STAGE, b_dst = a_dst + Cf::A_BYTES;
+          mbar_expect_tx(full(s), Cf::STAGE);
+          if (AMN) {
+            tma_load_2d(a_dst, &tmA, full(s), m0, kb * BK);
+            tma_load_2d(a_dst + 8192, &tmA, full(s), m0 + 64, kb * BK);
+          } else {
+            tma_load_2d(a_dst, &tmA, full(s), kb * BK, m0);
+          }
+          if (BMN) {
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i) tma_load_2d(b_dst + i * 8192, &tmB, full(s), n0 + i * 64, kb * BK);
+          } else {
+            tma_load_2d(b_dst, &tmB, full(s), kb * BK, n0);
+          }
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before the block exits
+        for (int j = max(0, it - Cf::STAGES); j < it; ++j)
+          mbar_wait(full(j % Cf::STAGES), (uint32_t)(j / Cf::STAGES) & 1u, abort_flag, nullptr, false);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      int it = 0, tcount = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++tcount) {
+        int mb, nb, sp;
+        decode(tile, mb, nb, sp);
+        const int kb0 = sp * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+        const int acc = tcount & 1;
+        const uint32_t aph = (uint32_t)(tcount >> 1) & 1u;
+        if (!mbar_wait(tempty(acc), aph ^ 1u, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % Cf::STAGES;
+          const uint32_t ph = (uint32_t)(it / Cf::STAGES) & 1u;
+          if (!mbar_wait(full(s), ph, abort_flag, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_base = base + s * Cf::STAGE, b_base = a_base + Cf::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = AMN ? sdesc(a_base + k * 2048, 8192, 1024)
+                                    : sdesc(a_base + k * 32, 16, 1024);
+            const uint64_t bd = BMN ? sdesc(b_base + k * 2048, 8192, 1024)
+                                    : sdesc(b_base + k * 32, 16, 1024);
+            umma_bf16(d, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+          }
+          umma_commit(empty(s));
+        }
+        if (!ok) break;
+        umma_commit(tfull(acc));
+      }
+      // all issued MMAs complete before tensor memory is released
+      umma_commit(final_bar);
+      mbar_wait(final_bar, 0, abort_flag, nullptr, false);
+    }
+  } else {
+    // ---------------- epilogue warps 2..5; warp % 4 selects the TMEM lane quarter
+    const int q = warp & 3;
+    int tcount = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tcount) {
+      int mb, nb, sp;
+      decode(tile, mb, nb, sp);
+      const int acc = tcount & 1;
+      const uint32_t aph = (uint32_t)(tcount >> 1) & 1u;
+      bool ok = mbar_wait(tfull(acc), aph, abort_flag, p.err);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int row = mb * BM + q * 32 + lane;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = nb * BN + c * 32;
+        if (col0 >= p.N) break;
+        float v[32];
+        tmem_ld32(taddr + c * 32, v);
+        if (row < p.M) epilogue32(p, row, col0, sp, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty(acc));
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cf::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+  });
+  return fn;
+}
+
+// 2-D bf16 map over a row-major matrix: `inner` contiguous elements per row, `outer`
+// rows, `ld` elements between rows; box = box_inner x box_outer, 128-byte swizzle,
+// out-of-range elements read as zero.
+static bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                     uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, bool AMN, bool BMN>
+static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
+  using Cf = Cfg<BN>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, AMN, BMN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  CUtensorMap ma, mb;
+  bool ok = AMN ? make_map(&ma, g.A, g.M, g.K, g.lda, 64, 64)
+                : make_map(&ma, g.A, g.K, g.M, g.lda, 64, BM);
+  ok = ok && (BMN ? make_map(&mb, g.B, g.N, g.K, g.ldb, 64, 64)
+                  : make_map(&mb, g.B, g.K, g.N, g.ldb, 64, BN));
+  if (!ok) return cudaErrorInvalidValue;
+  Params p;
+  p.M = g.M; p.N = g.N; p.K = g.K;
+  p.num_m = ceil_div(g.M, BM);
+  p.num_n = ceil_div(g.N, BN);
+  p.num_kb = g.K / BK;
+  p.splits = (g.epi == EPI_ACCUM && g.splits > 1) ? g.splits : 1;
+  p.kb_per_split = ceil_div(p.num_kb, p.splits);
+  p.splits = ceil_div(p.num_kb, p.kb_per_split);
+  p.epi = g.epi;
+  p.out = g.out; p.ldo = g.ldo;
+  p.bias = (const bf16*)g.bias; p.resid = (const bf16*)g.resid;
+  p.pre = (bf16*)g.pre; p.aux = (const bf16*)g.aux;
+  p.accum = g.accum; p.scale = g.scale; p.workspace = g.workspace;
+  p.err = g.err;
+  if (p.splits > 1 && !g.workspace) return cudaErrorInvalidValue;
+  const int tiles = p.num_m * p.num_n * p.splits;
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  gemm_kernel<BN, AMN, BMN><<<grid, THREADS, Cf::SMEM, s>>>(ma, mb, p); count_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.splits > 1) return splitk_reduce(g.accum, g.workspace, p.splits, (long long)g.M * g.N, g.scale, s);
+  return cudaSuccess;
+}
+
+}  // namespace tc
+
+int gemm_tc_num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+static int pick_bn(int N) { return (N % 256 == 0) ? 256 : 128; }
+
+int gemm_tc_pick_splits(int M, int N, int K, int num_sms) {
+  const int bn = pick_bn(N);
+  const int tiles = ceil_div(M, tc::BM) * ceil_div(N, bn);
+  const int nkb = K / tc::BK;
+  if (tiles >= num_sms) return 1;
+  int s = num_sms / tiles;
+  while (s > 1 && nkb / s < 8) --s;
+  return s < 1 ? 1 : s;
+}
+
+cudaError_t gemm_bf16_tc(const GemmArgs& g, cudaStream_t s) {
+  if (g.M <= 0 || g.N <= 0 || g.K <= 0 || g.N % 64 || g.K % 64) return cudaErrorInvalidValue;
+  const int sms = gemm_tc_num_sms();
+  GemmArgs a = g;
+  if (a.epi == EPI_ACCUM && a.splits <= 0) a.splits = gemm_tc_pick_splits(a.M, a.N, a.K, sms);
+  const int bn = pick_bn(a.N);
+#define GEMM_TC_DISPATCH(BN_)                                                  \
+  if (!a.a_mn && !a.b_mn) return tc::launch<BN_, false, false>(a, sms, s);     \
+  if (!a.a_mn && a.b_mn) return tc::launch<BN_, false, true>(a, sms, s);       \
+  if (a.a_mn && a.b_mn) return tc::launch<BN_, true, true>(a, sms, s);         \
+  return tc::launch<BN_, true, false>(a, sms, s);
+  if (bn == 256) { GEMM_TC_DISPATCH(256) }
+  GEMM_TC_DISPATCH(128)
+#undef GEMM_TC_DISPATCH
+}
+
+}  // namespace gpt2k

@@ -1,0 +1,116 @@
+// Host-side launchers for every kernel of the training step. Each launcher enqueues on
+// `stream`, never synchronises and never allocates; it returns the launch status.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace gpt2k {
+
+// Number of kernels this library has launched (every launcher adds its own count).
+long long& launch_counter();
+inline void count_launches(int n) { launch_counter() += n; }
+
+enum class DType : int { F32 = 0, BF16 = 1 };
+
+// ---------------------------------------------------------------- GEMM
+// C(m, n) = sum_k A(m, k) * B(n, k), with
+//   A(m, k) = a_mn ? A[k * lda + m] : A[m * lda + k]
+//   B(n, k) = b_mn ? B[k * ldb + n] : B[n * ldb + k]
+// and one of these epilogues on the fp32 accumulator v = C(m, n):
+enum GemmEpi : int {
+  EPI_STORE = 0,     // out = v (+ bias[n]) (+ resid[m, n])
+  EPI_GELU_FWD = 1,  // pre = v + bias[n]; out = gelu_tanh(pre)
+  EPI_GELU_BWD = 2,  // out = v * gelu_tanh'(aux[m, n])
+  EPI_ACCUM = 3,     // accum[m, n] += scale * v   (fp32; wgrad into the grad buffer)
+};
+
+struct GemmArgs {
+  int M = 0, N = 0, K = 0;
+  const void* A = nullptr; long long lda = 0; bool a_mn = false;
+  const void* B = nullptr; long long ldb = 0; bool b_mn = false;
+  int epi = EPI_STORE;
+  void* out = nullptr; long long ldo = 0;   // element type = the path's activation type
+  const void* bias = nullptr;               // [N], activation type
+  const void* resid = nullptr;              // [M, ldo]
+  void* pre = nullptr;                      // EPI_GELU_FWD pre-activation [M, ldo]
+  const void* aux = nullptr;                // EPI_GELU_BWD pre-activation [M, ldo]
+  float* accum = nullptr;                   // EPI_ACCUM target [M, ldo] fp32
+  float scale = 1.0f;
+  int splits = 1;                           // EPI_ACCUM split-K count (tensor-core path)
+  float* workspace = nullptr;               // splits * M * N fp32 when splits > 1
+  int* err = nullptr;                       // device error word
+};
+
+// fp32 SIMT GEMM (all operands float).
+cudaError_t gemm_f32(const GemmArgs& g, cudaStream_t s);
+// bf16 tcgen05 GEMM (A, B, out, bias, resid, pre, aux bf16; accum fp32).
+// Needs M, N, K > 0, N % 64 == 0, K % 64 == 0, 16-byte aligned pointers and leading
+// dimensions that are multiples of 8 elements.
+cudaError_t gemm_bf16_tc(const GemmArgs& g, cudaStream_t s);
+// Largest split-K factor gemm_bf16_tc would choose for an EPI_ACCUM call of this shape.
+int gemm_tc_pick_splits(int M, int N, int K, int num_sms);
+// Sum of split-K partials into the fp32 accumulator: accum += scale * sum_s ws[s].
+cudaError_t splitk_reduce(float* accum, const float* ws, int splits, long long n,
+                          float scale, cudaStream_t s);
+int gemm_tc_num_sms();
+
+// ---------------------------------------------------------------- elementwise
+cudaError_t encoder_forward(DType t, void* x, const int* tokens, const void* wte, const void* wpe,
+                            int B, int T, int C, int V, int* err, cudaStream_t s);
+// Deterministic embedding backward: counting sort of positions by token id, then a
+// per-id segmented sum in position order. scratch: encoder_backward_scratch_bytes(M, Vp).
+size_t encoder_backward_scratch_bytes(int M, int Vp);
+cudaError_t encoder_backward(DType t, float* dwte, float* dwpe, const void* dx, const int* tokens,
+                             int B, int T, int C, int Vp, float scale, void* scratch,
+                             cudaStream_t s);
+
+cudaError_t layernorm_forward(DType t, void* y, float* mean, float* rstd, const void* x,
+                              const void* w, const void* b, int M, int C, cudaStream_t s);
+// dres (+)= dx of LayerNorm; dw, db += scale * column sums (two deterministic stages).
+// partials: layernorm_backward_partials(M) * 2 * C floats.
+int layernorm_backward_blocks(int M);
+cudaError_t layernorm_backward(DType t, void* dres, int accumulate, float* dw, float* db,
+                               const void* dy, const void* x, const void* w, const float* mean,
+                               const float* rstd, int M, int C, float scale, float* partials,
+                               cudaStream_t s);
+
+// Fused classifier over the logits rows: per row loss = lse - z[y] over the first V
+// columns; in place, logits become dlogits = (softmax - onehot) / M (0 in pad columns).
+cudaError_t classifier(DType t, void* logits, float* losses, const int* targets, int M, int V,
+                       int Vp, int* err, cudaStream_t s);
+// loss_out[0] = mean(losses[0..M))  (one block, fixed order)
+cudaError_t mean_loss(float* loss_out, const float* losses, int M, cudaStream_t s);
+// argmax over the first V columns of each row (lowest index on ties)
+cudaError_t argmax_rows(DType t, int* out, const void* logits, int M, int V, int Vp,
+                        cudaStream_t s);
+
+// Bias gradient: db[n] += scale * sum_m dy[m, n] (two deterministic stages).
+int colsum_blocks(int M);
+cudaError_t bias_grad(DType t, float* db, const void* dy, int M, int N, float scale,
+                      float* partials, cudaStream_t s);
+
+// ---------------------------------------------------------------- attention
+// qkv [B, T, 3C] -> out [B, T, C], lse [B, H, T] (natural log)
+cudaError_t attention_forward(DType t, void* out, float* lse, const void* qkv, int B, int T, int C,
+                              int H, cudaStream_t s);
+// dout [B, T, C] -> dqkv [B, T, 3C]; Dbuf [B, H, T] scratch
+cudaError_t attention_backward(DType t, void* dqkv, float* Dbuf, const void* dout,
+                               const void* out, const void* qkv, const float* lse, int B, int T,
+                               int C, int H, cudaStream_t s);
+
+// ---------------------------------------------------------------- optimiser
+// partials: norm_partials_count() floats; out[0] = ||g||, out[1] = clip coefficient
+int norm_partials_count();
+cudaError_t grad_norm(float* out, float* partials, const float* g, long long n, float max_norm,
+                      cudaStream_t s);
+// One AdamW step over n elements (t counts from 1). The gradient is multiplied by
+// coef[0] (device, from grad_norm) when coef is non-null. p_bf16 (optional) receives the
+// bf16 copy of the updated parameters.
+cudaError_t adamw(float* p, const float* g, float* m, float* v, void* p_bf16, long long n,
+                  float lr, float beta1, float beta2, float eps, float weight_decay, int t,
+                  const float* coef, cudaStream_t s);
+// dst[i] = bf16(src[i]) (round to nearest even)
+cudaError_t to_bf16(void* dst, const float* src, long long n, cudaStream_t s);
+
+}  // namespace gpt2k

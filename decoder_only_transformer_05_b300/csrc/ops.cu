@@ -1,0 +1,78 @@
+// Single-kernel entry points (include/gpt2_ops.h): thin wrappers over launch.h.
+#include "../../include/gpt2.h"
+#include "../../include/gpt2_ops.h"
+#include "launch.h"
+
+using namespace gpt2k;
+
+static int status(cudaError_t e) {
+  if (e == cudaSuccess) return GPT2_OK;
+  return e == cudaErrorInvalidValue ? GPT2_ERR_ARG : GPT2_ERR_CUDA;
+}
+static DType dtype(int precision) { return precision == GPT2_BF16 ? DType::BF16 : DType::F32; }
+
+extern "C" int gpt2_op_gemm(int precision, int M, int N, int K, const void* A, int64_t lda,
+                            int a_mn, const void* B, int64_t ldb, int b_mn, int epi, void* out,
+                            int64_t ldo, const void* bias, const void* resid, void* pre,
+                            const void* aux, float* accum, float scale, int splits,
+                            float* workspace, size_t workspace_bytes, void* stream) {
+  if (epi < 0 || epi > 3) return GPT2_ERR_ARG;
+  GemmArgs g;
+  g.M = M; g.N = N; g.K = K;
+  g.A = A; g.lda = lda; g.a_mn = a_mn != 0;
+  g.B = B; g.ldb = ldb; g.b_mn = b_mn != 0;
+  g.epi = epi; g.out = out; g.ldo = ldo;
+  g.bias = bias; g.resid = resid; g.pre = pre; g.aux = aux;
+  g.accum = accum; g.scale = scale;
+  g.splits = splits; g.workspace = workspace;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (precision != GPT2_BF16) return status(gemm_f32(g, s));
+  if (epi == EPI_ACCUM) {
+    int sp = splits > 0 ? splits : gemm_tc_pick_splits(M, N, K, gemm_tc_num_sms());
+    if (sp > 1 && (!workspace || workspace_bytes < (size_t)sp * M * N * sizeof(float)))
+      return GPT2_ERR_ARG;
+    g.splits = sp;
+  }
+  return status(gemm_bf16_tc(g, s));
+}
+
+extern "C" int gpt2_op_attention_forward(int precision, void* out, float* lse, const void* qkv,
+                                         int B, int T, int C, int H, void* stream) {
+  return status(attention_forward(dtype(precision), out, lse, qkv, B, T, C, H,
+                                  (cudaStream_t)stream));
+}
+
+extern "C" int gpt2_op_attention_backward(int precision, void* dqkv, float* Dbuf,
+                                          const void* dout, const void* out, const void* qkv,
+                                          const float* lse, int B, int T, int C, int H,
+                                          void* stream) {
+  return status(attention_backward(dtype(precision), dqkv, Dbuf, dout, out, qkv, lse, B, T, C,
+                                   H, (cudaStream_t)stream));
+}
+
+extern "C" int gpt2_op_layernorm_forward(int precision, void* y, float* mean, float* rstd,
+                                         const void* x, const void* w, const void* b, int M,
+                                         int C, void* stream) {
+  return status(layernorm_forward(dtype(precision), y, mean, rstd, x, w, b, M, C,
+                                  (cudaStream_t)stream));
+}
+
+extern "C" size_t gpt2_op_layernorm_partials_floats(int M, int C) {
+  return (size_t)layernorm_backward_blocks(M) * 2 * (size_t)C;
+}
+
+extern "C" int gpt2_op_layernorm_backward(int precision, void* dres, int accumulate, float* dw,
+                                          float* db, const void* dy, const void* x,
+                                          const void* w, const float* mean, const float* rstd,
+                                          int M, int C, float scale, float* partials,
+                                          void* stream) {
+  return status(layernorm_backward(dtype(precision), dres, accumulate, dw, db, dy, x, w, mean,
+                                   rstd, M, C, scale, partials, (cudaStream_t)stream));
+}
+
+extern "C" int gpt2_op_classifier(int precision, void* logits, float* losses,
+                                  const int32_t* targets, int M, int V, int Vp, int* err,
+                                  void* stream) {
+  return status(classifier(dtype(precision), logits, losses, targets, M, V, Vp, err,
+                           (cudaStream_t)stream));
+}

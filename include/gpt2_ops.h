@@ -1,0 +1,74 @@
+/*
+ * gpt2_ops.h — single-kernel entry points of libgpt2, on caller-owned device buffers.
+ * They run exactly the kernels gpt2_forward / gpt2_backward use and exist so that each
+ * step of the training step can be checked on its own. Same conventions as gpt2.h:
+ * int return (GPT2_OK or GPT2_ERR_*), work queued on `stream` (a cudaStream_t, NULL =
+ * legacy default stream), no synchronisation, no allocation. `precision` selects the
+ * element type of the activation operands: GPT2_FP32 (float) or GPT2_BF16 (bf16).
+ */
+#ifndef GPT2_OPS_H
+#define GPT2_OPS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  GPT2_EPI_STORE = 0,    /* out = v (+ bias[n]) (+ resid[m, n]) */
+  GPT2_EPI_GELU_FWD = 1, /* pre = v + bias[n]; out = gelu_tanh(pre) */
+  GPT2_EPI_GELU_BWD = 2, /* out = v * gelu_tanh'(aux[m, n]) */
+  GPT2_EPI_ACCUM = 3     /* accum[m, n] += scale * v (fp32) */
+};
+
+/*
+ * C(m, n) = sum_k A(m, k) B(n, k) for m < M, n < N, k < K, with
+ *   A(m, k) = a_mn ? A[k*lda + m] : A[m*lda + k],  B(n, k) = b_mn ? B[k*ldb + n] : B[n*ldb + k]
+ * followed by the epilogue `epi` on v = C(m, n); outputs are row-major with leading
+ * dimension ldo (out, pre, aux, resid, accum). This is every Linear layer of the model:
+ * forward Y = X W^T (K-major x K-major), dgrad dX = dY W (K-major x MN-major), wgrad
+ * dW += dY^T X (MN-major x MN-major). GPT2_BF16 runs the tcgen05 tensor-core kernel and
+ * needs N % 64 == 0, K % 64 == 0, 16-byte aligned pointers and leading dimensions that
+ * are multiples of 8; GPT2_EPI_ACCUM may then split K (splits = 0: automatic, needs
+ * `workspace` of splits * M * N floats; 1: no split).
+ */
+int gpt2_op_gemm(int precision, int M, int N, int K, const void* A, int64_t lda, int a_mn,
+                 const void* B, int64_t ldb, int b_mn, int epi, void* out, int64_t ldo,
+                 const void* bias, const void* resid, void* pre, const void* aux, float* accum,
+                 float scale, int splits, float* workspace, size_t workspace_bytes,
+                 void* stream);
+
+/* Causal attention over qkv [B, T, 3C] (Q, K, V thirds; head h = columns h*hs..) ->
+   out [B, T, C] (heads concatenated) and lse [B, H, T] fp32 (natural log).
+   GPT2_BF16 needs head size 64. */
+int gpt2_op_attention_forward(int precision, void* out, float* lse, const void* qkv, int B,
+                              int T, int C, int H, void* stream);
+/* dout [B, T, C] -> dqkv [B, T, 3C]; Dbuf is [B, H, T] fp32 scratch. */
+int gpt2_op_attention_backward(int precision, void* dqkv, float* Dbuf, const void* dout,
+                               const void* out, const void* qkv, const float* lse, int B,
+                               int T, int C, int H, void* stream);
+
+/* y = LN(x) over rows of C (biased variance, eps 1e-5); mean, rstd fp32 [M]. */
+int gpt2_op_layernorm_forward(int precision, void* y, float* mean, float* rstd, const void* x,
+                              const void* w, const void* b, int M, int C, void* stream);
+/* dres = (accumulate ? dres : 0) + dx; dw, db += scale * column sums (fp32).
+   partials: gpt2_op_layernorm_partials_floats(M, C) floats of scratch. */
+size_t gpt2_op_layernorm_partials_floats(int M, int C);
+int gpt2_op_layernorm_backward(int precision, void* dres, int accumulate, float* dw, float* db,
+                               const void* dy, const void* x, const void* w, const float* mean,
+                               const float* rstd, int M, int C, float scale, float* partials,
+                               void* stream);
+
+/* Per row of logits [M, Vp]: losses[row] = logsumexp(z[:V]) - z[target]; logits become,
+   in place, (softmax - onehot) / M over the first V columns and 0 in [V, Vp).
+   err: device int, OR-ed with 4 when a target is out of range. */
+int gpt2_op_classifier(int precision, void* logits, float* losses, const int32_t* targets,
+                       int M, int V, int Vp, int* err, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPT2_OPS_H */
