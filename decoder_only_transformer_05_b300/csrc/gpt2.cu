@@ -28,6 +28,8 @@ static int fail(int code, const char* fmt, ...) {
   return code;
 }
 
+int gpt2_set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
 #define CK(x)                                                                               \
   do {                                                                                      \
     cudaError_t e_ = (x);                                                                   \

@@ -5,9 +5,13 @@
 
 using namespace gpt2k;
 
+int gpt2_set_error(int code, const char* msg);   // gpt2.cu
+
 static int status(cudaError_t e) {
   if (e == cudaSuccess) return GPT2_OK;
-  return e == cudaErrorInvalidValue ? GPT2_ERR_ARG : GPT2_ERR_CUDA;
+  if (e == cudaErrorInvalidValue)
+    return gpt2_set_error(GPT2_ERR_ARG, "unsupported shape, alignment or argument");
+  return gpt2_set_error(GPT2_ERR_CUDA, cudaGetErrorString(e));
 }
 static DType dtype(int precision) { return precision == GPT2_BF16 ? DType::BF16 : DType::F32; }
 
@@ -16,7 +20,7 @@ extern "C" int gpt2_op_gemm(int precision, int M, int N, int K, const void* A, i
                             int64_t ldo, const void* bias, const void* resid, void* pre,
                             const void* aux, float* accum, float scale, int splits,
                             float* workspace, size_t workspace_bytes, void* stream) {
-  if (epi < 0 || epi > 3) return GPT2_ERR_ARG;
+  if (epi < 0 || epi > 3) return gpt2_set_error(GPT2_ERR_ARG, "bad epilogue");
   GemmArgs g;
   g.M = M; g.N = N; g.K = K;
   g.A = A; g.lda = lda; g.a_mn = a_mn != 0;
@@ -30,7 +34,7 @@ extern "C" int gpt2_op_gemm(int precision, int M, int N, int K, const void* A, i
   if (epi == EPI_ACCUM) {
     int sp = splits > 0 ? splits : gemm_tc_pick_splits(M, N, K, gemm_tc_num_sms());
     if (sp > 1 && (!workspace || workspace_bytes < (size_t)sp * M * N * sizeof(float)))
-      return GPT2_ERR_ARG;
+      return gpt2_set_error(GPT2_ERR_ARG, "split-K workspace missing or too small");
     g.splits = sp;
   }
   return status(gemm_bf16_tc(g, s));

@@ -62,16 +62,19 @@ def gemm_ref(A, B_, a_mn, b_mn):
 def test_gemm_store(prec, a_mn, b_mn, shape):
     M, N, K = shape
     dt = torch.bfloat16 if prec == "bf16" else torch.float32
-    A = rnd((K, M) if a_mn else (M, K), 1)
+    # an MN-major A is stored [K, lda] with lda padded to a multiple of 8 elements
+    lda = (M + 7) // 8 * 8 if a_mn else K
+    A = rnd((K, lda) if a_mn else (M, K), 1)
     Bm = rnd((K, N) if b_mn else (N, K), 2)
     bias = rnd((N,), 3)
     resid = rnd((M, N), 4)
     dA, dB, db, dr = dev(A, dt), dev(Bm, dt), dev(bias, dt), dev(resid, dt)
     out = torch.empty(M, N, dtype=dt, device="cuda")
-    G.op_gemm(prec, M, N, K, dA, M if a_mn else K, a_mn, dB, N if b_mn else K, b_mn, "store",
+    G.op_gemm(prec, M, N, K, dA, lda, a_mn, dB, N if b_mn else K, b_mn, "store",
               out=out, ldo=N, bias=db, resid=dr)
     torch.cuda.synchronize()
-    ref = gemm_ref(host(dA), host(dB), a_mn, b_mn) + host(db)[None, :] + host(dr)
+    Ah = host(dA)[:, :M] if a_mn else host(dA)
+    ref = gemm_ref(Ah, host(dB), a_mn, b_mn) + host(db)[None, :] + host(dr)
     got = host(out)
     if prec == "bf16":
         assert rel_inf(got, ref) < 8e-3
@@ -125,9 +128,15 @@ def test_gemm_wgrad_accumulate_bf16(splits, shape):
 
 
 def test_gemm_rejects_unaligned_sizes():
-    x = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(G.GPT2Error):
+    x = torch.zeros(64 * 130, dtype=torch.bfloat16, device="cuda")
+    # N not a multiple of 64
+    with pytest.raises(G.GPT2Error) as e:
         G.op_gemm("bf16", 64, 48, 64, x, 64, False, x, 64, False, "store", out=x, ldo=64)
+    assert e.value.name == "ARG"
+    # leading dimension of an MN-major operand not a multiple of 8 elements
+    with pytest.raises(G.GPT2Error) as e:
+        G.op_gemm("bf16", 130, 64, 64, x, 130, True, x, 64, False, "store", out=x, ldo=64)
+    assert e.value.name == "ARG"
 
 
 def test_gemm_large_forward_shape():

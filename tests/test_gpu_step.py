@@ -123,6 +123,7 @@ def test_fp32_adamw_update(tiny):
 
 def test_fp32_gradient_accumulation_is_linear(tiny):
     m = tiny["m"]
+    m.set_params(tiny["params"])      # the AdamW test moved them
     m.zero_grad()
     m.forward(tiny["dtok"], tiny["dtgt"])
     m.backward(0.5)
@@ -130,7 +131,12 @@ def test_fp32_gradient_accumulation_is_linear(tiny):
     m.backward(0.5)
     g2 = m.get_grads()
     for name in g2:
-        assert np.array_equal(g2[name], tiny["grads"][name]), name
+        if name == "wte":
+            # the tied embedding gets two contributions per backward (lm_head and the
+            # embedding scatter), so the rounding order of the two sums differs
+            np.testing.assert_allclose(g2[name], tiny["grads"][name], rtol=1e-6, atol=1e-12)
+        else:
+            assert np.array_equal(g2[name], tiny["grads"][name]), name
 
 
 # ----------------------------------------------------------------- bf16 path
@@ -148,6 +154,8 @@ def bf16_step_check(name, B, loss_tol=2e-2, cos_min=0.999):
     for k in grads:
         worst[k] = cosine(grads[k], rgrads[k])
     bad = {k: v for k, v in worst.items() if v < cos_min}
+    print(f"\n{name} B={B}: loss {loss:.6f} oracle {ref['loss']:.6f}; min grad cosine "
+          f"{min(worst.values()):.6f} ({min(worst, key=worst.get)})")
     assert not bad, bad
     m.close()
     return loss, ref["loss"], worst
