@@ -133,8 +133,12 @@ def test_fp32_gradient_accumulation_is_linear(tiny):
     for name in g2:
         if name == "wte":
             # the tied embedding gets two contributions per backward (lm_head and the
-            # embedding scatter), so the rounding order of the two sums differs
-            np.testing.assert_allclose(g2[name], tiny["grads"][name], rtol=1e-6, atol=1e-12)
+            # embedding scatter), so the fp32 rounding order of the sums differs; where
+            # the two contributions cancel, an element's own relative error is unbounded,
+            # so the bound is a few fp32 ulps of the tensor's largest element
+            ref = tiny["grads"][name]
+            ulp = np.float32(2.0 ** -24) * np.abs(ref).max()
+            assert np.abs(g2[name] - ref).max() <= 8 * ulp, name
         else:
             assert np.array_equal(g2[name], tiny["grads"][name]), name
 
