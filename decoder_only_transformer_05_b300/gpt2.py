@@ -83,6 +83,8 @@ SIGNATURES = {
     "gpt2_op_layernorm_backward": (_I, [_I, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _F,
                                         _P, _P]),
     "gpt2_op_classifier": (_I, [_I, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "gpt2_op_layernorm_backward_noalloc": (_I, [_I, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I,
+                                                _I, _F, _P]),
 }
 
 _lib = None
@@ -354,3 +356,13 @@ def op_classifier(precision, logits, losses, targets, M, V, Vp, err, stream=None
     lib = load_library()
     _check(lib.gpt2_op_classifier(_prec(precision), ptr(logits), ptr(losses), ptr(targets), M, V,
                                   Vp, ptr(err), stream_handle(stream)))
+
+
+def op_layernorm_backward_noalloc(precision, dres, accumulate, dw, db, dy, x, w, mean, rstd, M,
+                                  C, scale, stream=None):
+    """LayerNorm backward with the library's built-in scratch (no partials buffer)."""
+    lib = load_library()
+    _check(lib.gpt2_op_layernorm_backward_noalloc(_prec(precision), ptr(dres), int(accumulate),
+                                                  ptr(dw), ptr(db), ptr(dy), ptr(x), ptr(w),
+                                                  ptr(mean), ptr(rstd), M, C, scale,
+                                                  stream_handle(stream)))

@@ -61,6 +61,30 @@ int gpt2_op_layernorm_backward(int precision, void* dres, int accumulate, float*
                                const float* rstd, int M, int C, float scale, float* partials,
                                void* stream);
 
+/*
+ * gpt2_op_layernorm_backward without a scratch argument and without any allocation. The
+ * paper has no counterpart to this call; it exists for callers that cannot allocate device memory
+ * once they run (a host whose memory manager reserved the device's memory for its own
+ * pool at start-up, a plug-in interface that hands over only inputs and outputs, a loop
+ * that must never reach cudaMalloc/cudaFree because they can synchronise the device).
+ * Same arguments and results as gpt2_op_layernorm_backward minus `partials`.
+ *   - Scratch: one fixed array of 2^20 floats (4 MiB) built into the library's device
+ *     code. Every GPU that loads the library holds it until the process exits.
+ *   - Limit: gpt2_op_layernorm_partials_floats(M, C) must be <= 2^20 (true for C <= 1771
+ *     at any M, e.g. C = 768 or 1024); larger shapes return GPT2_ERR_ARG with a message
+ *     and launch nothing.
+ *   - Set-up: the first call on each device (made with that device current) looks up the
+ *     array's device address with cudaGetSymbolAddress; make that first call before any
+ *     stream capture on that device.
+ *   - Sharing: every call uses the same array. Calls whose work overlaps on the GPU (two
+ *     streams, or two host threads) race on it; serialise them. Nothing in the array needs
+ *     to start at zero: each call overwrites the partial sums it reads.
+ */
+int gpt2_op_layernorm_backward_noalloc(int precision, void* dres, int accumulate, float* dw,
+                                       float* db, const void* dy, const void* x,
+                                       const void* w, const float* mean, const float* rstd,
+                                       int M, int C, float scale, void* stream);
+
 /* Per row of logits [M, Vp]: losses[row] = logsumexp(z[:V]) - z[target]; logits become,
    in place, (softmax - onehot) / M over the first V columns and 0 in [V, Vp).
    err: device int, OR-ed with 4 when a target is out of range. */

@@ -1,0 +1,89 @@
+"""The allocation-free LayerNorm backward (gpt2_op_layernorm_backward_noalloc) against
+the ordinary entry point, through the C ABI.
+
+The variant exists for callers that cannot allocate device memory while they run (for
+example a host whose memory manager reserved the GPU's memory for its own pool at
+start-up, or a plug-in interface that passes only inputs and outputs): it keeps its
+partial sums in a fixed array inside the library instead of a caller buffer. Two calls
+in a row with different inputs check that the shared array's leftover contents from the
+first call do not leak into the second. This file is collected last so that a run that
+stops at the first failure has already run every other test.
+"""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+G = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    global G
+    from decoder_only_transformer_05_b300 import build, gpt2
+    build.build()
+    gpt2.load_library()
+    G = gpt2
+    torch.cuda.init()
+    yield
+
+
+def _inputs(prec, M, C, seed):
+    dt = torch.bfloat16 if prec == "bf16" else torch.float32
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    x = (2.0 * torch.randn(M, C, generator=g) + 0.5).to(dt).cuda()
+    w = (1.0 + 0.2 * torch.randn(C, generator=g)).to(dt).cuda()
+    b = (0.2 * torch.randn(C, generator=g)).to(dt).cuda()
+    dy = torch.randn(M, C, generator=g).to(dt).cuda()
+    dres = torch.randn(M, C, generator=g).to(dt).cuda()
+    y = torch.empty(M, C, dtype=dt, device="cuda")
+    mean = torch.empty(M, device="cuda")
+    rstd = torch.empty(M, device="cuda")
+    G.op_layernorm_forward(prec, y, mean, rstd, x, w, b, M, C)
+    return x, w, dy, dres, mean, rstd
+
+
+def _run(prec, M, C, seed, noalloc, scale=0.5):
+    x, w, dy, dres, mean, rstd = _inputs(prec, M, C, seed)
+    dw = torch.full((C,), 0.25, device="cuda")
+    db = torch.full((C,), -0.25, device="cuda")
+    if noalloc:
+        G.op_layernorm_backward_noalloc(prec, dres, 1, dw, db, dy, x, w, mean, rstd, M, C, scale)
+    else:
+        part = torch.empty(G.op_layernorm_partials_floats(M, C), device="cuda")
+        G.op_layernorm_backward(prec, dres, 1, dw, db, dy, x, w, mean, rstd, M, C, scale, part)
+    torch.cuda.synchronize()
+    return dres.float().cpu().numpy(), dw.cpu().numpy(), db.cpu().numpy()
+
+
+def _rel_inf(a, r):
+    return float(np.abs(a - r).max() / max(np.abs(r).max(), 1e-30))
+
+
+# the GPT-2 124M rows (B=12, T=1024, C=768), a ragged row count, and the fp32 path
+@pytest.mark.parametrize("prec,M,C", [("bf16", 12288, 768), ("bf16", 4133, 1024),
+                                      ("fp32", 1000, 384)])
+def test_noalloc_matches_caller_scratch_on_two_calls(prec, M, C):
+    tol = 1e-2 if prec == "bf16" else 1e-5     # the LayerNorm parity tests' bounds
+    for seed in (1, 2):                          # two calls in a row, different inputs
+        want = _run(prec, M, C, seed, noalloc=False)
+        got = _run(prec, M, C, seed, noalloc=True)
+        assert _rel_inf(got[0], want[0]) <= tol
+        assert _rel_inf(got[1], want[1]) <= 1e-4
+        assert _rel_inf(got[2], want[2]) <= 1e-4
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch():
+    M, C = 9472, 2048          # 296 blocks x 2 x 2048 floats > 2^20
+    assert G.op_layernorm_partials_floats(M, C) > 1 << 20
+    x, w, dy, dres, mean, rstd = _inputs("bf16", M, C, 3)
+    dw = torch.zeros(C, device="cuda")
+    db = torch.zeros(C, device="cuda")
+    before = dres.clone()
+    with pytest.raises(G.GPT2Error) as e:
+        G.op_layernorm_backward_noalloc("bf16", dres, 1, dw, db, dy, x, w, mean, rstd, M, C,
+                                        1.0)
+    assert e.value.name == "ARG" and "scratch" in str(e.value)
+    torch.cuda.synchronize()
+    assert torch.equal(dres, before) and not dw.any() and not db.any()
