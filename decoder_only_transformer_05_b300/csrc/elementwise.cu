@@ -1,7 +1,7 @@
 // Memory-bound kernels of the GPT-2 training step: embedding gather and its
-// deterministic scatter-add backward, LayerNorm forward/backward, the fused
-// softmax-cross-entropy classifier, bias-gradient column sums, split-K reduction,
-// global gradient norm and AdamW.
+// deterministic scatter-add backward, the fused softmax-cross-entropy classifier,
+// split-K reduction, global gradient norm and AdamW (LayerNorm and the column sums are
+// in layernorm.cu).
 //
 // Every reduction runs in a fixed order (fixed partitions, fixed combine order), so two
 // runs on the same inputs give bit-identical results.
@@ -289,242 +289,6 @@ cudaError_t encoder_backward(DType t, float* dwte, float* dwpe, const void* dx, 
 }
 
 // =====================================================================================
-// LayerNorm forward: y = (x - mean) * rstd * w + b, biased variance, eps 1e-5.
-// One warp per row; the row stays in registers (MAXV 16-byte vectors per lane).
-template <typename T, int MAXV>
-__global__ void ln_fwd_kernel(T* __restrict__ y, float* __restrict__ mean, float* __restrict__ rstd,
-                              const T* __restrict__ x, const T* __restrict__ w,
-                              const T* __restrict__ b, int M, int C) {
-  constexpr int VE = 16 / sizeof(T);
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= M) return;
-  const T* xr = x + (size_t)row * C;
-  float v[MAXV][VE];
-  float s = 0.f;
-#pragma unroll
-  for (int j = 0; j < MAXV; ++j) {
-    int c = (j * 32 + lane) * VE;
-    if (c < C) {
-      Vec16<T> a = ld16(xr + c);
-#pragma unroll
-      for (int e = 0; e < VE; ++e) { v[j][e] = to_f32(a.e[e]); s += v[j][e]; }
-    } else {
-#pragma unroll
-      for (int e = 0; e < VE; ++e) v[j][e] = 0.f;
-    }
-  }
-  const float mu = warp_sum(s) / C;
-  float q = 0.f;
-#pragma unroll
-  for (int j = 0; j < MAXV; ++j) {
-    int c = (j * 32 + lane) * VE;
-    if (c < C) {
-#pragma unroll
-      for (int e = 0; e < VE; ++e) { float d = v[j][e] - mu; q += d * d; }
-    }
-  }
-  const float rs = rsqrtf(warp_sum(q) / C + 1e-5f);
-  T* yr = y + (size_t)row * C;
-#pragma unroll
-  for (int j = 0; j < MAXV; ++j) {
-    int c = (j * 32 + lane) * VE;
-    if (c < C) {
-      Vec16<T> wv = ld16(w + c), bv = ld16(b + c), o;
-#pragma unroll
-      for (int e = 0; e < VE; ++e)
-        o.e[e] = from_f32<T>((v[j][e] - mu) * rs * to_f32(wv.e[e]) + to_f32(bv.e[e]));
-      st16(yr + c, o);
-    }
-  }
-  if (lane == 0) { mean[row] = mu; rstd[row] = rs; }
-}
-
-template <typename T>
-static cudaError_t ln_fwd_dispatch(T* y, float* mean, float* rstd, const T* x, const T* w,
-                                   const T* b, int M, int C, cudaStream_t s) {
-  constexpr int VE = 16 / sizeof(T);
-  int vpl = ceil_div(C, 32 * VE);
-  dim3 grid(ceil_div(M, 8)), block(256);
-  switch (vpl) {
-    case 1: ln_fwd_kernel<T, 1><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C); count_launches(1); break;
-    case 2: ln_fwd_kernel<T, 2><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C); count_launches(1); break;
-    case 3: ln_fwd_kernel<T, 3><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C); count_launches(1); break;
-    case 4: ln_fwd_kernel<T, 4><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C); count_launches(1); break;
-    case 5: case 6: ln_fwd_kernel<T, 6><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C); count_launches(1); break;
-    case 7: case 8: ln_fwd_kernel<T, 8><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C); count_launches(1); break;
-    default: return cudaErrorInvalidValue;
-  }
-  return last();
-}
-
-cudaError_t layernorm_forward(DType t, void* y, float* mean, float* rstd, const void* x,
-                              const void* w, const void* b, int M, int C, cudaStream_t s) {
-  if (t == DType::BF16) {
-    if (C % 8) return cudaErrorInvalidValue;
-    return ln_fwd_dispatch<bf16>((bf16*)y, mean, rstd, (const bf16*)x, (const bf16*)w,
-                                 (const bf16*)b, M, C, s);
-  }
-  if (C % 4) return cudaErrorInvalidValue;
-  return ln_fwd_dispatch<float>((float*)y, mean, rstd, (const float*)x, (const float*)w,
-                                (const float*)b, M, C, s);
-}
-
-// -------------------------------------------------------------------------------------
-// LayerNorm backward (「手写训练脚本：不用框架，从零实现GPT训练流程」 二: LayerNorm's
-// backward derived by hand):
-//   xhat = (x - mean) rstd;  g = dy * w
-//   dx = rstd (g - mean(g) - xhat mean(g xhat));  dres = (accumulate ? dres : 0) + dx
-//   dw += sum_rows dy xhat;  db += sum_rows dy
-// Block c handles a fixed contiguous range of rows; its per-column sums go to
-// partials[c] and a second kernel adds them in block order.
-constexpr int LNB_THREADS = 256;
-int layernorm_backward_blocks(int M) { return std::min(ceil_div(M, 32), 2 * 148); }
-
-template <typename T, int MAXV>
-__global__ void __launch_bounds__(LNB_THREADS)
-ln_bwd_kernel(T* __restrict__ dres, int accumulate, float* __restrict__ partials,
-              const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ w,
-              const float* __restrict__ mean, const float* __restrict__ rstd, int M, int C,
-              int rows_per_block) {
-  constexpr int VE = 16 / sizeof(T);
-  constexpr int WARPS = LNB_THREADS / 32;
-  extern __shared__ float smem_lnb[];   // [2][C]
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int r_begin = blockIdx.x * rows_per_block;
-  const int r_end = min(M, r_begin + rows_per_block);
-  float dw[MAXV][VE], db[MAXV][VE], wv[MAXV][VE];
-#pragma unroll
-  for (int j = 0; j < MAXV; ++j) {
-    int c = (j * 32 + lane) * VE;
-#pragma unroll
-    for (int e = 0; e < VE; ++e) { dw[j][e] = 0.f; db[j][e] = 0.f; wv[j][e] = 0.f; }
-    if (c < C) {
-      Vec16<T> a = ld16(w + c);
-#pragma unroll
-      for (int e = 0; e < VE; ++e) wv[j][e] = to_f32(a.e[e]);
-    }
-  }
-  for (int row = r_begin + wid; row < r_end; row += WARPS) {
-    const float mu = mean[row], rs = rstd[row];
-    float g[MAXV][VE], xh[MAXV][VE];
-    float sg = 0.f, sgx = 0.f;
-#pragma unroll
-    for (int j = 0; j < MAXV; ++j) {
-      int c = (j * 32 + lane) * VE;
-      if (c < C) {
-        Vec16<T> a = ld16(dy + (size_t)row * C + c), b = ld16(x + (size_t)row * C + c);
-#pragma unroll
-        for (int e = 0; e < VE; ++e) {
-          float d = to_f32(a.e[e]);
-          xh[j][e] = (to_f32(b.e[e]) - mu) * rs;
-          g[j][e] = d * wv[j][e];
-          sg += g[j][e];
-          sgx += g[j][e] * xh[j][e];
-          dw[j][e] += d * xh[j][e];
-          db[j][e] += d;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < VE; ++e) { g[j][e] = 0.f; xh[j][e] = 0.f; }
-      }
-    }
-    const float mg = warp_sum(sg) / C, mgx = warp_sum(sgx) / C;
-#pragma unroll
-    for (int j = 0; j < MAXV; ++j) {
-      int c = (j * 32 + lane) * VE;
-      if (c < C) {
-        T* dr = dres + (size_t)row * C + c;
-        Vec16<T> o;
-        if (accumulate) o = ld16(dr);
-#pragma unroll
-        for (int e = 0; e < VE; ++e) {
-          float dx = rs * (g[j][e] - mg - xh[j][e] * mgx);
-          o.e[e] = from_f32<T>((accumulate ? to_f32(o.e[e]) : 0.f) + dx);
-        }
-        st16(dr, o);
-      }
-    }
-  }
-  // combine the warps' column sums in warp order
-  for (int k = 0; k < WARPS; ++k) {
-    if (wid == k) {
-#pragma unroll
-      for (int j = 0; j < MAXV; ++j) {
-        int c = (j * 32 + lane) * VE;
-        if (c < C) {
-#pragma unroll
-          for (int e = 0; e < VE; ++e) {
-            if (k == 0) { smem_lnb[c + e] = dw[j][e]; smem_lnb[C + c + e] = db[j][e]; }
-            else { smem_lnb[c + e] += dw[j][e]; smem_lnb[C + c + e] += db[j][e]; }
-          }
-        }
-      }
-    }
-    __syncthreads();
-  }
-  float* out = partials + (size_t)blockIdx.x * 2 * C;
-  for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) out[c] = smem_lnb[c];
-}
-
-// out0[c] += scale * sum_k partials[k][c], out1[c] += scale * sum_k partials[k][C + c]
-__global__ void column_partials_reduce_kernel(float* __restrict__ out0, float* __restrict__ out1,
-                                              const float* __restrict__ partials, int nparts,
-                                              int C, int stride, float scale) {
-  int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= C) return;
-  float s0 = 0.f, s1 = 0.f;
-  for (int k = 0; k < nparts; ++k) {
-    s0 += partials[(size_t)k * stride + c];
-    if (out1) s1 += partials[(size_t)k * stride + C + c];
-  }
-  out0[c] += scale * s0;
-  if (out1) out1[c] += scale * s1;
-}
-
-template <typename T>
-static cudaError_t ln_bwd_dispatch(T* dres, int acc, float* dw, float* db, const T* dy, const T* x,
-                                   const T* w, const float* mean, const float* rstd, int M, int C,
-                                   float scale, float* partials, cudaStream_t s) {
-  constexpr int VE = 16 / sizeof(T);
-  int blocks = layernorm_backward_blocks(M);
-  int rpb = ceil_div(M, blocks);
-  blocks = ceil_div(M, rpb);
-  size_t sm = sizeof(float) * 2 * C;
-  int vpl = ceil_div(C, 32 * VE);
-  switch (vpl) {
-#define LNB_CASE(N)                                                                           \
-  ln_bwd_kernel<T, N><<<blocks, LNB_THREADS, sm, s>>>(dres, acc, partials, dy, x, w, mean,   \
-                                                      rstd, M, C, rpb); count_launches(1);  \
-  break;
-    case 1: LNB_CASE(1)
-    case 2: LNB_CASE(2)
-    case 3: LNB_CASE(3)
-    case 4: LNB_CASE(4)
-    case 5: case 6: LNB_CASE(6)
-    case 7: case 8: LNB_CASE(8)
-#undef LNB_CASE
-    default: return cudaErrorInvalidValue;
-  }
-  column_partials_reduce_kernel<<<ceil_div(C, 256), 256, 0, s>>>(dw, db, partials, blocks, C,
-                                                                  2 * C, scale); count_launches(1);
-  return last();
-}
-
-cudaError_t layernorm_backward(DType t, void* dres, int accumulate, float* dw, float* db,
-                               const void* dy, const void* x, const void* w, const float* mean,
-                               const float* rstd, int M, int C, float scale, float* partials,
-                               cudaStream_t s) {
-  if (t == DType::BF16)
-    return ln_bwd_dispatch<bf16>((bf16*)dres, accumulate, dw, db, (const bf16*)dy,
-                                 (const bf16*)x, (const bf16*)w, mean, rstd, M, C, scale,
-                                 partials, s);
-  return ln_bwd_dispatch<float>((float*)dres, accumulate, dw, db, (const float*)dy,
-                                (const float*)x, (const float*)w, mean, rstd, M, C, scale,
-                                partials, s);
-}
-
-// =====================================================================================
 // Fused classifier (「从零实现一个最小GPT」 二.7 forward step 4, F.cross_entropy with mean
 // reduction): one block per row. Pass 1 reads the row once with a running (max, sum of
 // exp) per thread over the first V columns; the block combines them into lse and the
@@ -668,59 +432,6 @@ cudaError_t argmax_rows(DType t, int* out, const void* logits, int M, int V, int
                         cudaStream_t s) {
   if (t == DType::BF16) { argmax_kernel<bf16><<<M, 256, 0, s>>>(out, (const bf16*)logits, V, Vp); count_launches(1); }
   else { argmax_kernel<float><<<M, 256, 0, s>>>(out, (const float*)logits, V, Vp); count_launches(1); }
-  return last();
-}
-
-// =====================================================================================
-// Bias gradient: db[n] += scale * sum_m dy[m, n]. Block (x, y) sums the rows of chunk y
-// for one strip of columns; the chunk sums are added in chunk order.
-constexpr int COLSUM_THREADS = 128;
-int colsum_blocks(int M) { return std::min(ceil_div(M, 64), 192); }
-
-template <typename T>
-__global__ void __launch_bounds__(COLSUM_THREADS)
-colsum_kernel(float* __restrict__ partials, const T* __restrict__ dy, int M, int N, int rpc) {
-  constexpr int VE = 16 / sizeof(T);
-  int c = (blockIdx.x * COLSUM_THREADS + threadIdx.x) * VE;
-  if (c >= N) return;
-  int r0 = blockIdx.y * rpc, r1 = min(M, r0 + rpc);
-  float acc[VE];
-#pragma unroll
-  for (int e = 0; e < VE; ++e) acc[e] = 0.f;
-  int r = r0;
-  for (; r + 4 <= r1; r += 4) {
-    Vec16<T> v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = ld16(dy + (size_t)(r + u) * N + c);
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int e = 0; e < VE; ++e) acc[e] += to_f32(v[u].e[e]);
-  }
-  for (; r < r1; ++r) {
-    Vec16<T> v = ld16(dy + (size_t)r * N + c);
-#pragma unroll
-    for (int e = 0; e < VE; ++e) acc[e] += to_f32(v.e[e]);
-  }
-  float* out = partials + (size_t)blockIdx.y * N + c;
-#pragma unroll
-  for (int e = 0; e < VE; ++e) out[e] = acc[e];
-}
-
-cudaError_t bias_grad(DType t, float* db, const void* dy, int M, int N, float scale,
-                      float* partials, cudaStream_t s) {
-  int chunks = colsum_blocks(M);
-  int rpc = ceil_div(M, chunks);
-  chunks = ceil_div(M, rpc);
-  if (t == DType::BF16) {
-    dim3 grid(ceil_div(N, COLSUM_THREADS * 8), chunks);
-    colsum_kernel<bf16><<<grid, COLSUM_THREADS, 0, s>>>(partials, (const bf16*)dy, M, N, rpc); count_launches(1);
-  } else {
-    dim3 grid(ceil_div(N, COLSUM_THREADS * 4), chunks);
-    colsum_kernel<float><<<grid, COLSUM_THREADS, 0, s>>>(partials, (const float*)dy, M, N, rpc); count_launches(1);
-  }
-  column_partials_reduce_kernel<<<ceil_div(N, 256), 256, 0, s>>>(db, nullptr, partials, chunks, N,
-                                                                  N, scale); count_launches(1);
   return last();
 }
 

@@ -327,8 +327,9 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   size_t o_logits = plan(M * (size_t)h->Vp * es), o_losses = plan(M * 4), o_argmax = plan(M * 4);
   size_t o_dres = plan(M * C * es), o_dln = plan(M * C * es), o_datt = plan(M * C * es);
   size_t o_dqkv = plan(M * 3 * C * es), o_dfch = plan(M * 4 * C * es), o_D = plan(BHT * 4);
-  size_t o_lnp = plan((size_t)layernorm_backward_blocks((int)M) * 2 * C * 4);
-  size_t o_csp = plan((size_t)colsum_blocks((int)M) * 4 * C * 4);
+  size_t o_lnp = plan(layernorm_backward_partials_floats((int)M, (int)C, true) * 4);
+  size_t o_csp = plan(std::max(colsum_partials_floats((int)M, 3 * (int)C),
+                               colsum_partials_floats((int)M, 4 * (int)C)) * 4);
   size_t ws = 0;
   if (h->is_bf16) {
     const int sms = gemm_tc_num_sms();
@@ -560,22 +561,24 @@ extern "C" int gpt2_backward(gpt2_handle h, float loss_scale) {
   // lm_head (tied): dlnf = dlogits wte ; dwte += sc dlogits^T lnf
   CKL(run_gemm(h, linear_dgrad(M, Vp, C, h->logits, h->pw(T_WTE), h->dln)));
   CKL(run_gemm(h, linear_wgrad(M, Vp, C, h->logits, h->lnf, h->gw(T_WTE), sc)));
+  // The column sums of each residual-stream gradient that a LayerNorm backward writes are
+  // the bias gradient of the projection that fed that stream: lnf -> fcproj of layer L-1,
+  // LN2 of layer l -> attproj of layer l, LN1 of layer l -> fcproj of layer l-1.
+  auto proj_bias = [&](int id, int layer) -> float* {
+    return (h->bias && layer >= 0) ? h->gw(id, layer) : nullptr;
+  };
   pi = prof_begin(h, PC_LN);
-  CKL(layernorm_backward(dt, h->dres, 0, h->gw(T_LNFW), h->gw(T_LNFB), h->dln, h->x[L],
-                         h->pw(T_LNFW), h->lnf_mean, h->lnf_rstd, M, C, sc, h->ln_partials, s));
+  CKL(layernorm_backward(dt, h->dres, 0, h->gw(T_LNFW), h->gw(T_LNFB), proj_bias(T_FCPROJB, L - 1),
+                         h->dln, h->x[L], h->pw(T_LNFW), h->lnf_mean, h->lnf_rstd, M, C, sc,
+                         h->ln_partials, s));
   prof_end(h, pi, (double)M * C * es * 3);
   for (int l = L - 1; l >= 0; --l) {
-    // x[l+1] = xmid + gelu(fch) Wp^T + bp
+    // x[l+1] = xmid + gelu(fch) Wp^T + bp  (bp's gradient came with dres, above)
     GemmArgs g = linear_dgrad(M, C, 4 * C, h->dres, h->pw(T_FCPROJW, l), h->dfch);
     g.epi = EPI_GELU_BWD;
     g.aux = h->fch[l];
     CKL(run_gemm(h, g));
     CKL(run_gemm(h, linear_wgrad(M, C, 4 * C, h->dres, h->fcg[l], h->gw(T_FCPROJW, l), sc)));
-    if (h->bias) {
-      pi = prof_begin(h, PC_OTHER);
-      CKL(bias_grad(dt, h->gw(T_FCPROJB, l), h->dres, M, C, sc, h->colsum_partials, s));
-      prof_end(h, pi, (double)M * C * es);
-    }
     // fch = ln2 Wfc^T + bfc
     CKL(run_gemm(h, linear_dgrad(M, 4 * C, C, h->dfch, h->pw(T_FCW, l), h->dln)));
     CKL(run_gemm(h, linear_wgrad(M, 4 * C, C, h->dfch, h->ln2[l], h->gw(T_FCW, l), sc)));
@@ -585,18 +588,13 @@ extern "C" int gpt2_backward(gpt2_handle h, float loss_scale) {
       prof_end(h, pi, (double)M * 4 * C * es);
     }
     pi = prof_begin(h, PC_LN);
-    CKL(layernorm_backward(dt, h->dres, 1, h->gw(T_LN2W, l), h->gw(T_LN2B, l), h->dln,
-                           h->xmid[l], h->pw(T_LN2W, l), h->ln2_mean[l], h->ln2_rstd[l], M, C,
-                           sc, h->ln_partials, s));
+    CKL(layernorm_backward(dt, h->dres, 1, h->gw(T_LN2W, l), h->gw(T_LN2B, l),
+                           proj_bias(T_ATTPROJB, l), h->dln, h->xmid[l], h->pw(T_LN2W, l),
+                           h->ln2_mean[l], h->ln2_rstd[l], M, C, sc, h->ln_partials, s));
     prof_end(h, pi, (double)M * C * es * 4);
-    // xmid = x + att Wo^T + bo
+    // xmid = x + att Wo^T + bo  (bo's gradient came with dres, above)
     CKL(run_gemm(h, linear_dgrad(M, C, C, h->dres, h->pw(T_ATTPROJW, l), h->datt)));
     CKL(run_gemm(h, linear_wgrad(M, C, C, h->dres, h->att[l], h->gw(T_ATTPROJW, l), sc)));
-    if (h->bias) {
-      pi = prof_begin(h, PC_OTHER);
-      CKL(bias_grad(dt, h->gw(T_ATTPROJB, l), h->dres, M, C, sc, h->colsum_partials, s));
-      prof_end(h, pi, (double)M * C * es);
-    }
     pi = prof_begin(h, PC_ATTN);
     CKL(attention_backward(dt, h->dqkv, h->Dbuf, h->datt, h->att[l], h->qkv[l], h->lse[l], B, T,
                            C, H, s));
@@ -610,9 +608,9 @@ extern "C" int gpt2_backward(gpt2_handle h, float loss_scale) {
       prof_end(h, pi, (double)M * 3 * C * es);
     }
     pi = prof_begin(h, PC_LN);
-    CKL(layernorm_backward(dt, h->dres, 1, h->gw(T_LN1W, l), h->gw(T_LN1B, l), h->dln, h->x[l],
-                           h->pw(T_LN1W, l), h->ln1_mean[l], h->ln1_rstd[l], M, C, sc,
-                           h->ln_partials, s));
+    CKL(layernorm_backward(dt, h->dres, 1, h->gw(T_LN1W, l), h->gw(T_LN1B, l),
+                           proj_bias(T_FCPROJB, l - 1), h->dln, h->x[l], h->pw(T_LN1W, l),
+                           h->ln1_mean[l], h->ln1_rstd[l], M, C, sc, h->ln_partials, s));
     prof_end(h, pi, (double)M * C * es * 4);
   }
   pi = prof_begin(h, PC_ENC);

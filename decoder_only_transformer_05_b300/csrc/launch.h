@@ -67,13 +67,16 @@ cudaError_t encoder_backward(DType t, float* dwte, float* dwpe, const void* dx, 
 
 cudaError_t layernorm_forward(DType t, void* y, float* mean, float* rstd, const void* x,
                               const void* w, const void* b, int M, int C, cudaStream_t s);
-// dres (+)= dx of LayerNorm; dw, db += scale * column sums (two deterministic stages).
-// partials: layernorm_backward_partials(M) * 2 * C floats.
+// dres (+)= dx of LayerNorm; dw, db += scale * column sums of dy*xhat and dy; when dproj
+// is non-null, dproj += scale * column sums of the dres this call writes (the bias
+// gradient of the projection that produced the residual stream). Two deterministic
+// stages; partials: layernorm_backward_partials_floats(M, C, dproj != nullptr) floats.
 int layernorm_backward_blocks(int M);
+size_t layernorm_backward_partials_floats(int M, int C, bool dproj);
 cudaError_t layernorm_backward(DType t, void* dres, int accumulate, float* dw, float* db,
-                               const void* dy, const void* x, const void* w, const float* mean,
-                               const float* rstd, int M, int C, float scale, float* partials,
-                               cudaStream_t s);
+                               float* dproj, const void* dy, const void* x, const void* w,
+                               const float* mean, const float* rstd, int M, int C, float scale,
+                               float* partials, cudaStream_t s);
 
 // Fused classifier over the logits rows: per row loss = lse - z[y] over the first V
 // columns; in place, logits become dlogits = (softmax - onehot) / M (0 in pad columns).
@@ -85,8 +88,9 @@ cudaError_t mean_loss(float* loss_out, const float* losses, int M, cudaStream_t 
 cudaError_t argmax_rows(DType t, int* out, const void* logits, int M, int V, int Vp,
                         cudaStream_t s);
 
-// Bias gradient: db[n] += scale * sum_m dy[m, n] (two deterministic stages).
-int colsum_blocks(int M);
+// Bias gradient: db[n] += scale * sum_m dy[m, n] (two deterministic stages);
+// partials: colsum_partials_floats(M, N) floats.
+size_t colsum_partials_floats(int M, int N);
 cudaError_t bias_grad(DType t, float* db, const void* dy, int M, int N, float scale,
                       float* partials, cudaStream_t s);
 

@@ -64,7 +64,7 @@ extern "C" int gpt2_op_layernorm_backward_noalloc(int precision, void* dres, int
                                                   const float* mean, const float* rstd, int M,
                                                   int C, float scale, void* stream) {
   if (M <= 0 || C <= 0) return gpt2_set_error(GPT2_ERR_ARG, "M and C must be positive");
-  const size_t need = (size_t)layernorm_backward_blocks(M) * 2 * (size_t)C;
+  const size_t need = layernorm_backward_partials_floats(M, C, false);
   if (need > kScratchFloats) {
     char msg[256];
     snprintf(msg, sizeof(msg),
@@ -79,8 +79,8 @@ extern "C" int gpt2_op_layernorm_backward_noalloc(int precision, void* dres, int
   // Every block of the backward kernel writes its whole row of partial sums before the
   // reduction reads it, so the previous call's contents never need clearing.
   cudaError_t e = layernorm_backward(precision == GPT2_BF16 ? DType::BF16 : DType::F32, dres,
-                                     accumulate, dw, db, dy, x, w, mean, rstd, M, C, scale,
-                                     scratch, (cudaStream_t)stream);
+                                     accumulate, dw, db, nullptr, dy, x, w, mean, rstd, M, C,
+                                     scale, scratch, (cudaStream_t)stream);
   if (e == cudaSuccess) return GPT2_OK;
   if (e == cudaErrorInvalidValue)
     return gpt2_set_error(GPT2_ERR_ARG, "unsupported shape, alignment or argument");

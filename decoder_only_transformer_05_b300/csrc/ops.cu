@@ -62,7 +62,7 @@ extern "C" int gpt2_op_layernorm_forward(int precision, void* y, float* mean, fl
 }
 
 extern "C" size_t gpt2_op_layernorm_partials_floats(int M, int C) {
-  return (size_t)layernorm_backward_blocks(M) * 2 * (size_t)C;
+  return layernorm_backward_partials_floats(M, C, false);
 }
 
 extern "C" int gpt2_op_layernorm_backward(int precision, void* dres, int accumulate, float* dw,
@@ -70,8 +70,8 @@ extern "C" int gpt2_op_layernorm_backward(int precision, void* dres, int accumul
                                           const void* w, const float* mean, const float* rstd,
                                           int M, int C, float scale, float* partials,
                                           void* stream) {
-  return status(layernorm_backward(dtype(precision), dres, accumulate, dw, db, dy, x, w, mean,
-                                   rstd, M, C, scale, partials, (cudaStream_t)stream));
+  return status(layernorm_backward(dtype(precision), dres, accumulate, dw, db, nullptr, dy, x,
+                                   w, mean, rstd, M, C, scale, partials, (cudaStream_t)stream));
 }
 
 extern "C" int gpt2_op_classifier(int precision, void* logits, float* losses,

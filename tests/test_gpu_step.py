@@ -95,6 +95,34 @@ def test_fp32_gradients(tiny):
         assert rel_inf(g, r) <= 1e-3, (name, rel_inf(g, r))
 
 
+def test_fp32_gradients_with_linear_biases():
+    # the tiny model with biases on every Linear layer (non-zero, so the forward adds
+    # them too): the projection biases' gradients come from the LayerNorm backward's
+    # column sums, the fc/qkv ones from the column-sum kernel
+    w = dict(S.WORKLOADS["tiny-fp32"])
+    w["bias"] = True
+    m = G.GPT2(vocab_size=w["V"], padded_vocab_size=w["Vp"], block_size=w["T"],
+               n_layer=w["L"], n_head=w["H"], n_embd=w["C"], batch_size=w["B"], bias=True,
+               precision="fp32", init=False)
+    params = S.init_params(w["w_seed"], w["V"], w["Vp"], w["T"], w["L"], w["C"], True)
+    rng = np.random.default_rng(7)
+    for k in ("qkvb", "attprojb", "fcb", "fcprojb"):
+        params[k] = (0.02 * rng.standard_normal(params[k].shape)).astype(np.float32)
+    m.set_params(params)
+    tok, tgt, dtok, dtgt = tokens_for(w, w["B"])
+    loss = m.forward(dtok, dtgt, want_loss=True)
+    m.zero_grad()
+    m.backward(1.0)
+    grads = m.get_grads()
+    cfg = O.Config(w["V"], w["Vp"], w["T"], w["L"], w["H"], w["C"], True)
+    ref = O.forward(params, cfg, tok, tgt)
+    rgrads = O.backward(params, cfg, ref["cache"], 1.0)
+    assert abs(loss - ref["loss"]) / ref["loss"] <= 1e-5
+    for name, g in grads.items():
+        assert rel_inf(g, rgrads[name]) <= 1e-3, (name, rel_inf(g, rgrads[name]))
+    m.close()
+
+
 def test_fp32_adamw_update(tiny):
     m, params = tiny["m"], tiny["params"]
     lr, b1, b2, eps, wd = 1e-3, 0.9, 0.95, 1e-8, 0.1
