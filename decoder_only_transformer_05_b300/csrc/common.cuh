@@ -77,4 +77,26 @@ __device__ __forceinline__ float gelu_tanh_grad(float x) {
   return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * k * (1.0f + 3.0f * 0.044715f * x * x);
 }
 
+// The same two functions with tanh from the hardware approximation (PTX tanh.approx.f32,
+// relative error about 2^-11): used where the result is rounded to bf16 (8 significant
+// bits), so the approximation error stays well below the rounding step.
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float gelu_tanh_fast(float x) {
+  const float k0 = 0.7978845608028654f, k1 = 0.044715f * 0.7978845608028654f;
+  const float t = tanh_approx(x * fmaf(k1, x * x, k0));
+  const float hx = 0.5f * x;
+  return fmaf(hx, t, hx);
+}
+__device__ __forceinline__ float gelu_tanh_grad_fast(float x) {
+  const float k0 = 0.7978845608028654f, k1 = 0.044715f * 0.7978845608028654f;
+  const float x2 = x * x;
+  const float t = tanh_approx(x * fmaf(k1, x2, k0));
+  // 0.5 (1 + t) + 0.5 x (1 - t^2) (k0 + 3 k1 x^2)
+  return fmaf(0.5f * x * fmaf(-t, t, 1.0f), fmaf(3.0f * k1, x2, k0), fmaf(0.5f, t, 0.5f));
+}
+
 __host__ __device__ inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }

@@ -6,18 +6,22 @@
 // (m or n contiguous). Forward GEMMs are K-major x K-major, dgrad GEMMs K-major x
 // MN-major, wgrad GEMMs MN-major x MN-major.
 //
-// Structure (one persistent block of 192 threads per SM):
+// Structure (one persistent block of 320 threads per SM):
 //   warp 0      TMA producer: 128x64 A and BNx64 B tiles, 128-byte swizzle, into a
 //               ring of shared-memory stages (mbarrier full/empty handshake)
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN, K=16) into a
 //               fp32 accumulator in tensor memory; two accumulators alternate so the
 //               epilogue of one tile overlaps the main loop of the next
-//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time (each warp owns the 32 TMEM
-//               lanes = rows its warp index selects), apply the epilogue, store
+//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).. (the rows of its quarter),
+//               warps w and w+4 take alternate 32-column chunks of the tile. Per chunk:
+//               tcgen05.ld, the epilogue arithmetic, the result into a swizzled
+//               shared-memory staging buffer, then one TMA bulk-tensor store (or, for
+//               gradient accumulation, a TMA bulk-tensor reduce-add) of the 32x32 chunk.
 // Every mbarrier wait is bounded: on timeout the block records DEV_ERR_TIMEOUT, stops
 // issuing work, waits for its own copies and MMAs and frees its tensor memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -27,7 +31,9 @@ namespace gpt2k {
 namespace tc {
 
 constexpr int BM = 128, BK = 64;
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int STG_BYTES = 4096;   // per epilogue warp: 32 rows x 128 B
 constexpr unsigned long long TIMEOUT_NS = 2000000000ull;   // 2 s per wait
 
 template <int BN> struct Cfg {
@@ -37,16 +43,16 @@ template <int BN> struct Cfg {
   static constexpr int STAGES = BN == 256 ? 4 : 6;
   static constexpr int TMEM_COLS = 2 * BN;      // two accumulators
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = STAGES * STAGE + 1024 + BAR_BYTES;
+  static constexpr int SMEM = STAGES * STAGE + EPI_WARPS * STG_BYTES + 1024 + BAR_BYTES;
 };
 
 struct Params {
   int M, N, K;
   int num_m, num_n, splits, kb_per_split, num_kb;
   int epi;
-  void* out; long long ldo;
-  const bf16* bias; const bf16* resid; bf16* pre; const bf16* aux;
-  float* accum; float scale; float* workspace;
+  long long ldo;
+  const bf16* bias; const bf16* resid; const bf16* aux;
+  float scale;
   int* err;
 };
 
@@ -149,6 +155,57 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+               ::"l"((unsigned long long)map), "r"(src), "r"(c0), "r"(c1) : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+      ::"l"((unsigned long long)map), "r"(src), "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int c0,
+                                                  int c1) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];"
+      ::"l"((unsigned long long)map), "r"(src), "r"(c0), "r"(c1) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the staging buffer may be overwritten once the previous stores have read it
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void st_shared16(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+// Row `r` (the lane) of a 32x32 bf16 chunk, 64 B per row, into staging laid out for a
+// TMA map with 64-byte swizzle: 16-byte unit j of row r sits at unit j ^ ((r >> 1) & 3).
+__device__ __forceinline__ void stage_row_bf16(uint32_t buf, int r, const uint32_t (&w)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    st_shared16(buf + r * 64 + ((j ^ ((r >> 1) & 3)) << 4),
+                make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]));
+}
+// Row `r` of a 32x32 fp32 chunk, 128 B per row, for a 128-byte-swizzle map: unit j of
+// row r sits at unit j ^ (r & 7).
+__device__ __forceinline__ void stage_row_f32(uint32_t buf, int r, const float (&v)[32], float s) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    st_shared16(buf + r * 128 + ((j ^ (r & 7)) << 4),
+                make_uint4(__float_as_uint(s * v[4 * j]), __float_as_uint(s * v[4 * j + 1]),
+                           __float_as_uint(s * v[4 * j + 2]), __float_as_uint(s * v[4 * j + 3])));
+}
+
 // Shared-memory matrix descriptor: 128-byte swizzle, descriptor version 1.
 //   K-major tile: rows of 128 B (64 bf16 of k), 8-row groups 1024 B apart (SBO).
 //   MN-major tile: rows of 128 B (64 bf16 of m or n) per k, 8-k-row groups 1024 B
@@ -169,76 +226,81 @@ __host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool 
 }
 
 // ------------------------------------------------------------------ epilogue
-__device__ __forceinline__ void epilogue32(const Params& p, int row, int col0, int split,
-                                           const float (&v)[32]) {
-  const size_t o = (size_t)row * p.ldo + col0;
-  switch (p.epi) {
-    case EPI_STORE: {
-      bf16* out = (bf16*)p.out + o;
+// One 32x32 chunk: this thread's row `row`, columns [col0, col0 + 32), accumulator v.
+// Results go to the warp's staging buffer `stg` (and `stg + 2048` for the GELU
+// pre-activation); lane 0 then stores the chunk with TMA.
+struct EpiMaps {
+  CUtensorMap out;   // bf16 [M, N] (64-byte swizzle) or fp32 [M, N] / [splits, M, N] (128-byte)
+  CUtensorMap pre;   // bf16 [M, N], EPI_GELU_FWD only
+};
+
+__device__ __forceinline__ void epilogue_chunk(const Params& p, const EpiMaps& maps, int row,
+                                               int row0, int col0, int split, uint32_t stg,
+                                               uint32_t taddr) {
+  const int lane = threadIdx.x & 31;
+  // inputs first, so that their latency overlaps the tensor-memory load
+  uint4 bia[4], inp[4];
+  if (p.bias && p.epi != EPI_ACCUM) {
 #pragma unroll
-      for (int j = 0; j < 32; j += 8) {
-        Vec16<bf16> r, b, w;
-        if (p.resid) r = ld16(p.resid + o + j);
-        if (p.bias) b = ld16(p.bias + col0 + j);
+    for (int i = 0; i < 4; ++i) bia[i] = __ldg(reinterpret_cast<const uint4*>(p.bias + col0) + i);
+  }
+  const bf16* src = p.epi == EPI_GELU_BWD ? p.aux : (p.epi == EPI_STORE ? p.resid : nullptr);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float x = v[j + e];
-          if (p.bias) x += to_f32(b.e[e]);
-          if (p.resid) x += to_f32(r.e[e]);
-          w.e[e] = __float2bfloat16_rn(x);
-        }
-        st16(out + j, w);
+  for (int i = 0; i < 4; ++i) inp[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (src && row < p.M) {   // rows past M are computed but never stored (TMA clips them)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      inp[i] = __ldg(reinterpret_cast<const uint4*>(src + (size_t)row * p.ldo + col0) + i);
+  }
+  float v[32];
+  tmem_ld32(taddr, v);
+  if (p.bias && p.epi != EPI_ACCUM) {
+    const bf16* b = reinterpret_cast<const bf16*>(bia);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] += __bfloat162float(b[e]);
+  }
+  if (lane == 0) bulk_wait_read();
+  __syncwarp();
+  if (p.epi == EPI_ACCUM) {
+    stage_row_f32(stg, lane, v, p.splits == 1 ? p.scale : 1.0f);
+  } else {
+    uint32_t w[16];
+    if (p.epi == EPI_STORE) {
+      if (src) {
+        const bf16* r = reinterpret_cast<const bf16*>(inp);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] += __bfloat162float(r[e]);
       }
-      break;
-    }
-    case EPI_GELU_FWD: {
-      bf16* out = (bf16*)p.out + o;
-      bf16* pre = p.pre + o;
 #pragma unroll
-      for (int j = 0; j < 32; j += 8) {
-        Vec16<bf16> b, u, a;
-        if (p.bias) b = ld16(p.bias + col0 + j);
+      for (int e = 0; e < 16; ++e) w[e] = pack2_bf16(v[2 * e], v[2 * e + 1]);
+    } else if (p.epi == EPI_GELU_FWD) {
+      uint32_t u[16];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float x = v[j + e];
-          if (p.bias) x += to_f32(b.e[e]);
-          u.e[e] = __float2bfloat16_rn(x);
-          a.e[e] = __float2bfloat16_rn(gelu_tanh(x));
-        }
-        st16(pre + j, u);
-        st16(out + j, a);
+      for (int e = 0; e < 16; ++e) {
+        u[e] = pack2_bf16(v[2 * e], v[2 * e + 1]);
+        w[e] = pack2_bf16(gelu_tanh_fast(v[2 * e]), gelu_tanh_fast(v[2 * e + 1]));
       }
-      break;
+      stage_row_bf16(stg + 2048, lane, u);
+    } else {   // EPI_GELU_BWD
+      const bf16* a = reinterpret_cast<const bf16*>(inp);
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        w[e] = pack2_bf16(v[2 * e] * gelu_tanh_grad_fast(__bfloat162float(a[2 * e])),
+                          v[2 * e + 1] * gelu_tanh_grad_fast(__bfloat162float(a[2 * e + 1])));
     }
-    case EPI_GELU_BWD: {
-      bf16* out = (bf16*)p.out + o;
-#pragma unroll
-      for (int j = 0; j < 32; j += 8) {
-        Vec16<bf16> u = ld16(p.aux + o + j), w;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) w.e[e] = __float2bfloat16_rn(v[j + e] * gelu_tanh_grad(to_f32(u.e[e])));
-        st16(out + j, w);
-      }
-      break;
+    stage_row_bf16(stg, lane, w);
+  }
+  fence_proxy_async();
+  __syncwarp();
+  if (lane == 0 && row0 < p.M) {   // stores start in range; TMA clips the rest
+    if (p.epi == EPI_ACCUM) {
+      if (p.splits == 1) tma_reduce_add_2d(&maps.out, stg, col0, row0);
+      else tma_store_3d(&maps.out, stg, col0, row0, split);
+    } else {
+      tma_store_2d(&maps.out, stg, col0, row0);
+      if (p.epi == EPI_GELU_FWD) tma_store_2d(&maps.pre, stg + 2048, col0, row0);
     }
-    case EPI_ACCUM: {
-      if (p.splits == 1) {
-        float* a = p.accum + o;
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          float4 x = *reinterpret_cast<float4*>(a + j);
-          x.x += p.scale * v[j]; x.y += p.scale * v[j + 1];
-          x.z += p.scale * v[j + 2]; x.w += p.scale * v[j + 3];
-          *reinterpret_cast<float4*>(a + j) = x;
-        }
-      } else {
-        float* w = p.workspace + (size_t)split * p.M * p.N + (size_t)row * p.N + col0;
-#pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(w + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-      }
-      break;
-    }
+    bulk_commit();
   }
 }
 
@@ -246,15 +308,16 @@ __device__ __forceinline__ void epilogue32(const Params& p, int row, int col0, i
 template <int BN, bool AMN, bool BMN>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-            const Params p) {
+            const __grid_constant__ EpiMaps maps, const Params p) {
   using Cf = Cfg<BN>;
   constexpr uint32_t IDESC = make_idesc(BM, BN, AMN, BMN);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t bars = base + Cf::STAGES * Cf::STAGE;
-  uint8_t* bars_ptr = base_ptr + Cf::STAGES * Cf::STAGE;
+  const uint32_t staging = base + Cf::STAGES * Cf::STAGE;
+  const uint32_t bars = staging + EPI_WARPS * STG_BYTES;
+  uint8_t* bars_ptr = base_ptr + Cf::STAGES * Cf::STAGE + EPI_WARPS * STG_BYTES;
   // barrier layout: full[S] empty[S] tfull[2] tempty[2] final, then tmem slot, abort flag
   auto full = [&](int s) { return bars + 8u * s; };
   auto empty = [&](int s) { return bars + 8u * (Cf::STAGES + s); };
@@ -268,7 +331,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cf::STAGES; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), 4); }
+    for (int a = 0; a < 2; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), EPI_WARPS); }
     mbar_init(final_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -364,8 +427,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       mbar_wait(final_bar, 0, abort_flag, nullptr, false);
     }
   } else {
-    // ---------------- epilogue warps 2..5; warp % 4 selects the TMEM lane quarter
-    const int q = warp & 3;
+    // ---------------- epilogue warps 2..9; warp % 4 selects the TMEM lane quarter, and
+    // warps w, w + 4 split the tile's 32-column chunks between them (even / odd)
+    const int q = warp & 3, ew = warp - 2, half = ew >> 2;
+    const uint32_t stg = staging + ew * STG_BYTES;
+    if (p.epi == EPI_GELU_FWD && lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"((unsigned long long)&maps.pre) : "memory");
+    }
     int tcount = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tcount) {
       int mb, nb, sp;
@@ -376,20 +444,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const int row = mb * BM + q * 32 + lane;
+      const int row0 = mb * BM + q * 32;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = half; c < BN / 32; c += 2) {
         const int col0 = nb * BN + c * 32;
         if (col0 >= p.N) break;
-        float v[32];
-        tmem_ld32(taddr + c * 32, v);
-        if (row < p.M) epilogue32(p, row, col0, sp, v);
+        epilogue_chunk(p, maps, row0 + lane, row0, col0, sp, stg, taddr + c * 32);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty(acc));
     }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   __syncthreads();
   if (warp == 1) {
@@ -414,21 +482,33 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 map over a row-major matrix: `inner` contiguous elements per row, `outer`
-// rows, `ld` elements between rows; box = box_inner x box_outer, 128-byte swizzle,
-// out-of-range elements read as zero.
-static bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
-                     uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
+// Tensor map over a row-major matrix (rank 2) or a stack of them (rank 3): `inner`
+// contiguous elements per row, `outer` rows `ld` elements apart, `depth` matrices `dstride`
+// elements apart; box = box_inner x box_outer (x 1); out-of-range elements read as zero
+// and are not written.
+static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* ptr,
+                     uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
+                     uint32_t box_outer, CUtensorMapSwizzle swz, uint64_t depth = 0,
+                     uint64_t dstride = 0) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {ld * 2};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (((uintptr_t)ptr & 15u) || (ld * esize) % 16 || (depth && (dstride * esize) % 16))
+    return false;
+  const cuuint32_t rank = depth ? 3 : 2;
+  cuuint64_t dims[3] = {inner, outer, depth};
+  cuuint64_t strides[2] = {ld * esize, dstride * esize};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, dt, rank, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+static bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                          uint64_t ld, uint32_t box_inner, uint32_t box_outer,
+                          CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, inner, outer, ld, box_inner,
+                  box_outer, swz);
 }
 
 template <int BN, bool AMN, bool BMN>
@@ -442,10 +522,10 @@ static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
     attr_done = true;
   }
   CUtensorMap ma, mb;
-  bool ok = AMN ? make_map(&ma, g.A, g.M, g.K, g.lda, 64, 64)
-                : make_map(&ma, g.A, g.K, g.M, g.lda, 64, BM);
-  ok = ok && (BMN ? make_map(&mb, g.B, g.N, g.K, g.ldb, 64, 64)
-                  : make_map(&mb, g.B, g.K, g.N, g.ldb, 64, BN));
+  bool ok = AMN ? make_map_bf16(&ma, g.A, g.M, g.K, g.lda, 64, 64)
+                : make_map_bf16(&ma, g.A, g.K, g.M, g.lda, 64, BM);
+  ok = ok && (BMN ? make_map_bf16(&mb, g.B, g.N, g.K, g.ldb, 64, 64)
+                  : make_map_bf16(&mb, g.B, g.K, g.N, g.ldb, 64, BN));
   if (!ok) return cudaErrorInvalidValue;
   Params p;
   p.M = g.M; p.N = g.N; p.K = g.K;
@@ -456,15 +536,36 @@ static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
   p.kb_per_split = ceil_div(p.num_kb, p.splits);
   p.splits = ceil_div(p.num_kb, p.kb_per_split);
   p.epi = g.epi;
-  p.out = g.out; p.ldo = g.ldo;
+  p.ldo = g.ldo;
   p.bias = (const bf16*)g.bias; p.resid = (const bf16*)g.resid;
-  p.pre = (bf16*)g.pre; p.aux = (const bf16*)g.aux;
-  p.accum = g.accum; p.scale = g.scale; p.workspace = g.workspace;
+  p.aux = (const bf16*)g.aux;
+  p.scale = g.scale;
   p.err = g.err;
   if (p.splits > 1 && !g.workspace) return cudaErrorInvalidValue;
+  if ((g.bias && ((uintptr_t)g.bias & 15u)) || (g.resid && ((uintptr_t)g.resid & 15u)) ||
+      (g.aux && ((uintptr_t)g.aux & 15u)) || (g.ldo % 8))
+    return cudaErrorInvalidValue;
+  EpiMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  if (g.epi == EPI_ACCUM) {
+    if (p.splits == 1)
+      ok = make_map(&maps.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.accum, g.N, g.M, g.ldo, 32,
+                    32, CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+      ok = make_map(&maps.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.workspace, g.N, g.M, g.N,
+                    32, 32, CU_TENSOR_MAP_SWIZZLE_128B, (uint64_t)p.splits,
+                    (uint64_t)g.M * g.N);
+  } else {
+    if (g.epi == EPI_GELU_BWD && !g.aux) return cudaErrorInvalidValue;
+    ok = make_map_bf16(&maps.out, g.out, g.N, g.M, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (ok && g.epi == EPI_GELU_FWD)
+      ok = g.pre && make_map_bf16(&maps.pre, g.pre, g.N, g.M, g.ldo, 32, 32,
+                                  CU_TENSOR_MAP_SWIZZLE_64B);
+  }
+  if (!ok) return cudaErrorInvalidValue;
   const int tiles = p.num_m * p.num_n * p.splits;
   const int grid = tiles < num_sms ? tiles : num_sms;
-  gemm_kernel<BN, AMN, BMN><<<grid, THREADS, Cf::SMEM, s>>>(ma, mb, p); count_launches(1);
+  gemm_kernel<BN, AMN, BMN><<<grid, THREADS, Cf::SMEM, s>>>(ma, mb, maps, p); count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (p.splits > 1) return splitk_reduce(g.accum, g.workspace, p.splits, (long long)g.M * g.N, g.scale, s);
@@ -484,7 +585,12 @@ int gemm_tc_num_sms() {
   return n;
 }
 
-static int pick_bn(int N) { return (N % 256 == 0) ? 256 : 128; }
+// 256-wide tiles unless the columns a partial last tile wastes exceed 1/16 of N (the
+// padded vocabulary, 50304 = 196.5 x 256, keeps 256; N = 384 takes 128).
+static int pick_bn(int N) {
+  const int waste = (256 - N % 256) % 256;
+  return waste * 16 <= N ? 256 : 128;
+}
 
 int gemm_tc_pick_splits(int M, int N, int K, int num_sms) {
   const int bn = pick_bn(N);

@@ -139,6 +139,28 @@ def test_gemm_rejects_unaligned_sizes():
     assert e.value.name == "ARG"
 
 
+@pytest.mark.parametrize("epi", ["store", "gelu_fwd"])
+def test_gemm_partial_last_wide_tile(epi):
+    """N = 16.5 x 256 (as the padded vocabulary, 50304 = 196.5 x 256) keeps 256-wide tiles:
+    the last tile's B rows past N read as zero and its columns past N are not stored.
+    Ragged M as well."""
+    M, N, K = 200, 4224, 128
+    X, W, b = dev(rnd((M, K), 13), torch.bfloat16), dev(rnd((N, K), 14, 0.1), torch.bfloat16), \
+        dev(rnd((N,), 15), torch.bfloat16)
+    out = torch.full((M, N + 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    pre = torch.full((M, N + 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    G.op_gemm("bf16", M, N, K, X, K, False, W, K, False, epi, out=out, ldo=N + 64, bias=b,
+              pre=pre if epi == "gelu_fwd" else None)
+    torch.cuda.synchronize()
+    u = host(X) @ host(W).T + host(b)[None, :]
+    ref = O.gelu(u) if epi == "gelu_fwd" else u
+    assert rel_inf(host(out)[:, :N], ref) < 8e-3
+    assert torch.all(out[:, N:] == 7.0)          # the padding columns are untouched
+    if epi == "gelu_fwd":
+        assert rel_inf(host(pre)[:, :N], u) < 8e-3
+        assert torch.all(pre[:, N:] == 7.0)
+
+
 def test_gemm_large_forward_shape():
     """The 124M model's QKV projection at full size (M = 12 x 1024 tokens), row-sampled."""
     M, N, K = 12288, 2304, 768
