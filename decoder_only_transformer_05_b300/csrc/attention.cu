@@ -266,104 +266,6 @@ __device__ __forceinline__ void zero(float (&a)[8][4]) {
     for (int j = 0; j < 4; ++j) a[i][j] = 0.f;
 }
 
-__global__ void __launch_bounds__(THREADS)
-fwd_kernel(bf16* __restrict__ out, float* __restrict__ lse, const bf16* __restrict__ qkv, int T,
-           int C, int H) {
-  __shared__ __align__(1024) uint8_t sm[5 * TILE_BYTES];
-  const uint32_t Qs = smem_u32(sm), Ks0 = Qs + TILE_BYTES, Vs0 = Qs + 3 * TILE_BYTES;
-  const int nq = gridDim.x;
-  const int qb = nq - 1 - blockIdx.x;              // heavy (late) blocks first
-  const int bh = blockIdx.y, b = bh / H, h = bh % H;
-  const long long ld = 3LL * C;
-  const bf16* base = qkv + (size_t)b * T * ld;
-  const int l = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int g = l >> 2, tq = l & 3;
-  const float sl2 = rsqrtf((float)D) * LOG2E;
-
-  load_tile(Qs, base, qb * BR, T, ld, h * D);
-  load_tile(Ks0, base, 0, T, ld, C + h * D);
-  load_tile(Vs0, base, 0, T, ld, 2 * C + h * D);
-  cp_commit();
-
-  uint32_t qa[4][4];
-  float o[8][4];
-  zero(o);
-  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-  const int r0 = qb * BR + w * 16 + g;   // this thread's rows r0 and r0 + 8
-  const int nkv = qb + 1;
-  for (int kb = 0; kb < nkv; ++kb) {
-    const int buf = kb & 1;
-    if (kb + 1 < nkv) {
-      load_tile(Ks0 + (buf ^ 1) * TILE_BYTES, base, (kb + 1) * BR, T, ld, C + h * D);
-      load_tile(Vs0 + (buf ^ 1) * TILE_BYTES, base, (kb + 1) * BR, T, ld, 2 * C + h * D);
-      cp_commit();
-      cp_wait<1>();
-    } else {
-      cp_wait<0>();
-    }
-    __syncthreads();
-    if (kb == 0) load_a_frags(Qs, w * 16, qa);
-    const uint32_t Ks = Ks0 + buf * TILE_BYTES, Vs = Vs0 + buf * TILE_BYTES;
-    float s[8][4];
-    zero(s);
-    mma_abt(s, qa, Ks);
-    // scale into the log2 domain, mask the future on the diagonal tile
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        int key = kb * BR + nt * 8 + tq * 2 + (e & 1);
-        int row = r0 + (e >> 1) * 8;
-        float v = s[nt][e] * sl2;
-        if (kb == qb && key > row) v = -INFINITY;
-        s[nt][e] = v;
-        mx[e >> 1] = fmaxf(mx[e >> 1], v);
-      }
-    float alpha[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-      float mn = fmaxf(mrow[r], mx[r]);
-      alpha[r] = fast_exp2(mrow[r] - mn);
-      mrow[r] = mn;
-      lrow[r] *= alpha[r];
-    }
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float p = fast_exp2(s[nt][e] - mrow[e >> 1]);
-        s[nt][e] = p;
-        lrow[e >> 1] += p;
-        o[nt][e] *= alpha[e >> 1];
-      }
-    uint32_t pa[4][4];
-    acc_to_a(s, pa);
-    mma_ab(o, pa, Vs);
-    __syncthreads();
-  }
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
-    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
-  }
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int row = r0 + r * 8;
-    if (row >= T) continue;
-    const float inv = 1.0f / lrow[r];
-    bf16* dst = out + ((size_t)b * T + row) * C + h * D;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      uint32_t v = pack_bf16(o[nt][2 * r] * inv, o[nt][2 * r + 1] * inv);
-      *reinterpret_cast<uint32_t*>(dst + nt * 8 + tq * 2) = v;
-    }
-    if (tq == 0) lse[((size_t)b * H + h) * T + row] = (mrow[r] + __log2f(lrow[r])) * (1.0f / LOG2E);
-  }
-}
-
 // D_i = dO_i . O_i, one thread per (b, t, h)
 __global__ void bwd_D_kernel(float* __restrict__ Dbuf, const bf16* __restrict__ dout,
                              const bf16* __restrict__ out, int B, int T, int C, int H) {
@@ -574,13 +476,8 @@ bwd_dq_kernel(bf16* __restrict__ dqkv, const float* __restrict__ Dbuf,
 
 // =====================================================================================
 cudaError_t attention_forward(DType t, void* out, float* lse, const void* qkv, int B, int T, int C,
-                              int H, cudaStream_t s) {
-  if (t == DType::BF16) {
-    if (C / H != fa::D || C % H) return cudaErrorInvalidValue;
-    dim3 grid(ceil_div(T, fa::BR), B * H);
-    fa::fwd_kernel<<<grid, fa::THREADS, 0, s>>>((bf16*)out, lse, (const bf16*)qkv, T, C, H); count_launches(1);
-    return cudaGetLastError();
-  }
+                              int H, int* err, cudaStream_t s) {
+  if (t == DType::BF16) return attention_forward_tc(out, lse, qkv, B, T, C, H, err, s);
   long long warps = (long long)B * H * T;
   attn_fwd_f32_kernel<<<ceil_div(warps, 4), 128, 4 * T * sizeof(float), s>>>(
       (float*)out, lse, (const float*)qkv, B, T, C, H); count_launches(1);

@@ -504,7 +504,7 @@ extern "C" int gpt2_forward(gpt2_handle h, const int32_t* tokens, const int32_t*
     if (h->bias) g.bias = h->pw(T_QKVB, l);
     CKL(run_gemm(h, g));
     pi = prof_begin(h, PC_ATTN);
-    CKL(attention_forward(dt, h->att[l], h->lse[l], h->qkv[l], B, T, C, H, s));
+    CKL(attention_forward(dt, h->att[l], h->lse[l], h->qkv[l], B, T, C, H, h->d_err, s));
     prof_end(h, pi, 2.0 * 2.0 * B * H * (double)T * (T + 1) / 2 * (C / H));
     g = linear_fwd(M, C, C, h->att[l], h->pw(T_ATTPROJW, l), h->xmid[l]);
     if (h->bias) g.bias = h->pw(T_ATTPROJB, l);

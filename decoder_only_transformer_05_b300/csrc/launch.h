@@ -95,9 +95,12 @@ cudaError_t bias_grad(DType t, float* db, const void* dy, int M, int N, float sc
                       float* partials, cudaStream_t s);
 
 // ---------------------------------------------------------------- attention
-// qkv [B, T, 3C] -> out [B, T, C], lse [B, H, T] (natural log)
+// qkv [B, T, 3C] -> out [B, T, C], lse [B, H, T] (natural log). The bf16 path runs the
+// tcgen05 kernel (head size 64; err, when non-null, receives DEV_ERR_TIMEOUT).
 cudaError_t attention_forward(DType t, void* out, float* lse, const void* qkv, int B, int T, int C,
-                              int H, cudaStream_t s);
+                              int H, int* err, cudaStream_t s);
+cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, int T, int C,
+                                 int H, int* err, cudaStream_t s);
 // dout [B, T, C] -> dqkv [B, T, 3C]; Dbuf [B, H, T] scratch
 cudaError_t attention_backward(DType t, void* dqkv, float* Dbuf, const void* dout,
                                const void* out, const void* qkv, const float* lse, int B, int T,

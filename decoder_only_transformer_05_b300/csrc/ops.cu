@@ -42,7 +42,7 @@ extern "C" int gpt2_op_gemm(int precision, int M, int N, int K, const void* A, i
 
 extern "C" int gpt2_op_attention_forward(int precision, void* out, float* lse, const void* qkv,
                                          int B, int T, int C, int H, void* stream) {
-  return status(attention_forward(dtype(precision), out, lse, qkv, B, T, C, H,
+  return status(attention_forward(dtype(precision), out, lse, qkv, B, T, C, H, nullptr,
                                   (cudaStream_t)stream));
 }
 
