@@ -486,25 +486,15 @@ cudaError_t attention_forward(DType t, void* out, float* lse, const void* qkv, i
 
 cudaError_t attention_backward(DType t, void* dqkv, float* Dbuf, const void* dout,
                                const void* out, const void* qkv, const float* lse, int B, int T,
-                               int C, int H, cudaStream_t s) {
+                               int C, int H, int* err, cudaStream_t s) {
   if (t == DType::BF16) {
-    if (C / H != fa::D || C % H) return cudaErrorInvalidValue;
+    if (C / H != fa::D || C % H || T % 4) return cudaErrorInvalidValue;
     long long n = (long long)B * T * H;
     fa::bwd_D_kernel<<<ceil_div(n, 256), 256, 0, s>>>(Dbuf, (const bf16*)dout, (const bf16*)out,
                                                       B, T, C, H); count_launches(1);
-    dim3 grid(ceil_div(T, fa::BR), B * H);
-    const int sm = 6 * fa::TILE_BYTES;
-    static bool attr = false;
-    if (!attr) {
-      cudaFuncSetAttribute(fa::bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-      cudaFuncSetAttribute(fa::bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-      attr = true;
-    }
-    fa::bwd_dkv_kernel<<<grid, fa::THREADS, sm, s>>>((bf16*)dqkv, Dbuf, (const bf16*)dout,
-                                                     (const bf16*)qkv, lse, T, C, H); count_launches(1);
-    fa::bwd_dq_kernel<<<grid, fa::THREADS, sm, s>>>((bf16*)dqkv, Dbuf, (const bf16*)dout,
-                                                    (const bf16*)qkv, lse, T, C, H); count_launches(1);
-    return cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return attention_backward_tc(dqkv, Dbuf, dout, qkv, lse, B, T, C, H, err, s);
   }
   long long warps = (long long)B * H * T;
   int blocks = ceil_div(warps, 4);

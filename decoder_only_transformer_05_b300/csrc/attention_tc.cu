@@ -276,6 +276,470 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
   }
 }
 
+// =====================================================================================
+// Backward. With P recomputed from the forward's lse (P = exp2(s sl2 - lse log2 e)) and
+// D = rowsum(dO * O), every element is independent: dS = P (dP - D), dP = dO V^T, and
+//   dV = P^T dO,  dK = dS^T Q / sqrt(64),  dQ = dS K / sqrt(64).
+// Two kernels, each owning its output rows, so no partial sums cross blocks and the
+// result is deterministic. 320 threads: warp 0 TMA, warp 1 MMA, warps 2..9 elementwise
+// (warp w reads TMEM lane quarter w % 4; warps w and w + 4 take columns 0..63 and 64..127).
+constexpr int BWD_THREADS = 320;
+constexpr int BWD_STAGES = 2;
+
+struct BwdParams {
+  int T, H, C, nqb;
+  const float* lse;
+  const float* Dbuf;
+  int* err;
+};
+
+// dK, dV for one block of 128 keys; loops over the query blocks at or after it.
+//   S^T = K Q_i^T, dP^T = V dO_i^T (TMEM, 128 + 128 columns), then
+//   dV += P^T dO_i, dK += dS^T Q_i (TMEM, 64 + 64 columns) with P^T and dS^T staged as
+//   bf16 in shared memory (the A operands).
+constexpr int DKV_SM_K = 0;
+constexpr int DKV_SM_V = DKV_SM_K + TILE;
+constexpr int DKV_SM_QD = DKV_SM_V + TILE;                       // stage s: Q at +2s, dO at +2s+1
+constexpr int DKV_SM_PT = DKV_SM_QD + 2 * BWD_STAGES * TILE;     // P^T, two 64-query halves
+constexpr int DKV_SM_DST = DKV_SM_PT + 2 * TILE;                 // dS^T
+constexpr int DKV_SM_LD = DKV_SM_DST + 2 * TILE;                 // stage s: [lse 128 | D 128]
+constexpr int DKV_SM_BAR = DKV_SM_LD + BWD_STAGES * 256 * 4;
+constexpr int DKV_SMEM = DKV_SM_BAR + 256 + 1024;
+
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
+               const __grid_constant__ CUtensorMap tm_dqkv, const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bars = base + DKV_SM_BAR;
+  // barriers: kv_full, qd_full[S], qd_empty[S], s_full, s_empty, p_full, done, final
+  const uint32_t kv_full = bars;
+  auto qd_full = [&](int s) { return bars + 8u * (1 + s); };
+  auto qd_empty = [&](int s) { return bars + 8u * (1 + BWD_STAGES + s); };
+  const uint32_t s_full = bars + 8u * (1 + 2 * BWD_STAGES);
+  const uint32_t s_empty = bars + 8u * (2 + 2 * BWD_STAGES);
+  const uint32_t p_full = bars + 8u * (3 + 2 * BWD_STAGES);
+  const uint32_t done = bars + 8u * (4 + 2 * BWD_STAGES);
+  const uint32_t final_bar = bars + 8u * (5 + 2 * BWD_STAGES);
+  const uint32_t slot = bars + 8u * (6 + 2 * BWD_STAGES);
+  volatile uint32_t* slot_ptr = (volatile uint32_t*)(base_ptr + DKV_SM_BAR + 8 * (6 + 2 * BWD_STAGES));
+  volatile int* abort_flag = (volatile int*)(base_ptr + DKV_SM_BAR + 8 * (7 + 2 * BWD_STAGES));
+  float* sm_ld = reinterpret_cast<float*>(base_ptr + DKV_SM_LD);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kb = blockIdx.x;                        // key block; query blocks kb..nqb-1
+  const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
+  const int n = p.nqb - kb;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < BWD_STAGES; ++s) { mbar_init(qd_full(s), 1); mbar_init(qd_empty(s), 1); }
+    mbar_init(s_full, 1);
+    mbar_init(s_empty, 8);
+    mbar_init(p_full, 8);
+    mbar_init(done, 1);
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot_ptr;
+  constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 320;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      mbar_expect_tx(kv_full, 2 * TILE);
+      tma_load_3d(base + DKV_SM_K, &tm_qkv, kv_full, p.C + h * D, kb * BKV, b);
+      tma_load_3d(base + DKV_SM_V, &tm_qkv, kv_full, 2 * p.C + h * D, kb * BKV, b);
+      int i = 0;
+      for (; i < n && ok; ++i) {
+        const int s = i % BWD_STAGES;
+        if (!mbar_wait(qd_empty(s), ((uint32_t)(i / BWD_STAGES) & 1u) ^ 1u, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = base + DKV_SM_QD + 2 * s * TILE;
+        const int qbi = kb + i;
+        // lse and D of the block's queries ride with the Q / dO tiles (T % 4 == 0, so the
+        // row start and the byte count are multiples of 16)
+        const uint32_t nb = (uint32_t)min(BQ, p.T - qbi * BQ) * 4u;
+        const size_t t0 = (size_t)bh * p.T + (size_t)qbi * BQ;
+        mbar_expect_tx(qd_full(s), 2 * TILE + 2 * nb);
+        tma_load_3d(dst, &tm_qkv, qd_full(s), h * D, qbi * BQ, b);
+        tma_load_3d(dst + TILE, &tm_do, qd_full(s), h * D, qbi * BQ, b);
+        const uint32_t ld_dst = base + DKV_SM_LD + s * 1024;
+        bulk_load(ld_dst, p.lse + t0, nb, qd_full(s));
+        bulk_load(ld_dst + 512, p.Dbuf + t0, nb, qd_full(s));
+      }
+      mbar_wait(kv_full, 0, abort_flag, nullptr, false);
+      for (int k = max(0, i - BWD_STAGES); k < i; ++k)
+        mbar_wait(qd_full(k % BWD_STAGES), (uint32_t)(k / BWD_STAGES) & 1u, abort_flag, nullptr,
+                  false);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = make_idesc(BKV, BQ, false, false);
+      constexpr uint32_t IDESC_G = make_idesc(BKV, D, false, true);
+      bool ok = mbar_wait(kv_full, 0, abort_flag, p.err);
+      auto issue_s = [&](int i) -> bool {
+        const int s = i % BWD_STAGES;
+        if (!mbar_wait(qd_full(s), (uint32_t)(i / BWD_STAGES) & 1u, abort_flag, p.err)) return false;
+        if (i >= 1 && !mbar_wait(s_empty, (uint32_t)(i - 1) & 1u, abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint32_t qa = base + DKV_SM_QD + 2 * s * TILE, da = qa + TILE;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          umma_bf16(tmem + COL_S, sdesc(base + DKV_SM_K + k * 32, 16, 1024),
+                    sdesc(qa + k * 32, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+          umma_bf16(tmem + COL_DP, sdesc(base + DKV_SM_V + k * 32, 16, 1024),
+                    sdesc(da + k * 32, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+        }
+        umma_commit(s_full);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int i = 0; i < n && ok; ++i) {
+        if (i + 1 < n && !issue_s(i + 1)) { ok = false; break; }
+        if (!mbar_wait(p_full, (uint32_t)i & 1u, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t qa = base + DKV_SM_QD + 2 * (i % BWD_STAGES) * TILE, da = qa + TILE;
+#pragma unroll
+        for (int k = 0; k < BQ / 16; ++k) {
+          const uint32_t off = (k >> 2) * TILE + (k & 3) * 32;
+          umma_bf16(tmem + COL_DV, sdesc(base + DKV_SM_PT + off, 16, 1024),
+                    sdesc(da + k * 2048, 16384, 1024), IDESC_G, (i > 0 || k > 0) ? 1u : 0u);
+          umma_bf16(tmem + COL_DK, sdesc(base + DKV_SM_DST + off, 16, 1024),
+                    sdesc(qa + k * 2048, 16384, 1024), IDESC_G, (i > 0 || k > 0) ? 1u : 0u);
+        }
+        umma_commit(done);
+        umma_commit(qd_empty(i % BWD_STAGES));
+      }
+      umma_commit(final_bar);
+      mbar_wait(final_bar, 0, abort_flag, nullptr, false);
+    }
+  } else {
+    // ---------------- elementwise warps: key row r, query columns c0 .. c0 + 63
+    const int q = warp & 3, half = (warp - 2) >> 2;
+    const int r = q * 32 + lane, c0 = half * 64;
+    const int key = kb * BKV + r;
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const float sl2 = rsqrtf((float)D) * LOG2E;
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      // this stage's lse and D (copied with Q_i, dO_i); the stage is not refilled before
+      // the MMAs that follow p_full(i) have finished
+      const float* ld = sm_ld + (i % BWD_STAGES) * 256;
+      ok = mbar_wait(qd_full(i % BWD_STAGES), (uint32_t)(i / BWD_STAGES) & 1u, abort_flag, p.err) &&
+           mbar_wait(s_full, (uint32_t)i & 1u, abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sv[2][32], dv[2][32];
+      tmem_ld32_nowait(lane_base + COL_S + c0, sv[0]);
+      tmem_ld32_nowait(lane_base + COL_S + c0 + 32, sv[1]);
+      tmem_ld32_nowait(lane_base + COL_DP + c0, dv[0]);
+      tmem_ld32_nowait(lane_base + COL_DP + c0 + 32, dv[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_empty);
+      const int qbase = (kb + i) * BQ + c0;
+      uint32_t pk[32], dk[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pp[2], dd[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int qc = c * 32 + e + u;           // query column within this half
+            const int query = qbase + qc;
+            float pv = fast_exp2(fmaf(__uint_as_float(sv[c][e + u]), sl2, -ld[c0 + qc] * LOG2E));
+            if (query < key || query >= p.T) pv = 0.f;
+            pp[u] = pv;
+            dd[u] = pv * (__uint_as_float(dv[c][e + u]) - ld[128 + c0 + qc]);
+          }
+          pk[c * 16 + e / 2] = pack2_bf16(pp[0], pp[1]);
+          dk[c * 16 + e / 2] = pack2_bf16(dd[0], dd[1]);
+        }
+      if (i > 0) {
+        ok = mbar_wait(done, (uint32_t)(i - 1) & 1u, abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      }
+      // rows of P^T and dS^T: this half's 64 queries are one 128-byte swizzled row
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t off = half * TILE + r * 128 + ((u ^ (r & 7)) << 4);
+        st_shared16(base + DKV_SM_PT + off,
+                    make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
+        st_shared16(base + DKV_SM_DST + off,
+                    make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]));
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (ok) ok = mbar_wait(done, (uint32_t)(n - 1) & 1u, abort_flag, p.err);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      // this warp's 32 of the 64 head columns of dK and dV, into the (now free) Q/dO stage 0
+      uint32_t kv[2][32];
+      tmem_ld32_nowait(lane_base + COL_DK + half * 32, kv[0]);
+      tmem_ld32_nowait(lane_base + COL_DV + half * 32, kv[1]);
+      tmem_wait_ld();
+      const float scale = rsqrtf((float)D);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const float sc = t == 0 ? scale : 1.0f;
+        const uint32_t stg = base + DKV_SM_QD + t * TILE;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t* v = &kv[t][u * 8];
+          const int unit = half * 4 + u;
+          st_shared16(stg + r * 128 + ((unit ^ (r & 7)) << 4),
+                      make_uint4(pack2_bf16(__uint_as_float(v[0]) * sc, __uint_as_float(v[1]) * sc),
+                                 pack2_bf16(__uint_as_float(v[2]) * sc, __uint_as_float(v[3]) * sc),
+                                 pack2_bf16(__uint_as_float(v[4]) * sc, __uint_as_float(v[5]) * sc),
+                                 pack2_bf16(__uint_as_float(v[6]) * sc, __uint_as_float(v[7]) * sc)));
+        }
+      }
+      fence_proxy_async();
+    }
+    named_bar_sync(1, 256);
+    if (threadIdx.x == 64 && ok) {
+      tma_store_3d(&tm_dqkv, base + DKV_SM_QD, p.C + h * D, kb * BKV, b);
+      tma_store_3d(&tm_dqkv, base + DKV_SM_QD + TILE, 2 * p.C + h * D, kb * BKV, b);
+      bulk_commit();
+      bulk_wait_all();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// dQ for one block of 128 queries; loops over the key blocks up to the diagonal.
+//   S = Q K_j^T, dP = dO V_j^T (TMEM), dS = P (dP - D) as bf16 in shared memory, then
+//   dQ += dS K_j (TMEM, 64 columns).
+constexpr int DQ_SM_Q = 0;
+constexpr int DQ_SM_DO = DQ_SM_Q + TILE;
+constexpr int DQ_SM_KV = DQ_SM_DO + TILE;                        // stage s: K at +2s, V at +2s+1
+constexpr int DQ_SM_DS = DQ_SM_KV + 2 * BWD_STAGES * TILE;
+constexpr int DQ_SM_BAR = DQ_SM_DS + 2 * TILE;
+constexpr int DQ_SMEM = DQ_SM_BAR + 256 + 1024;
+
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
+              const __grid_constant__ CUtensorMap tm_dqkv, const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bars = base + DQ_SM_BAR;
+  const uint32_t q_full = bars;
+  auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
+  auto kv_empty = [&](int s) { return bars + 8u * (1 + BWD_STAGES + s); };
+  const uint32_t s_full = bars + 8u * (1 + 2 * BWD_STAGES);
+  const uint32_t s_empty = bars + 8u * (2 + 2 * BWD_STAGES);
+  const uint32_t p_full = bars + 8u * (3 + 2 * BWD_STAGES);
+  const uint32_t done = bars + 8u * (4 + 2 * BWD_STAGES);
+  const uint32_t final_bar = bars + 8u * (5 + 2 * BWD_STAGES);
+  const uint32_t slot = bars + 8u * (6 + 2 * BWD_STAGES);
+  volatile uint32_t* slot_ptr = (volatile uint32_t*)(base_ptr + DQ_SM_BAR + 8 * (6 + 2 * BWD_STAGES));
+  volatile int* abort_flag = (volatile int*)(base_ptr + DQ_SM_BAR + 8 * (7 + 2 * BWD_STAGES));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qb = p.nqb - 1 - (int)blockIdx.x;
+  const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
+  const int n = qb + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < BWD_STAGES; ++s) { mbar_init(kv_full(s), 1); mbar_init(kv_empty(s), 1); }
+    mbar_init(s_full, 1);
+    mbar_init(s_empty, 8);
+    mbar_init(p_full, 8);
+    mbar_init(done, 1);
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot_ptr;
+  constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      mbar_expect_tx(q_full, 2 * TILE);
+      tma_load_3d(base + DQ_SM_Q, &tm_qkv, q_full, h * D, qb * BQ, b);
+      tma_load_3d(base + DQ_SM_DO, &tm_do, q_full, h * D, qb * BQ, b);
+      int j = 0;
+      for (; j < n && ok; ++j) {
+        const int s = j % BWD_STAGES;
+        if (!mbar_wait(kv_empty(s), ((uint32_t)(j / BWD_STAGES) & 1u) ^ 1u, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = base + DQ_SM_KV + 2 * s * TILE;
+        mbar_expect_tx(kv_full(s), 2 * TILE);
+        tma_load_3d(dst, &tm_qkv, kv_full(s), p.C + h * D, j * BKV, b);
+        tma_load_3d(dst + TILE, &tm_qkv, kv_full(s), 2 * p.C + h * D, j * BKV, b);
+      }
+      mbar_wait(q_full, 0, abort_flag, nullptr, false);
+      for (int k = max(0, j - BWD_STAGES); k < j; ++k)
+        mbar_wait(kv_full(k % BWD_STAGES), (uint32_t)(k / BWD_STAGES) & 1u, abort_flag, nullptr,
+                  false);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = make_idesc(BQ, BKV, false, false);
+      constexpr uint32_t IDESC_G = make_idesc(BQ, D, false, true);
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
+      auto issue_s = [&](int j) -> bool {
+        const int s = j % BWD_STAGES;
+        if (!mbar_wait(kv_full(s), (uint32_t)(j / BWD_STAGES) & 1u, abort_flag, p.err)) return false;
+        if (j >= 1 && !mbar_wait(s_empty, (uint32_t)(j - 1) & 1u, abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint32_t ka = base + DQ_SM_KV + 2 * s * TILE, va = ka + TILE;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          umma_bf16(tmem + COL_S, sdesc(base + DQ_SM_Q + k * 32, 16, 1024),
+                    sdesc(ka + k * 32, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+          umma_bf16(tmem + COL_DP, sdesc(base + DQ_SM_DO + k * 32, 16, 1024),
+                    sdesc(va + k * 32, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+        }
+        umma_commit(s_full);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; j < n && ok; ++j) {
+        if (j + 1 < n && !issue_s(j + 1)) { ok = false; break; }
+        if (!mbar_wait(p_full, (uint32_t)j & 1u, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t ka = base + DQ_SM_KV + 2 * (j % BWD_STAGES) * TILE;
+#pragma unroll
+        for (int k = 0; k < BKV / 16; ++k)
+          umma_bf16(tmem + COL_DQ, sdesc(base + DQ_SM_DS + (k >> 2) * TILE + (k & 3) * 32, 16, 1024),
+                    sdesc(ka + k * 2048, 16384, 1024), IDESC_G, (j > 0 || k > 0) ? 1u : 0u);
+        umma_commit(done);
+        umma_commit(kv_empty(j % BWD_STAGES));
+      }
+      umma_commit(final_bar);
+      mbar_wait(final_bar, 0, abort_flag, nullptr, false);
+    }
+  } else {
+    // ---------------- elementwise warps: query row r, key columns c0 .. c0 + 63
+    const int q = warp & 3, half = (warp - 2) >> 2;
+    const int r = q * 32 + lane, c0 = half * 64;
+    const int query = qb * BQ + r;
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const float sl2 = rsqrtf((float)D) * LOG2E;
+    float lse2 = 0.f, Dr = 0.f;
+    if (query < p.T) {
+      lse2 = __ldg(p.lse + (size_t)bh * p.T + query) * LOG2E;
+      Dr = __ldg(p.Dbuf + (size_t)bh * p.T + query);
+    }
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      ok = mbar_wait(s_full, (uint32_t)j & 1u, abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sv[2][32], dv[2][32];
+      tmem_ld32_nowait(lane_base + COL_S + c0, sv[0]);
+      tmem_ld32_nowait(lane_base + COL_S + c0 + 32, sv[1]);
+      tmem_ld32_nowait(lane_base + COL_DP + c0, dv[0]);
+      tmem_ld32_nowait(lane_base + COL_DP + c0 + 32, dv[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_empty);
+      const int kbase = j * BKV + c0;
+      uint32_t dk[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float dd[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int kc = kbase + c * 32 + e + u;
+            float pv = fast_exp2(fmaf(__uint_as_float(sv[c][e + u]), sl2, -lse2));
+            if (kc > query) pv = 0.f;
+            dd[u] = pv * (__uint_as_float(dv[c][e + u]) - Dr);
+          }
+          dk[c * 16 + e / 2] = pack2_bf16(dd[0], dd[1]);
+        }
+      if (j > 0) {
+        ok = mbar_wait(done, (uint32_t)(j - 1) & 1u, abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        st_shared16(base + DQ_SM_DS + half * TILE + r * 128 + ((u ^ (r & 7)) << 4),
+                    make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]));
+      fence_proxy_async();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (ok) ok = mbar_wait(done, (uint32_t)(n - 1) & 1u, abort_flag, p.err);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      uint32_t v[32];
+      tmem_ld32_nowait(lane_base + COL_DQ + half * 32, v);
+      tmem_wait_ld();
+      const float sc = rsqrtf((float)D);
+      const uint32_t stg = base + DQ_SM_Q;     // Q is no longer read
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t* w = &v[u * 8];
+        const int unit = half * 4 + u;
+        st_shared16(stg + r * 128 + ((unit ^ (r & 7)) << 4),
+                    make_uint4(pack2_bf16(__uint_as_float(w[0]) * sc, __uint_as_float(w[1]) * sc),
+                               pack2_bf16(__uint_as_float(w[2]) * sc, __uint_as_float(w[3]) * sc),
+                               pack2_bf16(__uint_as_float(w[4]) * sc, __uint_as_float(w[5]) * sc),
+                               pack2_bf16(__uint_as_float(w[6]) * sc, __uint_as_float(w[7]) * sc)));
+      }
+      fence_proxy_async();
+    }
+    named_bar_sync(1, 256);
+    if (threadIdx.x == 64 && ok) {
+      tma_store_3d(&tm_dqkv, base + DQ_SM_Q, h * D, qb * BQ, b);
+      bulk_commit();
+      bulk_wait_all();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 // [B][T][width] bf16 as a 3-D map {width, T, B}, box {64, 128, 1}, 128-byte swizzle
 static bool map_btw(CUtensorMap* m, const void* ptr, int B, int T, int width) {
@@ -311,6 +775,39 @@ cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, 
   p.err = err;
   dim3 grid(p.nqb, B * H);
   fwd_kernel<<<grid, THREADS, SMEM, s>>>(mq, mo, p);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t attention_backward_tc(void* dqkv, const float* Dbuf, const void* dout,
+                                  const void* qkv, const float* lse, int B, int T, int C, int H,
+                                  int* err, cudaStream_t s) {
+  using namespace fatc;
+  if (C / H != D || C % H || C % 64 || T % 4 || ((uintptr_t)lse & 15u) || ((uintptr_t)Dbuf & 15u))
+    return cudaErrorInvalidValue;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_dkv_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, DKV_SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               DQ_SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  CUtensorMap mq, md, mg;
+  if (!map_btw(&mq, qkv, B, T, 3 * C) || !map_btw(&md, dout, B, T, C) ||
+      !map_btw(&mg, dqkv, B, T, 3 * C))
+    return cudaErrorInvalidValue;
+  BwdParams p;
+  p.T = T; p.H = H; p.C = C; p.nqb = ceil_div(T, BQ);
+  p.lse = lse; p.Dbuf = Dbuf; p.err = err;
+  dim3 grid(p.nqb, B * H);
+  bwd_dkv_kernel<<<grid, BWD_THREADS, DKV_SMEM, s>>>(mq, md, mg, p);
+  count_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_dq_kernel<<<grid, BWD_THREADS, DQ_SMEM, s>>>(mq, md, mg, p);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -551,6 +551,8 @@ extern "C" int gpt2_forward(gpt2_handle h, const int32_t* tokens, const int32_t*
 extern "C" int gpt2_backward(gpt2_handle h, float loss_scale) {
   if (!h) return fail(GPT2_ERR_ARG, "null handle");
   if (!h->have_targets) return fail(GPT2_ERR_STATE, "backward needs a forward with targets");
+  if (h->is_bf16 && h->last_T % 4)
+    return fail(GPT2_ERR_ARG, "the bf16 backward needs T %% 4 == 0 (T = %d)", h->last_T);
   const int B = h->last_B, T = h->last_T, M = B * T, C = h->C, L = h->L, H = h->H, Vp = h->Vp;
   const DType dt = h->dt;
   cudaStream_t s = h->stream;
@@ -597,7 +599,7 @@ extern "C" int gpt2_backward(gpt2_handle h, float loss_scale) {
     CKL(run_gemm(h, linear_wgrad(M, C, C, h->dres, h->att[l], h->gw(T_ATTPROJW, l), sc)));
     pi = prof_begin(h, PC_ATTN);
     CKL(attention_backward(dt, h->dqkv, h->Dbuf, h->datt, h->att[l], h->qkv[l], h->lse[l], B, T,
-                           C, H, s));
+                           C, H, h->d_err, s));
     prof_end(h, pi, 2.5 * 2.0 * 2.0 * B * H * (double)T * (T + 1) / 2 * (C / H));
     // qkv = ln1 Wqkv^T + bqkv
     CKL(run_gemm(h, linear_dgrad(M, 3 * C, C, h->dqkv, h->pw(T_QKVW, l), h->dln)));

@@ -101,10 +101,14 @@ cudaError_t attention_forward(DType t, void* out, float* lse, const void* qkv, i
                               int H, int* err, cudaStream_t s);
 cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, int T, int C,
                                  int H, int* err, cudaStream_t s);
-// dout [B, T, C] -> dqkv [B, T, 3C]; Dbuf [B, H, T] scratch
+// dout [B, T, C] -> dqkv [B, T, 3C]; Dbuf [B, H, T] scratch. The bf16 path runs D =
+// rowsum(dout * out) and then the tcgen05 dK/dV and dQ kernels (needs T % 4 == 0).
 cudaError_t attention_backward(DType t, void* dqkv, float* Dbuf, const void* dout,
                                const void* out, const void* qkv, const float* lse, int B, int T,
-                               int C, int H, cudaStream_t s);
+                               int C, int H, int* err, cudaStream_t s);
+cudaError_t attention_backward_tc(void* dqkv, const float* Dbuf, const void* dout,
+                                  const void* qkv, const float* lse, int B, int T, int C, int H,
+                                  int* err, cudaStream_t s);
 
 // ---------------------------------------------------------------- optimiser
 // partials: norm_partials_count() floats; out[0] = ||g||, out[1] = clip coefficient

@@ -51,7 +51,7 @@ extern "C" int gpt2_op_attention_backward(int precision, void* dqkv, float* Dbuf
                                           const float* lse, int B, int T, int C, int H,
                                           void* stream) {
   return status(attention_backward(dtype(precision), dqkv, Dbuf, dout, out, qkv, lse, B, T, C,
-                                   H, (cudaStream_t)stream));
+                                   H, nullptr, (cudaStream_t)stream));
 }
 
 extern "C" int gpt2_op_layernorm_forward(int precision, void* y, float* mean, float* rstd,

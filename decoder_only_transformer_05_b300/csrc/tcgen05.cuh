@@ -151,6 +151,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "l"((unsigned long long)map), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// contiguous global -> shared copy of `bytes` (16-byte aligned, multiple of 16)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"((unsigned long long)src), "r"(bytes), "r"(bar) : "memory");
+}
 // named barrier over `count` threads (a multiple of 32), id 1..15
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -176,7 +176,8 @@ def test_gemm_large_forward_shape():
 
 
 # ------------------------------------------------------------------- attention
-@pytest.mark.parametrize("B,T,H,hs", [(2, 256, 2, 64), (1, 1024, 12, 64), (2, 100, 3, 64)])
+@pytest.mark.parametrize("B,T,H,hs", [(2, 256, 2, 64), (1, 1024, 12, 64), (2, 100, 3, 64),
+                                      (3, 388, 2, 64)])
 def test_attention_bf16(B, T, H, hs):
     C = H * hs
     qkv = dev(rnd((B, T, 3 * C), 20), torch.bfloat16)
@@ -203,6 +204,18 @@ def test_attention_bf16(B, T, H, hs):
         sl = slice(part * C, (part + 1) * C)
         assert cosine(got[..., sl], ref_d[..., sl]) > 0.999, part
         assert rel_inf(got[..., sl], ref_d[..., sl]) < 3e-2, part
+
+
+def test_attention_bf16_backward_rejects_t_not_multiple_of_4():
+    B, T, H, C = 1, 66, 1, 64
+    qkv = torch.zeros(B, T, 3 * C, dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(B, T, C, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(B, H, T, dtype=torch.float32, device="cuda")
+    dqkv = torch.zeros_like(qkv)
+    Dbuf = torch.zeros_like(lse)
+    with pytest.raises(G.GPT2Error) as e:
+        G.op_attention_backward("bf16", dqkv, Dbuf, out, out, qkv, lse, B, T, C, H)
+    assert e.value.name == "ARG"
 
 
 def test_attention_fp32():
