@@ -4,21 +4,31 @@
 // dot-product attention of 「从零实现一个最小GPT：代码讲解 + 知识点全解」 二.3 Head / 三.3,
 // with the fused multi-head layout of the qkv projection).
 //
-// Forward: one block per (batch, head, 128 query rows), 192 threads.
-//   warp 0      TMA producer: the Q tile once, then K_j, V_j (128 keys x 64) into a ring
-//               of KV_STAGES stages
-//   warp 1      MMA issuer: S_j = Q K_j^T (M=128, N=128, K=64) into one of two TMEM score
-//               buffers, issued one block ahead; O += P_j V_j (M=128, N=64, K=128) into a
-//               TMEM accumulator once the softmax has written P_j
-//   warps 2..5  softmax: thread = query row (TMEM lane). Online softmax in registers in
-//               the log2 domain: m = running max, l = running sum; P_j = exp2(s - m) as
-//               bf16 into a swizzled shared-memory tile (the A operand of P V); when m
-//               grows, O is rescaled in tensor memory before P_j V_j is issued. At the end
-//               O / l goes out through a TMA store and lse = ln(l) + m ln 2 to memory.
+// All three kernels are persistent: one 320-thread block per SM walks a fixed list of
+// work units (heaviest first, unit c, c + G, c + 2G, ... for block c of G), and the TMA
+// ring runs on across units so the next unit's tiles load while this one computes.
+//   warp 0      TMA producer (Q / K / V / dO tiles of 128 rows x 64, 128-byte swizzle)
+//   warp 1      MMA issuer (one thread; tcgen05.mma, fp32 accumulators in tensor memory)
+//   warps 2..9  elementwise: warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31
+// Each elementwise warp stores its own 32 output rows with a TMA store from its own slice
+// of shared memory, so no barrier spans more than one warp. Every mbarrier wait is
+// bounded; on timeout the block records DEV_ERR_TIMEOUT and stops.
+//
+// Forward (unit = one (batch, head) and two consecutive 128-query tiles A, B):
+//   S_X = Q_X K_j^T (TMEM, 128 columns per tile), softmax by the tile's four warps (thread =
+//   query row) with an online max m and sum l in the log2 domain, P_X = exp2(s - m) as bf16
+//   into shared memory, O_X += P_X V_j (TMEM, 64 columns per tile). m only moves when the
+//   block's maximum exceeds it by more than 8 (P then stays below 2^8), and O is rescaled in
+//   tensor memory when it does. The two tiles' softmax warps run side by side and share
+//   every K, V tile.
+// Backward (D = rowsum(dO * O) from a separate kernel; P = exp2(s sl2 - lse log2 e)):
+//   dK/dV unit = (batch, head, 128 keys): S^T = K Q_i^T, dP^T = V dO_i^T, then
+//   dV += P^T dO_i, dK += dS^T Q_i with dS = P (dP - D); dQ unit = (batch, head, 128
+//   queries): S = Q K_j^T, dP = dO V_j^T, dQ += dS K_j. Each output row belongs to one
+//   unit, so the result is deterministic. The eight elementwise warps split the columns
+//   (warps w and w + 4 take 64 each): no row reduction is needed once lse and D are known.
 // Rows past T (ragged T) read zeros through the 3-D tensor maps and are never stored.
-// Every mbarrier wait is bounded; on timeout the block records DEV_ERR_TIMEOUT and leaves.
 #include <cstring>
-#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -31,241 +41,364 @@ using namespace tc;
 
 constexpr int D = 64;
 constexpr int BQ = 128, BKV = 128;
-constexpr int THREADS = 192;
-constexpr int KV_STAGES = 3;
+constexpr int THREADS = 320;
 constexpr int TILE = BQ * D * 2;                 // 16 KB: 128 rows x 128 B
-constexpr int SM_Q = 0;
-constexpr int SM_KV = SM_Q + TILE;               // stage s: K at +2s*TILE, V at +(2s+1)*TILE
-constexpr int SM_P = SM_KV + 2 * KV_STAGES * TILE;   // two 64-key halves of P
-constexpr int SM_BAR = SM_P + 2 * TILE;
-constexpr int SMEM = SM_BAR + 256 + 1024;
-constexpr uint32_t TMEM_COLS = 512;              // S0 [0,128) S1 [128,256) O [256,320)
-constexpr uint32_t COL_O = 256;
+constexpr uint32_t TMEM_COLS = 512;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
+constexpr float RESCALE_LOG2 = 8.0f;             // move the running max only past this margin
 
-struct FwdParams {
-  int T, H, C, nqb;
-  float* lse;
+// phase parity of the n-th completion (n = 0, 1, ...) of a barrier
+__device__ __forceinline__ uint32_t par(int n) { return (uint32_t)n & 1u; }
+
+// Row r (0..31 within the warp's slice) of a 32 x 64 bf16 tile, 128 B per row, 128-byte
+// swizzle: 16-byte unit u of the row at unit u ^ (r & 7).
+__device__ __forceinline__ void stage_row64(uint32_t slice, int r, const float* v, float sc) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    st_shared16(slice + r * 128 + ((u ^ (r & 7)) << 4),
+                make_uint4(pack2_bf16(v[8 * u] * sc, v[8 * u + 1] * sc),
+                           pack2_bf16(v[8 * u + 2] * sc, v[8 * u + 3] * sc),
+                           pack2_bf16(v[8 * u + 4] * sc, v[8 * u + 5] * sc),
+                           pack2_bf16(v[8 * u + 6] * sc, v[8 * u + 7] * sc)));
+}
+// Row r of a 32 x 32 bf16 tile, 64 B per row, 64-byte swizzle: unit u at u ^ ((r >> 1) & 3).
+__device__ __forceinline__ void stage_row32(uint32_t slice, int r, const float* v, float sc) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    st_shared16(slice + r * 64 + ((u ^ ((r >> 1) & 3)) << 4),
+                make_uint4(pack2_bf16(v[8 * u] * sc, v[8 * u + 1] * sc),
+                           pack2_bf16(v[8 * u + 2] * sc, v[8 * u + 3] * sc),
+                           pack2_bf16(v[8 * u + 4] * sc, v[8 * u + 5] * sc),
+                           pack2_bf16(v[8 * u + 6] * sc, v[8 * u + 7] * sc)));
+}
+// 64 packed bf16 pairs (128 columns) of row r into a K-major operand tile made of two
+// 64-column halves (16 KB apart), 128-byte swizzle
+__device__ __forceinline__ void store_operand_row128(uint32_t tile, int r, const uint32_t* pk) {
+#pragma unroll
+  for (int u = 0; u < 16; ++u)
+    st_shared16(tile + (u >> 3) * TILE + r * 128 + (((u & 7) ^ (r & 7)) << 4),
+                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
+}
+// 32 packed pairs (64 columns) of row r into one 64-column half
+__device__ __forceinline__ void store_operand_row64(uint32_t half_tile, int r, const uint32_t* pk) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    st_shared16(half_tile + r * 128 + ((u ^ (r & 7)) << 4),
+                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
+}
+
+struct Params {
+  int B, T, H, C, nqb, units;
+  float* lse;            // forward output, backward input [B, H, T]
+  const float* Dbuf;     // backward: rowsum(dO * O) [B, H, T]
   int* err;
 };
 
+// consecutive 8-byte mbarriers; after them the TMEM slot and the abort flag
+struct Bars {
+  uint32_t base;
+  __device__ uint32_t operator()(int i) const { return base + 8u * i; }
+};
+
+// =====================================================================================
+// forward
+constexpr int F_KV_STAGES = 3;
+constexpr int F_SM_Q = 0;                                  // [2 units][A, B]
+constexpr int F_SM_KV = F_SM_Q + 4 * TILE;                 // stage s: K at 2s, V at 2s+1
+constexpr int F_SM_P = F_SM_KV + 2 * F_KV_STAGES * TILE;   // [A, B] x two 64-key halves
+constexpr int F_SM_BAR = F_SM_P + 4 * TILE;
+constexpr int F_SMEM = F_SM_BAR + 256 + 1024;
+enum {
+  FB_QFULL = 0,              // [2]
+  FB_QEMPTY = 2,             // [2]
+  FB_KVFULL = 4,             // [3]
+  FB_KVEMPTY = 7,            // [3]
+  FB_SFULL = 10,             // [2] per tile
+  FB_SEMPTY = 12,            // [2]
+  FB_PFULL = 14,             // [2]
+  FB_ODONE = 16,             // [2]
+  FB_OFREE = 18,             // [2]
+  FB_FINAL = 20,
+  FB_COUNT = 21
+};
+
+struct FwdUnit {
+  int b, h, qa, nA, nB;      // tile A = query block qa, tile B = qa + 1 (nB = 0: absent)
+};
+__device__ __forceinline__ FwdUnit fwd_unit(const Params& p, int u) {
+  const int BH = p.B * p.H, npairs = (p.nqb + 1) / 2;
+  const int pair = npairs - 1 - u / BH, bh = u % BH;
+  FwdUnit w;
+  w.b = bh / p.H;
+  w.h = bh % p.H;
+  w.qa = 2 * pair;
+  w.nA = w.qa + 1;
+  w.nB = (w.qa + 1 < p.nqb) ? w.qa + 2 : 0;
+  return w;
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_out,
-           const FwdParams p) {
+           const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t bars = base + SM_BAR;
-  // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], s_empty[2], p_full, o_done, final
-  const uint32_t q_full = bars;
-  auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return bars + 8u * (1 + KV_STAGES + s); };
-  auto s_full = [&](int b) { return bars + 8u * (1 + 2 * KV_STAGES + b); };
-  auto s_empty = [&](int b) { return bars + 8u * (3 + 2 * KV_STAGES + b); };
-  const uint32_t p_full = bars + 8u * (5 + 2 * KV_STAGES);
-  const uint32_t o_done = bars + 8u * (6 + 2 * KV_STAGES);
-  const uint32_t final_bar = bars + 8u * (7 + 2 * KV_STAGES);
-  const uint32_t slot = bars + 8u * (8 + 2 * KV_STAGES);
-  volatile uint32_t* slot_ptr = (volatile uint32_t*)(base_ptr + SM_BAR + 8 * (8 + 2 * KV_STAGES));
-  volatile int* abort_flag = (volatile int*)(base_ptr + SM_BAR + 8 * (9 + 2 * KV_STAGES));
-
+  const Bars bar{base + F_SM_BAR};
+  volatile uint32_t* slot_ptr = (volatile uint32_t*)(base_ptr + F_SM_BAR + 8 * FB_COUNT);
+  volatile int* abort_flag = (volatile int*)(base_ptr + F_SM_BAR + 8 * FB_COUNT + 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qb = p.nqb - 1 - (int)blockIdx.x;     // heavy (late) query blocks first
-  const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
-  const int nkv = qb + 1;                          // key blocks 0..qb (BQ == BKV)
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < KV_STAGES; ++s) { mbar_init(kv_full(s), 1); mbar_init(kv_empty(s), 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(s_full(i), 1); mbar_init(s_empty(i), 4); }
-    mbar_init(p_full, 4);
-    mbar_init(o_done, 1);
-    mbar_init(final_bar, 1);
+    for (int i = 0; i < 2; ++i) { mbar_init(bar(FB_QFULL + i), 1); mbar_init(bar(FB_QEMPTY + i), 1); }
+    for (int s = 0; s < F_KV_STAGES; ++s) {
+      mbar_init(bar(FB_KVFULL + s), 1);
+      mbar_init(bar(FB_KVEMPTY + s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(FB_SFULL + x), 1);
+      mbar_init(bar(FB_SEMPTY + x), 4);
+      mbar_init(bar(FB_PFULL + x), 4);
+      mbar_init(bar(FB_ODONE + x), 1);
+      mbar_init(bar(FB_OFREE + x), 4);
+    }
+    mbar_init(bar(FB_FINAL), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    tmem_alloc(slot, TMEM_COLS);
+    tmem_alloc(bar(FB_COUNT), TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot_ptr;
+  // TMEM: S_A [0,128), S_B [128,256), O_A [256,320), O_B [320,384)
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
       bool ok = true;
-      mbar_expect_tx(q_full, TILE);
-      tma_load_3d(base + SM_Q, &tm_qkv, q_full, h * D, qb * BQ, b);
-      int j = 0;
-      for (; j < nkv && ok; ++j) {
-        const int s = j % KV_STAGES;
-        if (!mbar_wait(kv_empty(s), ((uint32_t)(j / KV_STAGES) & 1u) ^ 1u, abort_flag, p.err)) {
+      int uc = 0, kv = 0;      // units done, K/V tiles issued (ring position)
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
+        const FwdUnit w = fwd_unit(p, u);
+        const int qbuf = uc & 1;
+        if (uc >= 2 && !mbar_wait(bar(FB_QEMPTY + qbuf), par((uc >> 1) - 1), abort_flag, p.err)) {
           ok = false;
           break;
         }
-        const uint32_t kdst = base + SM_KV + 2 * s * TILE;
-        mbar_expect_tx(kv_full(s), 2 * TILE);
-        tma_load_3d(kdst, &tm_qkv, kv_full(s), p.C + h * D, j * BKV, b);
-        tma_load_3d(kdst + TILE, &tm_qkv, kv_full(s), 2 * p.C + h * D, j * BKV, b);
+        const uint32_t qdst = base + F_SM_Q + qbuf * 2 * TILE;
+        mbar_expect_tx(bar(FB_QFULL + qbuf), (w.nB ? 2 : 1) * TILE);
+        tma_load_3d(qdst, &tm_qkv, bar(FB_QFULL + qbuf), w.h * D, w.qa * BQ, w.b);
+        if (w.nB) tma_load_3d(qdst + TILE, &tm_qkv, bar(FB_QFULL + qbuf), w.h * D, (w.qa + 1) * BQ, w.b);
+        const int nkv = w.nB ? w.nB : w.nA;
+        for (int j = 0; j < nkv; ++j, ++kv) {
+          const int s = kv % F_KV_STAGES;
+          if (!mbar_wait(bar(FB_KVEMPTY + s), par(kv / F_KV_STAGES) ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t kdst = base + F_SM_KV + 2 * s * TILE;
+          mbar_expect_tx(bar(FB_KVFULL + s), 2 * TILE);
+          tma_load_3d(kdst, &tm_qkv, bar(FB_KVFULL + s), p.C + w.h * D, j * BKV, w.b);
+          tma_load_3d(kdst + TILE, &tm_qkv, bar(FB_KVFULL + s), 2 * p.C + w.h * D, j * BKV, w.b);
+        }
       }
-      // copies in flight land before the block leaves
-      mbar_wait(q_full, 0, abort_flag, nullptr, false);
-      for (int i = max(0, j - KV_STAGES); i < j; ++i)
-        mbar_wait(kv_full(i % KV_STAGES), (uint32_t)(i / KV_STAGES) & 1u, abort_flag, nullptr,
-                  false);
+      if (!ok) {   // let issued copies land before the block leaves
+        for (int i = 0; i < 2; ++i)
+          if (uc - i >= 0)
+            mbar_wait(bar(FB_QFULL + ((uc - i) & 1)), par((uc - i) >> 1), abort_flag, nullptr,
+                      false);
+        for (int k = max(0, kv - F_KV_STAGES); k < kv; ++k)
+          mbar_wait(bar(FB_KVFULL + k % F_KV_STAGES), par(k / F_KV_STAGES), abort_flag, nullptr,
+                    false);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
       constexpr uint32_t IDESC_S = make_idesc(BQ, BKV, false, false);
       constexpr uint32_t IDESC_O = make_idesc(BQ, D, false, true);
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % KV_STAGES, buf = j & 1;
-        if (!mbar_wait(kv_full(s), (uint32_t)(j / KV_STAGES) & 1u, abort_flag, p.err)) return false;
-        if (j >= 2 && !mbar_wait(s_empty(buf), (uint32_t)((j >> 1) - 1) & 1u, abort_flag, p.err))
+      bool ok = true;
+      int uc = 0, kv = 0;
+      int gs[2] = {0, 0};   // S issues per tile so far
+      int gp[2] = {0, 0};   // P V issues per tile so far
+      int uo[2] = {0, 0};   // units finished per tile (for O reuse)
+      auto issue_s = [&](int x, uint32_t qtile, int stage) -> bool {
+        if (gs[x] >= 1 && !mbar_wait(bar(FB_SEMPTY + x), par(gs[x] - 1), abort_flag, p.err))
           return false;
         tc_fence_after();
-        const uint32_t kb = base + SM_KV + 2 * s * TILE;
+        const uint32_t kb = base + F_SM_KV + 2 * stage * TILE;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          umma_bf16(tmem + buf * BKV, sdesc(base + SM_Q + k * 32, 16, 1024),
-                    sdesc(kb + k * 32, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
-        umma_commit(s_full(buf));
+          umma_bf16(tmem + x * BKV, sdesc(qtile + k * 32, 16, 1024), sdesc(kb + k * 32, 16, 1024),
+                    IDESC_S, k > 0 ? 1u : 0u);
+        umma_commit(bar(FB_SFULL + x));
+        ++gs[x];
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < nkv && ok; ++j) {
-        if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
-        if (!mbar_wait(p_full, (uint32_t)j & 1u, abort_flag, p.err)) { ok = false; break; }
+      auto issue_pv = [&](int x, int j, int stage) -> bool {
+        if (!mbar_wait(bar(FB_PFULL + x), par(gp[x]), abort_flag, p.err)) return false;
+        if (j == 0 && uo[x] >= 1 &&
+            !mbar_wait(bar(FB_OFREE + x), par(uo[x] - 1), abort_flag, p.err))
+          return false;
         tc_fence_after();
-        const uint32_t vb = base + SM_KV + (2 * (j % KV_STAGES) + 1) * TILE;
+        const uint32_t vb = base + F_SM_KV + (2 * stage + 1) * TILE;
+        const uint32_t pt = base + F_SM_P + x * 2 * TILE;
 #pragma unroll
         for (int k = 0; k < BKV / 16; ++k)
-          umma_bf16(tmem + COL_O, sdesc(base + SM_P + (k >> 2) * TILE + (k & 3) * 32, 16, 1024),
+          umma_bf16(tmem + 256 + x * D, sdesc(pt + (k >> 2) * TILE + (k & 3) * 32, 16, 1024),
                     sdesc(vb + k * 2048, 16384, 1024), IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
-        umma_commit(o_done);
-        umma_commit(kv_empty(j % KV_STAGES));
+        umma_commit(bar(FB_ODONE + x));
+        ++gp[x];
+        return true;
+      };
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
+        const FwdUnit w = fwd_unit(p, u);
+        const int qbuf = uc & 1;
+        const uint32_t qA = base + F_SM_Q + qbuf * 2 * TILE, qB = qA + TILE;
+        if (!mbar_wait(bar(FB_QFULL + qbuf), par(uc >> 1), abort_flag, p.err)) { ok = false; break; }
+        const int nkv = w.nB ? w.nB : w.nA;
+        // S for key block 0 of both tiles, then one block ahead of P V
+        if (!mbar_wait(bar(FB_KVFULL + kv % F_KV_STAGES), par(kv / F_KV_STAGES), abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        ok = issue_s(0, qA, kv % F_KV_STAGES) && (!w.nB || issue_s(1, qB, kv % F_KV_STAGES));
+        for (int j = 0; j < nkv && ok; ++j) {
+          const int st = (kv + j) % F_KV_STAGES;
+          if (j + 1 < nkv) {
+            const int nx = kv + j + 1;
+            if (!mbar_wait(bar(FB_KVFULL + nx % F_KV_STAGES), par(nx / F_KV_STAGES), abort_flag,
+                           p.err)) { ok = false; break; }
+            if (j + 1 < w.nA && !issue_s(0, qA, nx % F_KV_STAGES)) { ok = false; break; }
+            if (j + 1 < w.nB && !issue_s(1, qB, nx % F_KV_STAGES)) { ok = false; break; }
+          }
+          if (j < w.nA && !issue_pv(0, j, st)) { ok = false; break; }
+          if (j < w.nB && !issue_pv(1, j, st)) { ok = false; break; }
+          umma_commit(bar(FB_KVEMPTY + st));
+        }
+        if (!ok) break;
+        kv += nkv;
+        umma_commit(bar(FB_QEMPTY + qbuf));
+        ++uo[0];
+        if (w.nB) ++uo[1];
       }
-      umma_commit(final_bar);
-      mbar_wait(final_bar, 0, abort_flag, nullptr, false);
+      umma_commit(bar(FB_FINAL));
+      mbar_wait(bar(FB_FINAL), 0, abort_flag, nullptr, false);
     }
   } else {
-    // ---------------- softmax warps 2..5: TMEM lane quarter q = warp % 4, one row each
-    const int q = warp & 3;
-    const int r = q * 32 + lane;                      // row in the tile
-    const int query = qb * BQ + r;
+    // ---------------- softmax: tile x = 0 (warps 2..5) or 1 (warps 6..9)
+    const int x = (warp - 2) >> 2, q = warp & 3;
+    const int r = q * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t s_col = x * BKV, o_col = 256 + x * D;
+    const uint32_t p_tile = base + F_SM_P + x * 2 * TILE;
+    const uint32_t slice = p_tile + q * 4096;          // this warp's 32 rows of half 0
     const float sl2 = rsqrtf((float)D) * LOG2E;
-    float m = -INFINITY, l = 0.f;
+    int g = 0;                                          // S / P blocks of this tile so far
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int buf = j & 1;
-      ok = mbar_wait(s_full(buf), (uint32_t)(j >> 1) & 1u, abort_flag, p.err);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32_nowait(lane_base + buf * BKV + c * 32, sr[c]);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty(buf));
-      // scale into the log2 domain and mask the future on the diagonal block
-      float mx = -INFINITY;
-      const bool diag = (j == qb);
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float v = __uint_as_float(sr[c][e]) * sl2;
-          if (diag && (c * 32 + e) > r) v = -INFINITY;
-          sr[c][e] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
-        }
-      const float m_new = fmaxf(m, mx);
-      const float alpha = fast_exp2(m - m_new);
-      m = m_new;
-      float sum = 0.f;
-      uint32_t pk[4][16];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = fast_exp2(__uint_as_float(sr[c][2 * e]) - m_new);
-          const float p1 = fast_exp2(__uint_as_float(sr[c][2 * e + 1]) - m_new);
-          sum += p0 + p1;
-          pk[c][e] = pack2_bf16(p0, p1);
-        }
-      l = l * alpha + sum;
-      if (j > 0) {
-        // P_{j-1} V_{j-1} is complete: O is stable and the P tile is free
-        ok = mbar_wait(o_done, (uint32_t)(j - 1) & 1u, abort_flag, p.err);
+    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+      const FwdUnit w = fwd_unit(p, u);
+      const int n = x == 0 ? w.nA : w.nB;
+      if (n == 0) continue;
+      const int qblk = w.qa + x;
+      const int query = qblk * BQ + r;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < n; ++j, ++g) {
+        ok = mbar_wait(bar(FB_SFULL + x), par(g), abort_flag, p.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+        uint32_t sr[4][32];
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t o[32];
-            tmem_ld32_nowait(lane_base + COL_O + c * 32, o);
-            tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) tmem_ld32_nowait(lane_base + s_col + c * 32, sr[c]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(FB_SEMPTY + x));
+        if (j == qblk) {   // diagonal block: keys past the query are masked
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(lane_base + COL_O + c * 32, o);
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (c * 32 + e > r) sr[c][e] = __float_as_uint(-INFINITY);
+        }
+        float mx = __uint_as_float(sr[0][0]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+        mx *= sl2;
+        float alpha = 1.0f;
+        if (mx > m + RESCALE_LOG2) {
+          alpha = fast_exp2(m - mx);
+          m = mx;
+        }
+        float sum = 0.f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * e]), sl2, -m));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * e + 1]), sl2, -m));
+            sum += p0 + p1;
+            pk[c * 16 + e] = pack2_bf16(p0, p1);
           }
-          tmem_wait_st();
+        l = l * alpha + sum;
+        if (j > 0) {
+          // P V of the previous block is complete: O is stable and the P tile free
+          ok = mbar_wait(bar(FB_ODONE + x), par(g - 1), abort_flag, p.err);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              uint32_t o[32];
+              tmem_ld32_nowait(lane_base + o_col + c * 32, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st32(lane_base + o_col + c * 32, o);
+            }
+            tmem_wait_st();
+          }
+        } else {
+          // the slice may still be the source of the previous unit's output store
+          if (lane == 0) bulk_wait_read();
+          __syncwarp();
         }
+        store_operand_row128(p_tile, r, pk);
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(FB_PFULL + x));
       }
-      // P row r: keys 0..63 in the first half-tile, 64..127 in the second; 16-byte unit
-      // u of a 128-byte row sits at unit u ^ (r & 7) (128-byte swizzle)
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int unit = (c & 1) * 4 + u;
-          st_shared16(base + SM_P + (c >> 1) * TILE + r * 128 + ((unit ^ (r & 7)) << 4),
-                      make_uint4(pk[c][4 * u], pk[c][4 * u + 1], pk[c][4 * u + 2],
-                                 pk[c][4 * u + 3]));
-        }
-      fence_proxy_async();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-    }
-    if (ok) ok = mbar_wait(o_done, (uint32_t)(nkv - 1) & 1u, abort_flag, p.err);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
+      if (!ok) break;
+      ok = mbar_wait(bar(FB_ODONE + x), par(g - 1), abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       uint32_t o[2][32];
-      tmem_ld32_nowait(lane_base + COL_O, o[0]);
-      tmem_ld32_nowait(lane_base + COL_O + 32, o[1]);
+      tmem_ld32_nowait(lane_base + o_col, o[0]);
+      tmem_ld32_nowait(lane_base + o_col + 32, o[1]);
       tmem_wait_ld();
-      const float inv = 1.0f / l;
-      // O row into the Q tile's space (free now), 128-byte swizzle, then one TMA store
-      const uint32_t stg = base + SM_Q;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint32_t* src = &o[u >> 2][(u & 3) * 8];
-        st_shared16(stg + r * 128 + ((u ^ (r & 7)) << 4),
-                    make_uint4(pack2_bf16(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv),
-                               pack2_bf16(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv),
-                               pack2_bf16(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv),
-                               pack2_bf16(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv)));
-      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(FB_OFREE + x));
+      // O / l through this warp's slice (free: the last P V read it), one TMA store
+      stage_row64(slice, lane, reinterpret_cast<const float*>(o), 1.0f / l);
       fence_proxy_async();
-      if (query < p.T) p.lse[((size_t)b * p.H + h) * p.T + query] = (m + __log2f(l)) * LN2;
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&tm_out, slice, w.h * D, qblk * BQ + q * 32, w.b);
+        bulk_commit();
+      }
+      if (query < p.T) p.lse[((size_t)w.b * p.H + w.h) * p.T + query] = (m + __log2f(l)) * LN2;
     }
-    named_bar_sync(1, 128);
-    if (threadIdx.x == 64 && ok) {
-      tma_store_3d(&tm_out, base + SM_Q, h * D, qb * BQ, b);
-      bulk_commit();
-      bulk_wait_all();
-    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -277,75 +410,69 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
 }
 
 // =====================================================================================
-// Backward. With P recomputed from the forward's lse (P = exp2(s sl2 - lse log2 e)) and
-// D = rowsum(dO * O), every element is independent: dS = P (dP - D), dP = dO V^T, and
-//   dV = P^T dO,  dK = dS^T Q / sqrt(64),  dQ = dS K / sqrt(64).
-// Two kernels, each owning its output rows, so no partial sums cross blocks and the
-// result is deterministic. 320 threads: warp 0 TMA, warp 1 MMA, warps 2..9 elementwise
-// (warp w reads TMEM lane quarter w % 4; warps w and w + 4 take columns 0..63 and 64..127).
-constexpr int BWD_THREADS = 320;
-constexpr int BWD_STAGES = 2;
-
-struct BwdParams {
-  int T, H, C, nqb;
-  const float* lse;
-  const float* Dbuf;
-  int* err;
+// backward: dK, dV
+constexpr int K_QD_STAGES = 2;
+constexpr int K_SM_KV = 0;                                  // [2 units]: K, V
+constexpr int K_SM_QD = K_SM_KV + 4 * TILE;                 // stage s: Q at 2s, dO at 2s+1
+constexpr int K_SM_PT = K_SM_QD + 2 * K_QD_STAGES * TILE;   // P^T (two 64-query halves)
+constexpr int K_SM_DST = K_SM_PT + 2 * TILE;                // dS^T
+constexpr int K_SM_LD = K_SM_DST + 2 * TILE;                // stage s: lse[128], D[128]
+constexpr int K_SM_BAR = K_SM_LD + K_QD_STAGES * 1024;
+constexpr int K_SMEM = K_SM_BAR + 256 + 1024;
+enum {
+  KB_KVFULL = 0,    // [2]
+  KB_KVEMPTY = 2,   // [2]
+  KB_QDFULL = 4,    // [2]
+  KB_QDEMPTY = 6,   // [2]
+  KB_SFULL = 8,
+  KB_SEMPTY = 9,
+  KB_PFULL = 10,
+  KB_DONE = 11,
+  KB_ACCFREE = 12,
+  KB_FINAL = 13,
+  KB_COUNT = 14
 };
 
-// dK, dV for one block of 128 keys; loops over the query blocks at or after it.
-//   S^T = K Q_i^T, dP^T = V dO_i^T (TMEM, 128 + 128 columns), then
-//   dV += P^T dO_i, dK += dS^T Q_i (TMEM, 64 + 64 columns) with P^T and dS^T staged as
-//   bf16 in shared memory (the A operands).
-constexpr int DKV_SM_K = 0;
-constexpr int DKV_SM_V = DKV_SM_K + TILE;
-constexpr int DKV_SM_QD = DKV_SM_V + TILE;                       // stage s: Q at +2s, dO at +2s+1
-constexpr int DKV_SM_PT = DKV_SM_QD + 2 * BWD_STAGES * TILE;     // P^T, two 64-query halves
-constexpr int DKV_SM_DST = DKV_SM_PT + 2 * TILE;                 // dS^T
-constexpr int DKV_SM_LD = DKV_SM_DST + 2 * TILE;                 // stage s: [lse 128 | D 128]
-constexpr int DKV_SM_BAR = DKV_SM_LD + BWD_STAGES * 256 * 4;
-constexpr int DKV_SMEM = DKV_SM_BAR + 256 + 1024;
+__device__ __forceinline__ void dkv_unit(const Params& p, int u, int& b, int& h, int& kb, int& n) {
+  const int BH = p.B * p.H;
+  kb = u / BH;                       // ascending: key block 0 has the most query blocks
+  const int bh = u % BH;
+  b = bh / p.H;
+  h = bh % p.H;
+  n = p.nqb - kb;
+}
 
-__global__ void __launch_bounds__(BWD_THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 1)
 bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
-               const __grid_constant__ CUtensorMap tm_dqkv, const BwdParams p) {
+               const __grid_constant__ CUtensorMap tm_dqkv, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t bars = base + DKV_SM_BAR;
-  // barriers: kv_full, qd_full[S], qd_empty[S], s_full, s_empty, p_full, done, final
-  const uint32_t kv_full = bars;
-  auto qd_full = [&](int s) { return bars + 8u * (1 + s); };
-  auto qd_empty = [&](int s) { return bars + 8u * (1 + BWD_STAGES + s); };
-  const uint32_t s_full = bars + 8u * (1 + 2 * BWD_STAGES);
-  const uint32_t s_empty = bars + 8u * (2 + 2 * BWD_STAGES);
-  const uint32_t p_full = bars + 8u * (3 + 2 * BWD_STAGES);
-  const uint32_t done = bars + 8u * (4 + 2 * BWD_STAGES);
-  const uint32_t final_bar = bars + 8u * (5 + 2 * BWD_STAGES);
-  const uint32_t slot = bars + 8u * (6 + 2 * BWD_STAGES);
-  volatile uint32_t* slot_ptr = (volatile uint32_t*)(base_ptr + DKV_SM_BAR + 8 * (6 + 2 * BWD_STAGES));
-  volatile int* abort_flag = (volatile int*)(base_ptr + DKV_SM_BAR + 8 * (7 + 2 * BWD_STAGES));
-  float* sm_ld = reinterpret_cast<float*>(base_ptr + DKV_SM_LD);
-
+  const Bars bar{base + K_SM_BAR};
+  volatile uint32_t* slot_ptr = (volatile uint32_t*)(base_ptr + K_SM_BAR + 8 * KB_COUNT);
+  volatile int* abort_flag = (volatile int*)(base_ptr + K_SM_BAR + 8 * KB_COUNT + 8);
+  const float* sm_ld = reinterpret_cast<const float*>(base_ptr + K_SM_LD);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kb = blockIdx.x;                        // key block; query blocks kb..nqb-1
-  const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
-  const int n = p.nqb - kb;
 
   if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
-    for (int s = 0; s < BWD_STAGES; ++s) { mbar_init(qd_full(s), 1); mbar_init(qd_empty(s), 1); }
-    mbar_init(s_full, 1);
-    mbar_init(s_empty, 8);
-    mbar_init(p_full, 8);
-    mbar_init(done, 1);
-    mbar_init(final_bar, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(KB_KVFULL + i), 1);
+      mbar_init(bar(KB_KVEMPTY + i), 1);
+      mbar_init(bar(KB_QDFULL + i), 1);
+      mbar_init(bar(KB_QDEMPTY + i), 1);
+    }
+    mbar_init(bar(KB_SFULL), 1);
+    mbar_init(bar(KB_SEMPTY), 8);
+    mbar_init(bar(KB_PFULL), 8);
+    mbar_init(bar(KB_DONE), 1);
+    mbar_init(bar(KB_ACCFREE), 8);
+    mbar_init(bar(KB_FINAL), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    tmem_alloc(slot, TMEM_COLS);
+    tmem_alloc(bar(KB_COUNT), TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -357,171 +484,213 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
-      mbar_expect_tx(kv_full, 2 * TILE);
-      tma_load_3d(base + DKV_SM_K, &tm_qkv, kv_full, p.C + h * D, kb * BKV, b);
-      tma_load_3d(base + DKV_SM_V, &tm_qkv, kv_full, 2 * p.C + h * D, kb * BKV, b);
-      int i = 0;
-      for (; i < n && ok; ++i) {
-        const int s = i % BWD_STAGES;
-        if (!mbar_wait(qd_empty(s), ((uint32_t)(i / BWD_STAGES) & 1u) ^ 1u, abort_flag, p.err)) {
+      int uc = 0, it = 0;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
+        int b, h, kb, n;
+        dkv_unit(p, u, b, h, kb, n);
+        const int kbuf = uc & 1;
+        if (uc >= 2 && !mbar_wait(bar(KB_KVEMPTY + kbuf), par((uc >> 1) - 1), abort_flag, p.err)) {
           ok = false;
           break;
         }
-        const uint32_t dst = base + DKV_SM_QD + 2 * s * TILE;
-        const int qbi = kb + i;
-        // lse and D of the block's queries ride with the Q / dO tiles (T % 4 == 0, so the
-        // row start and the byte count are multiples of 16)
-        const uint32_t nb = (uint32_t)min(BQ, p.T - qbi * BQ) * 4u;
-        const size_t t0 = (size_t)bh * p.T + (size_t)qbi * BQ;
-        mbar_expect_tx(qd_full(s), 2 * TILE + 2 * nb);
-        tma_load_3d(dst, &tm_qkv, qd_full(s), h * D, qbi * BQ, b);
-        tma_load_3d(dst + TILE, &tm_do, qd_full(s), h * D, qbi * BQ, b);
-        const uint32_t ld_dst = base + DKV_SM_LD + s * 1024;
-        bulk_load(ld_dst, p.lse + t0, nb, qd_full(s));
-        bulk_load(ld_dst + 512, p.Dbuf + t0, nb, qd_full(s));
+        const uint32_t kdst = base + K_SM_KV + kbuf * 2 * TILE;
+        mbar_expect_tx(bar(KB_KVFULL + kbuf), 2 * TILE);
+        tma_load_3d(kdst, &tm_qkv, bar(KB_KVFULL + kbuf), p.C + h * D, kb * BKV, b);
+        tma_load_3d(kdst + TILE, &tm_qkv, bar(KB_KVFULL + kbuf), 2 * p.C + h * D, kb * BKV, b);
+        const size_t bh_t = ((size_t)b * p.H + h) * p.T;
+        for (int i = 0; i < n; ++i, ++it) {
+          const int s = it % K_QD_STAGES;
+          if (!mbar_wait(bar(KB_QDEMPTY + s), par(it / K_QD_STAGES) ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const int qbi = kb + i;
+          // lse and D of the block's queries ride with the Q / dO tiles (T % 4 == 0: the
+          // row start and the byte count are multiples of 16)
+          const uint32_t nb = (uint32_t)min(BQ, p.T - qbi * BQ) * 4u;
+          const uint32_t dst = base + K_SM_QD + 2 * s * TILE;
+          mbar_expect_tx(bar(KB_QDFULL + s), 2 * TILE + 2 * nb);
+          tma_load_3d(dst, &tm_qkv, bar(KB_QDFULL + s), h * D, qbi * BQ, b);
+          tma_load_3d(dst + TILE, &tm_do, bar(KB_QDFULL + s), h * D, qbi * BQ, b);
+          bulk_load(base + K_SM_LD + s * 1024, p.lse + bh_t + (size_t)qbi * BQ, nb, bar(KB_QDFULL + s));
+          bulk_load(base + K_SM_LD + s * 1024 + 512, p.Dbuf + bh_t + (size_t)qbi * BQ, nb,
+                    bar(KB_QDFULL + s));
+        }
       }
-      mbar_wait(kv_full, 0, abort_flag, nullptr, false);
-      for (int k = max(0, i - BWD_STAGES); k < i; ++k)
-        mbar_wait(qd_full(k % BWD_STAGES), (uint32_t)(k / BWD_STAGES) & 1u, abort_flag, nullptr,
-                  false);
+      if (!ok) {
+        for (int i = 0; i < 2; ++i)
+          if (uc - i >= 0)
+            mbar_wait(bar(KB_KVFULL + ((uc - i) & 1)), par((uc - i) >> 1), abort_flag, nullptr,
+                      false);
+        for (int k = max(0, it - K_QD_STAGES); k < it; ++k)
+          mbar_wait(bar(KB_QDFULL + k % K_QD_STAGES), par(k / K_QD_STAGES), abort_flag, nullptr,
+                    false);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t IDESC_S = make_idesc(BKV, BQ, false, false);
       constexpr uint32_t IDESC_G = make_idesc(BKV, D, false, true);
-      bool ok = mbar_wait(kv_full, 0, abort_flag, p.err);
-      auto issue_s = [&](int i) -> bool {
-        const int s = i % BWD_STAGES;
-        if (!mbar_wait(qd_full(s), (uint32_t)(i / BWD_STAGES) & 1u, abort_flag, p.err)) return false;
-        if (i >= 1 && !mbar_wait(s_empty, (uint32_t)(i - 1) & 1u, abort_flag, p.err)) return false;
-        tc_fence_after();
-        const uint32_t qa = base + DKV_SM_QD + 2 * s * TILE, da = qa + TILE;
+      bool ok = true;
+      int uc = 0, it = 0, gs = 0, gp = 0;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
+        int b, h, kb, n;
+        dkv_unit(p, u, b, h, kb, n);
+        const int kbuf = uc & 1;
+        const uint32_t kt = base + K_SM_KV + kbuf * 2 * TILE, vt = kt + TILE;
+        if (!mbar_wait(bar(KB_KVFULL + kbuf), par(uc >> 1), abort_flag, p.err)) { ok = false; break; }
+        for (int i = 0; i <= n && ok; ++i) {
+          // S^T, dP^T of block i (one block ahead of dV, dK of block i - 1)
+          if (i < n) {
+            const int s = (it + i) % K_QD_STAGES;
+            if (!mbar_wait(bar(KB_QDFULL + s), par((it + i) / K_QD_STAGES), abort_flag, p.err) ||
+                (gs >= 1 && !mbar_wait(bar(KB_SEMPTY), par(gs - 1), abort_flag, p.err))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t qa = base + K_SM_QD + 2 * s * TILE, da = qa + TILE;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          umma_bf16(tmem + COL_S, sdesc(base + DKV_SM_K + k * 32, 16, 1024),
-                    sdesc(qa + k * 32, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
-          umma_bf16(tmem + COL_DP, sdesc(base + DKV_SM_V + k * 32, 16, 1024),
-                    sdesc(da + k * 32, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
-        }
-        umma_commit(s_full);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      for (int i = 0; i < n && ok; ++i) {
-        if (i + 1 < n && !issue_s(i + 1)) { ok = false; break; }
-        if (!mbar_wait(p_full, (uint32_t)i & 1u, abort_flag, p.err)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t qa = base + DKV_SM_QD + 2 * (i % BWD_STAGES) * TILE, da = qa + TILE;
+            for (int k = 0; k < D / 16; ++k) {
+              umma_bf16(tmem + COL_S, sdesc(kt + k * 32, 16, 1024), sdesc(qa + k * 32, 16, 1024),
+                        IDESC_S, k > 0 ? 1u : 0u);
+              umma_bf16(tmem + COL_DP, sdesc(vt + k * 32, 16, 1024), sdesc(da + k * 32, 16, 1024),
+                        IDESC_S, k > 0 ? 1u : 0u);
+            }
+            umma_commit(bar(KB_SFULL));
+            ++gs;
+          }
+          if (i >= 1) {
+            const int ib = i - 1, s = (it + ib) % K_QD_STAGES;
+            if (!mbar_wait(bar(KB_PFULL), par(gp), abort_flag, p.err) ||
+                (ib == 0 && uc >= 1 && !mbar_wait(bar(KB_ACCFREE), par(uc - 1), abort_flag, p.err))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t qa = base + K_SM_QD + 2 * s * TILE, da = qa + TILE;
 #pragma unroll
-        for (int k = 0; k < BQ / 16; ++k) {
-          const uint32_t off = (k >> 2) * TILE + (k & 3) * 32;
-          umma_bf16(tmem + COL_DV, sdesc(base + DKV_SM_PT + off, 16, 1024),
-                    sdesc(da + k * 2048, 16384, 1024), IDESC_G, (i > 0 || k > 0) ? 1u : 0u);
-          umma_bf16(tmem + COL_DK, sdesc(base + DKV_SM_DST + off, 16, 1024),
-                    sdesc(qa + k * 2048, 16384, 1024), IDESC_G, (i > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < BQ / 16; ++k) {
+              const uint32_t off = (k >> 2) * TILE + (k & 3) * 32;
+              umma_bf16(tmem + COL_DV, sdesc(base + K_SM_PT + off, 16, 1024),
+                        sdesc(da + k * 2048, 16384, 1024), IDESC_G, (ib > 0 || k > 0) ? 1u : 0u);
+              umma_bf16(tmem + COL_DK, sdesc(base + K_SM_DST + off, 16, 1024),
+                        sdesc(qa + k * 2048, 16384, 1024), IDESC_G, (ib > 0 || k > 0) ? 1u : 0u);
+            }
+            umma_commit(bar(KB_DONE));
+            umma_commit(bar(KB_QDEMPTY + s));
+            ++gp;
+          }
         }
-        umma_commit(done);
-        umma_commit(qd_empty(i % BWD_STAGES));
+        if (!ok) break;
+        it += n;
+        umma_commit(bar(KB_KVEMPTY + kbuf));
       }
-      umma_commit(final_bar);
-      mbar_wait(final_bar, 0, abort_flag, nullptr, false);
+      umma_commit(bar(KB_FINAL));
+      mbar_wait(bar(KB_FINAL), 0, abort_flag, nullptr, false);
     }
   } else {
-    // ---------------- elementwise warps: key row r, query columns c0 .. c0 + 63
+    // ---------------- elementwise: key row r, query columns c0 .. c0 + 63
     const int q = warp & 3, half = (warp - 2) >> 2;
     const int r = q * 32 + lane, c0 = half * 64;
-    const int key = kb * BKV + r;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    // this warp's 32 rows of its P^T / dS^T half: the staging slices for dK / dV
+    const uint32_t slice_k = base + K_SM_PT + half * TILE + q * 4096;
+    const uint32_t slice_v = base + K_SM_DST + half * TILE + q * 4096;
     const float sl2 = rsqrtf((float)D) * LOG2E;
+    int it = 0, g = 0;
     bool ok = true;
-    for (int i = 0; i < n; ++i) {
-      // this stage's lse and D (copied with Q_i, dO_i); the stage is not refilled before
-      // the MMAs that follow p_full(i) have finished
-      const float* ld = sm_ld + (i % BWD_STAGES) * 256;
-      ok = mbar_wait(qd_full(i % BWD_STAGES), (uint32_t)(i / BWD_STAGES) & 1u, abort_flag, p.err) &&
-           mbar_wait(s_full, (uint32_t)i & 1u, abort_flag, p.err);
+    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+      int b, h, kb, n;
+      dkv_unit(p, u, b, h, kb, n);
+      const int key = kb * BKV + r;
+      for (int i = 0; i < n; ++i, ++it, ++g) {
+        const int s = it % K_QD_STAGES;
+        ok = mbar_wait(bar(KB_QDFULL + s), par(it / K_QD_STAGES), abort_flag, p.err) &&
+             mbar_wait(bar(KB_SFULL), par(g), abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sv[2][32], dv[2][32];
+        tmem_ld32_nowait(lane_base + COL_S + c0, sv[0]);
+        tmem_ld32_nowait(lane_base + COL_S + c0 + 32, sv[1]);
+        tmem_ld32_nowait(lane_base + COL_DP + c0, dv[0]);
+        tmem_ld32_nowait(lane_base + COL_DP + c0 + 32, dv[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(KB_SEMPTY));
+        const float4* lse4 = reinterpret_cast<const float4*>(sm_ld + s * 256 + c0);
+        const float4* D4 = reinterpret_cast<const float4*>(sm_ld + s * 256 + 128 + c0);
+        const int q0 = (kb + i) * BQ + c0;              // first query of these columns
+        const bool masked = (i == 0) || (q0 + 64 > p.T);
+        uint32_t pk[32], dk[32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 L = lse4[c * 8 + e4], Dd = D4[c * 8 + e4];
+            const float lv[4] = {L.x, L.y, L.z, L.w}, dd[4] = {Dd.x, Dd.y, Dd.z, Dd.w};
+            float pp[4], ds[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int e = e4 * 4 + t;
+              float pv = fast_exp2(fmaf(__uint_as_float(sv[c][e]), sl2, -lv[t] * LOG2E));
+              float dsv = pv * (__uint_as_float(dv[c][e]) - dd[t]);
+              if (masked) {
+                // past T the lse / D entries were never loaded: zero both results outright
+                const int query = q0 + c * 32 + e;
+                if (query < key || query >= p.T) { pv = 0.f; dsv = 0.f; }
+              }
+              pp[t] = pv;
+              ds[t] = dsv;
+            }
+            pk[c * 16 + e4 * 2] = pack2_bf16(pp[0], pp[1]);
+            pk[c * 16 + e4 * 2 + 1] = pack2_bf16(pp[2], pp[3]);
+            dk[c * 16 + e4 * 2] = pack2_bf16(ds[0], ds[1]);
+            dk[c * 16 + e4 * 2 + 1] = pack2_bf16(ds[2], ds[3]);
+          }
+        // the previous block's dV, dK MMAs have read P^T, dS^T (for the first block of a
+        // unit, that is the previous unit's last block, and the slices may still be the
+        // source of its output stores)
+        if (g >= 1) {
+          ok = mbar_wait(bar(KB_DONE), par(g - 1), abort_flag, p.err);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        }
+        if (i == 0) {
+          if (lane == 0) bulk_wait_read();
+          __syncwarp();
+        }
+        store_operand_row64(base + K_SM_PT + half * TILE, r, pk);
+        store_operand_row64(base + K_SM_DST + half * TILE, r, dk);
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(KB_PFULL));
+      }
+      if (!ok) break;
+      ok = mbar_wait(bar(KB_DONE), par(g - 1), abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sv[2][32], dv[2][32];
-      tmem_ld32_nowait(lane_base + COL_S + c0, sv[0]);
-      tmem_ld32_nowait(lane_base + COL_S + c0 + 32, sv[1]);
-      tmem_ld32_nowait(lane_base + COL_DP + c0, dv[0]);
-      tmem_ld32_nowait(lane_base + COL_DP + c0 + 32, dv[1]);
+      uint32_t kv2[2][32];
+      tmem_ld32_nowait(lane_base + COL_DK + half * 32, kv2[0]);
+      tmem_ld32_nowait(lane_base + COL_DV + half * 32, kv2[1]);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty);
-      const int qbase = (kb + i) * BQ + c0;
-      uint32_t pk[32], dk[32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pp[2], dd[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int qc = c * 32 + e + u;           // query column within this half
-            const int query = qbase + qc;
-            float pv = fast_exp2(fmaf(__uint_as_float(sv[c][e + u]), sl2, -ld[c0 + qc] * LOG2E));
-            if (query < key || query >= p.T) pv = 0.f;
-            pp[u] = pv;
-            dd[u] = pv * (__uint_as_float(dv[c][e + u]) - ld[128 + c0 + qc]);
-          }
-          pk[c * 16 + e / 2] = pack2_bf16(pp[0], pp[1]);
-          dk[c * 16 + e / 2] = pack2_bf16(dd[0], dd[1]);
-        }
-      if (i > 0) {
-        ok = mbar_wait(done, (uint32_t)(i - 1) & 1u, abort_flag, p.err);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      }
-      // rows of P^T and dS^T: this half's 64 queries are one 128-byte swizzled row
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint32_t off = half * TILE + r * 128 + ((u ^ (r & 7)) << 4);
-        st_shared16(base + DKV_SM_PT + off,
-                    make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
-        st_shared16(base + DKV_SM_DST + off,
-                    make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]));
-      }
+      if (lane == 0) mbar_arrive(bar(KB_ACCFREE));
+      stage_row32(slice_k, lane, reinterpret_cast<const float*>(kv2[0]), rsqrtf((float)D));
+      stage_row32(slice_v, lane, reinterpret_cast<const float*>(kv2[1]), 1.0f);
       fence_proxy_async();
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-    }
-    if (ok) ok = mbar_wait(done, (uint32_t)(n - 1) & 1u, abort_flag, p.err);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
-      tc_fence_after();
-      // this warp's 32 of the 64 head columns of dK and dV, into the (now free) Q/dO stage 0
-      uint32_t kv[2][32];
-      tmem_ld32_nowait(lane_base + COL_DK + half * 32, kv[0]);
-      tmem_ld32_nowait(lane_base + COL_DV + half * 32, kv[1]);
-      tmem_wait_ld();
-      const float scale = rsqrtf((float)D);
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const float sc = t == 0 ? scale : 1.0f;
-        const uint32_t stg = base + DKV_SM_QD + t * TILE;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t* v = &kv[t][u * 8];
-          const int unit = half * 4 + u;
-          st_shared16(stg + r * 128 + ((unit ^ (r & 7)) << 4),
-                      make_uint4(pack2_bf16(__uint_as_float(v[0]) * sc, __uint_as_float(v[1]) * sc),
-                                 pack2_bf16(__uint_as_float(v[2]) * sc, __uint_as_float(v[3]) * sc),
-                                 pack2_bf16(__uint_as_float(v[4]) * sc, __uint_as_float(v[5]) * sc),
-                                 pack2_bf16(__uint_as_float(v[6]) * sc, __uint_as_float(v[7]) * sc)));
-        }
+      if (lane == 0) {
+        const int row = kb * BKV + q * 32;
+        tma_store_3d(&tm_dqkv, slice_k, p.C + h * D + half * 32, row, b);
+        tma_store_3d(&tm_dqkv, slice_v, 2 * p.C + h * D + half * 32, row, b);
+        bulk_commit();
       }
-      fence_proxy_async();
     }
-    named_bar_sync(1, 256);
-    if (threadIdx.x == 64 && ok) {
-      tma_store_3d(&tm_dqkv, base + DKV_SM_QD, p.C + h * D, kb * BKV, b);
-      tma_store_3d(&tm_dqkv, base + DKV_SM_QD + TILE, 2 * p.C + h * D, kb * BKV, b);
-      bulk_commit();
-      bulk_wait_all();
-    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -532,54 +701,66 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
   }
 }
 
-// dQ for one block of 128 queries; loops over the key blocks up to the diagonal.
-//   S = Q K_j^T, dP = dO V_j^T (TMEM), dS = P (dP - D) as bf16 in shared memory, then
-//   dQ += dS K_j (TMEM, 64 columns).
-constexpr int DQ_SM_Q = 0;
-constexpr int DQ_SM_DO = DQ_SM_Q + TILE;
-constexpr int DQ_SM_KV = DQ_SM_DO + TILE;                        // stage s: K at +2s, V at +2s+1
-constexpr int DQ_SM_DS = DQ_SM_KV + 2 * BWD_STAGES * TILE;
-constexpr int DQ_SM_BAR = DQ_SM_DS + 2 * TILE;
-constexpr int DQ_SMEM = DQ_SM_BAR + 256 + 1024;
+// =====================================================================================
+// backward: dQ
+constexpr int Q_KV_STAGES = 3;
+constexpr int Q_SM_QD = 0;                                   // [2 units]: Q, dO
+constexpr int Q_SM_KV = Q_SM_QD + 4 * TILE;                  // stage s: K at 2s, V at 2s+1
+constexpr int Q_SM_DS = Q_SM_KV + 2 * Q_KV_STAGES * TILE;    // dS (two 64-key halves)
+constexpr int Q_SM_BAR = Q_SM_DS + 2 * TILE;
+constexpr int Q_SMEM = Q_SM_BAR + 256 + 1024;
+enum {
+  QB_QFULL = 0,     // [2]
+  QB_QEMPTY = 2,    // [2]
+  QB_KVFULL = 4,    // [3]
+  QB_KVEMPTY = 7,   // [3]
+  QB_SFULL = 10,
+  QB_SEMPTY = 11,
+  QB_PFULL = 12,
+  QB_DONE = 13,
+  QB_ACCFREE = 14,
+  QB_FINAL = 15,
+  QB_COUNT = 16
+};
 
-__global__ void __launch_bounds__(BWD_THREADS, 1)
+__device__ __forceinline__ void dq_unit(const Params& p, int u, int& b, int& h, int& qb, int& n) {
+  const int BH = p.B * p.H;
+  qb = p.nqb - 1 - u / BH;           // descending: the last query block has the most keys
+  const int bh = u % BH;
+  b = bh / p.H;
+  h = bh % p.H;
+  n = qb + 1;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
-              const __grid_constant__ CUtensorMap tm_dqkv, const BwdParams p) {
+              const __grid_constant__ CUtensorMap tm_dqkv, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t bars = base + DQ_SM_BAR;
-  const uint32_t q_full = bars;
-  auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return bars + 8u * (1 + BWD_STAGES + s); };
-  const uint32_t s_full = bars + 8u * (1 + 2 * BWD_STAGES);
-  const uint32_t s_empty = bars + 8u * (2 + 2 * BWD_STAGES);
-  const uint32_t p_full = bars + 8u * (3 + 2 * BWD_STAGES);
-  const uint32_t done = bars + 8u * (4 + 2 * BWD_STAGES);
-  const uint32_t final_bar = bars + 8u * (5 + 2 * BWD_STAGES);
-  const uint32_t slot = bars + 8u * (6 + 2 * BWD_STAGES);
-  volatile uint32_t* slot_ptr = (volatile uint32_t*)(base_ptr + DQ_SM_BAR + 8 * (6 + 2 * BWD_STAGES));
-  volatile int* abort_flag = (volatile int*)(base_ptr + DQ_SM_BAR + 8 * (7 + 2 * BWD_STAGES));
-
+  const Bars bar{base + Q_SM_BAR};
+  volatile uint32_t* slot_ptr = (volatile uint32_t*)(base_ptr + Q_SM_BAR + 8 * QB_COUNT);
+  volatile int* abort_flag = (volatile int*)(base_ptr + Q_SM_BAR + 8 * QB_COUNT + 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qb = p.nqb - 1 - (int)blockIdx.x;
-  const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
-  const int n = qb + 1;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < BWD_STAGES; ++s) { mbar_init(kv_full(s), 1); mbar_init(kv_empty(s), 1); }
-    mbar_init(s_full, 1);
-    mbar_init(s_empty, 8);
-    mbar_init(p_full, 8);
-    mbar_init(done, 1);
-    mbar_init(final_bar, 1);
+    for (int i = 0; i < 2; ++i) { mbar_init(bar(QB_QFULL + i), 1); mbar_init(bar(QB_QEMPTY + i), 1); }
+    for (int s = 0; s < Q_KV_STAGES; ++s) {
+      mbar_init(bar(QB_KVFULL + s), 1);
+      mbar_init(bar(QB_KVEMPTY + s), 1);
+    }
+    mbar_init(bar(QB_SFULL), 1);
+    mbar_init(bar(QB_SEMPTY), 8);
+    mbar_init(bar(QB_PFULL), 8);
+    mbar_init(bar(QB_DONE), 1);
+    mbar_init(bar(QB_ACCFREE), 8);
+    mbar_init(bar(QB_FINAL), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    tmem_alloc(slot, TMEM_COLS);
+    tmem_alloc(bar(QB_COUNT), TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -591,145 +772,180 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
-      mbar_expect_tx(q_full, 2 * TILE);
-      tma_load_3d(base + DQ_SM_Q, &tm_qkv, q_full, h * D, qb * BQ, b);
-      tma_load_3d(base + DQ_SM_DO, &tm_do, q_full, h * D, qb * BQ, b);
-      int j = 0;
-      for (; j < n && ok; ++j) {
-        const int s = j % BWD_STAGES;
-        if (!mbar_wait(kv_empty(s), ((uint32_t)(j / BWD_STAGES) & 1u) ^ 1u, abort_flag, p.err)) {
+      int uc = 0, kv = 0;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
+        int b, h, qb, n;
+        dq_unit(p, u, b, h, qb, n);
+        const int qbuf = uc & 1;
+        if (uc >= 2 && !mbar_wait(bar(QB_QEMPTY + qbuf), par((uc >> 1) - 1), abort_flag, p.err)) {
           ok = false;
           break;
         }
-        const uint32_t dst = base + DQ_SM_KV + 2 * s * TILE;
-        mbar_expect_tx(kv_full(s), 2 * TILE);
-        tma_load_3d(dst, &tm_qkv, kv_full(s), p.C + h * D, j * BKV, b);
-        tma_load_3d(dst + TILE, &tm_qkv, kv_full(s), 2 * p.C + h * D, j * BKV, b);
+        const uint32_t qdst = base + Q_SM_QD + qbuf * 2 * TILE;
+        mbar_expect_tx(bar(QB_QFULL + qbuf), 2 * TILE);
+        tma_load_3d(qdst, &tm_qkv, bar(QB_QFULL + qbuf), h * D, qb * BQ, b);
+        tma_load_3d(qdst + TILE, &tm_do, bar(QB_QFULL + qbuf), h * D, qb * BQ, b);
+        for (int j = 0; j < n; ++j, ++kv) {
+          const int s = kv % Q_KV_STAGES;
+          if (!mbar_wait(bar(QB_KVEMPTY + s), par(kv / Q_KV_STAGES) ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = base + Q_SM_KV + 2 * s * TILE;
+          mbar_expect_tx(bar(QB_KVFULL + s), 2 * TILE);
+          tma_load_3d(dst, &tm_qkv, bar(QB_KVFULL + s), p.C + h * D, j * BKV, b);
+          tma_load_3d(dst + TILE, &tm_qkv, bar(QB_KVFULL + s), 2 * p.C + h * D, j * BKV, b);
+        }
       }
-      mbar_wait(q_full, 0, abort_flag, nullptr, false);
-      for (int k = max(0, j - BWD_STAGES); k < j; ++k)
-        mbar_wait(kv_full(k % BWD_STAGES), (uint32_t)(k / BWD_STAGES) & 1u, abort_flag, nullptr,
-                  false);
+      if (!ok) {
+        for (int i = 0; i < 2; ++i)
+          if (uc - i >= 0)
+            mbar_wait(bar(QB_QFULL + ((uc - i) & 1)), par((uc - i) >> 1), abort_flag, nullptr,
+                      false);
+        for (int k = max(0, kv - Q_KV_STAGES); k < kv; ++k)
+          mbar_wait(bar(QB_KVFULL + k % Q_KV_STAGES), par(k / Q_KV_STAGES), abort_flag, nullptr,
+                    false);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t IDESC_S = make_idesc(BQ, BKV, false, false);
       constexpr uint32_t IDESC_G = make_idesc(BQ, D, false, true);
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % BWD_STAGES;
-        if (!mbar_wait(kv_full(s), (uint32_t)(j / BWD_STAGES) & 1u, abort_flag, p.err)) return false;
-        if (j >= 1 && !mbar_wait(s_empty, (uint32_t)(j - 1) & 1u, abort_flag, p.err)) return false;
-        tc_fence_after();
-        const uint32_t ka = base + DQ_SM_KV + 2 * s * TILE, va = ka + TILE;
+      bool ok = true;
+      int uc = 0, kv = 0, gs = 0, gp = 0;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
+        int b, h, qb, n;
+        dq_unit(p, u, b, h, qb, n);
+        const int qbuf = uc & 1;
+        const uint32_t qt = base + Q_SM_QD + qbuf * 2 * TILE, dt = qt + TILE;
+        if (!mbar_wait(bar(QB_QFULL + qbuf), par(uc >> 1), abort_flag, p.err)) { ok = false; break; }
+        for (int j = 0; j <= n && ok; ++j) {
+          if (j < n) {
+            const int s = (kv + j) % Q_KV_STAGES;
+            if (!mbar_wait(bar(QB_KVFULL + s), par((kv + j) / Q_KV_STAGES), abort_flag, p.err) ||
+                (gs >= 1 && !mbar_wait(bar(QB_SEMPTY), par(gs - 1), abort_flag, p.err))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t ka = base + Q_SM_KV + 2 * s * TILE, va = ka + TILE;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          umma_bf16(tmem + COL_S, sdesc(base + DQ_SM_Q + k * 32, 16, 1024),
-                    sdesc(ka + k * 32, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
-          umma_bf16(tmem + COL_DP, sdesc(base + DQ_SM_DO + k * 32, 16, 1024),
-                    sdesc(va + k * 32, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+            for (int k = 0; k < D / 16; ++k) {
+              umma_bf16(tmem + COL_S, sdesc(qt + k * 32, 16, 1024), sdesc(ka + k * 32, 16, 1024),
+                        IDESC_S, k > 0 ? 1u : 0u);
+              umma_bf16(tmem + COL_DP, sdesc(dt + k * 32, 16, 1024), sdesc(va + k * 32, 16, 1024),
+                        IDESC_S, k > 0 ? 1u : 0u);
+            }
+            umma_commit(bar(QB_SFULL));
+            ++gs;
+          }
+          if (j >= 1) {
+            const int jb = j - 1, s = (kv + jb) % Q_KV_STAGES;
+            if (!mbar_wait(bar(QB_PFULL), par(gp), abort_flag, p.err) ||
+                (jb == 0 && uc >= 1 && !mbar_wait(bar(QB_ACCFREE), par(uc - 1), abort_flag, p.err))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t ka = base + Q_SM_KV + 2 * s * TILE;
+#pragma unroll
+            for (int k = 0; k < BKV / 16; ++k)
+              umma_bf16(tmem + COL_DQ, sdesc(base + Q_SM_DS + (k >> 2) * TILE + (k & 3) * 32, 16, 1024),
+                        sdesc(ka + k * 2048, 16384, 1024), IDESC_G, (jb > 0 || k > 0) ? 1u : 0u);
+            umma_commit(bar(QB_DONE));
+            umma_commit(bar(QB_KVEMPTY + s));
+            ++gp;
+          }
         }
-        umma_commit(s_full);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < n && ok; ++j) {
-        if (j + 1 < n && !issue_s(j + 1)) { ok = false; break; }
-        if (!mbar_wait(p_full, (uint32_t)j & 1u, abort_flag, p.err)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t ka = base + DQ_SM_KV + 2 * (j % BWD_STAGES) * TILE;
-#pragma unroll
-        for (int k = 0; k < BKV / 16; ++k)
-          umma_bf16(tmem + COL_DQ, sdesc(base + DQ_SM_DS + (k >> 2) * TILE + (k & 3) * 32, 16, 1024),
-                    sdesc(ka + k * 2048, 16384, 1024), IDESC_G, (j > 0 || k > 0) ? 1u : 0u);
-        umma_commit(done);
-        umma_commit(kv_empty(j % BWD_STAGES));
+        if (!ok) break;
+        kv += n;
+        umma_commit(bar(QB_QEMPTY + qbuf));
       }
-      umma_commit(final_bar);
-      mbar_wait(final_bar, 0, abort_flag, nullptr, false);
+      umma_commit(bar(QB_FINAL));
+      mbar_wait(bar(QB_FINAL), 0, abort_flag, nullptr, false);
     }
   } else {
-    // ---------------- elementwise warps: query row r, key columns c0 .. c0 + 63
+    // ---------------- elementwise: query row r, key columns c0 .. c0 + 63
     const int q = warp & 3, half = (warp - 2) >> 2;
     const int r = q * 32 + lane, c0 = half * 64;
-    const int query = qb * BQ + r;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t slice = base + Q_SM_DS + half * TILE + q * 4096;
     const float sl2 = rsqrtf((float)D) * LOG2E;
-    float lse2 = 0.f, Dr = 0.f;
-    if (query < p.T) {
-      lse2 = __ldg(p.lse + (size_t)bh * p.T + query) * LOG2E;
-      Dr = __ldg(p.Dbuf + (size_t)bh * p.T + query);
-    }
+    int g = 0;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      ok = mbar_wait(s_full, (uint32_t)j & 1u, abort_flag, p.err);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t sv[2][32], dv[2][32];
-      tmem_ld32_nowait(lane_base + COL_S + c0, sv[0]);
-      tmem_ld32_nowait(lane_base + COL_S + c0 + 32, sv[1]);
-      tmem_ld32_nowait(lane_base + COL_DP + c0, dv[0]);
-      tmem_ld32_nowait(lane_base + COL_DP + c0 + 32, dv[1]);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty);
-      const int kbase = j * BKV + c0;
-      uint32_t dk[32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float dd[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int kc = kbase + c * 32 + e + u;
-            float pv = fast_exp2(fmaf(__uint_as_float(sv[c][e + u]), sl2, -lse2));
-            if (kc > query) pv = 0.f;
-            dd[u] = pv * (__uint_as_float(dv[c][e + u]) - Dr);
-          }
-          dk[c * 16 + e / 2] = pack2_bf16(dd[0], dd[1]);
-        }
-      if (j > 0) {
-        ok = mbar_wait(done, (uint32_t)(j - 1) & 1u, abort_flag, p.err);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+      int b, h, qb, n;
+      dq_unit(p, u, b, h, qb, n);
+      const int query = qb * BQ + r;
+      float nlse2 = 0.f, Dr = 0.f;
+      if (query < p.T) {
+        const size_t t = ((size_t)b * p.H + h) * p.T + query;
+        nlse2 = -__ldg(p.lse + t) * LOG2E;
+        Dr = __ldg(p.Dbuf + t);
       }
+      for (int j = 0; j < n; ++j, ++g) {
+        ok = mbar_wait(bar(QB_SFULL), par(g), abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sv[2][32], dv[2][32];
+        tmem_ld32_nowait(lane_base + COL_S + c0, sv[0]);
+        tmem_ld32_nowait(lane_base + COL_S + c0 + 32, sv[1]);
+        tmem_ld32_nowait(lane_base + COL_DP + c0, dv[0]);
+        tmem_ld32_nowait(lane_base + COL_DP + c0 + 32, dv[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(QB_SEMPTY));
+        const int k0 = j * BKV + c0;
+        const bool masked = (j == qb);
+        uint32_t dk[32];
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        st_shared16(base + DQ_SM_DS + half * TILE + r * 128 + ((u ^ (r & 7)) << 4),
-                    make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]));
-      fence_proxy_async();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-    }
-    if (ok) ok = mbar_wait(done, (uint32_t)(n - 1) & 1u, abort_flag, p.err);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float ds[2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              float pv = fast_exp2(fmaf(__uint_as_float(sv[c][e + t]), sl2, nlse2));
+              if (masked && k0 + c * 32 + e + t > query) pv = 0.f;
+              ds[t] = pv * (__uint_as_float(dv[c][e + t]) - Dr);
+            }
+            dk[c * 16 + e / 2] = pack2_bf16(ds[0], ds[1]);
+          }
+        if (g >= 1) {
+          ok = mbar_wait(bar(QB_DONE), par(g - 1), abort_flag, p.err);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        }
+        if (j == 0) {
+          if (lane == 0) bulk_wait_read();
+          __syncwarp();
+        }
+        store_operand_row64(base + Q_SM_DS + half * TILE, r, dk);
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(QB_PFULL));
+      }
+      if (!ok) break;
+      ok = mbar_wait(bar(QB_DONE), par(g - 1), abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       uint32_t v[32];
       tmem_ld32_nowait(lane_base + COL_DQ + half * 32, v);
       tmem_wait_ld();
-      const float sc = rsqrtf((float)D);
-      const uint32_t stg = base + DQ_SM_Q;     // Q is no longer read
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint32_t* w = &v[u * 8];
-        const int unit = half * 4 + u;
-        st_shared16(stg + r * 128 + ((unit ^ (r & 7)) << 4),
-                    make_uint4(pack2_bf16(__uint_as_float(w[0]) * sc, __uint_as_float(w[1]) * sc),
-                               pack2_bf16(__uint_as_float(w[2]) * sc, __uint_as_float(w[3]) * sc),
-                               pack2_bf16(__uint_as_float(w[4]) * sc, __uint_as_float(w[5]) * sc),
-                               pack2_bf16(__uint_as_float(w[6]) * sc, __uint_as_float(w[7]) * sc)));
-      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(QB_ACCFREE));
+      stage_row32(slice, lane, reinterpret_cast<const float*>(v), rsqrtf((float)D));
       fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&tm_dqkv, slice, h * D + half * 32, qb * BQ + q * 32, b);
+        bulk_commit();
+      }
     }
-    named_bar_sync(1, 256);
-    if (threadIdx.x == 64 && ok) {
-      tma_store_3d(&tm_dqkv, base + DQ_SM_Q, h * D, qb * BQ, b);
-      bulk_commit();
-      bulk_wait_all();
-    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -741,17 +957,29 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
 }
 
 // ------------------------------------------------------------------ host side
-// [B][T][width] bf16 as a 3-D map {width, T, B}, box {64, 128, 1}, 128-byte swizzle
-static bool map_btw(CUtensorMap* m, const void* ptr, int B, int T, int width) {
+// [B][T][width] bf16 as a 3-D map {width, T, B}, box {box_w, box_rows, 1}
+static bool map_btw(CUtensorMap* m, const void* ptr, int B, int T, int width, int box_w,
+                    int box_rows, CUtensorMapSwizzle swz) {
   auto fn = tensor_map_encoder();
   if (!fn || ((uintptr_t)ptr & 15u) || (width * 2) % 16) return false;
   cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)T, (cuuint64_t)B};
   cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)T * width * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {(cuuint32_t)box_w, (cuuint32_t)box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
 }
 
 }  // namespace fatc
@@ -759,22 +987,24 @@ static bool map_btw(CUtensorMap* m, const void* ptr, int B, int T, int width) {
 cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, int T, int C,
                                  int H, int* err, cudaStream_t s) {
   using namespace fatc;
-  if (C / H != D || C % H || C % 64) return cudaErrorInvalidValue;
+  if (C / H != D || C % H || C % 64 || B <= 0 || T <= 0) return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM);
+                                         F_SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   CUtensorMap mq, mo;
-  if (!map_btw(&mq, qkv, B, T, 3 * C) || !map_btw(&mo, out, B, T, C)) return cudaErrorInvalidValue;
-  FwdParams p;
-  p.T = T; p.H = H; p.C = C; p.nqb = ceil_div(T, BQ);
-  p.lse = lse;
-  p.err = err;
-  dim3 grid(p.nqb, B * H);
-  fwd_kernel<<<grid, THREADS, SMEM, s>>>(mq, mo, p);
+  if (!map_btw(&mq, qkv, B, T, 3 * C, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !map_btw(&mo, out, B, T, C, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  Params p;
+  p.B = B; p.T = T; p.H = H; p.C = C; p.nqb = ceil_div(T, BQ);
+  p.units = B * H * ((p.nqb + 1) / 2);
+  p.lse = lse; p.Dbuf = nullptr; p.err = err;
+  const int grid = std::min(p.units, num_sms());
+  fwd_kernel<<<grid, THREADS, F_SMEM, s>>>(mq, mo, p);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -783,31 +1013,33 @@ cudaError_t attention_backward_tc(void* dqkv, const float* Dbuf, const void* dou
                                   const void* qkv, const float* lse, int B, int T, int C, int H,
                                   int* err, cudaStream_t s) {
   using namespace fatc;
-  if (C / H != D || C % H || C % 64 || T % 4 || ((uintptr_t)lse & 15u) || ((uintptr_t)Dbuf & 15u))
+  if (C / H != D || C % H || C % 64 || B <= 0 || T <= 0 || T % 4 || ((uintptr_t)lse & 15u) ||
+      ((uintptr_t)Dbuf & 15u))
     return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(bwd_dkv_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, DKV_SMEM);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, K_SMEM);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               DQ_SMEM);
+      e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Q_SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   CUtensorMap mq, md, mg;
-  if (!map_btw(&mq, qkv, B, T, 3 * C) || !map_btw(&md, dout, B, T, C) ||
-      !map_btw(&mg, dqkv, B, T, 3 * C))
+  if (!map_btw(&mq, qkv, B, T, 3 * C, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !map_btw(&md, dout, B, T, C, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !map_btw(&mg, dqkv, B, T, 3 * C, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  BwdParams p;
-  p.T = T; p.H = H; p.C = C; p.nqb = ceil_div(T, BQ);
-  p.lse = lse; p.Dbuf = Dbuf; p.err = err;
-  dim3 grid(p.nqb, B * H);
-  bwd_dkv_kernel<<<grid, BWD_THREADS, DKV_SMEM, s>>>(mq, md, mg, p);
+  Params p;
+  p.B = B; p.T = T; p.H = H; p.C = C; p.nqb = ceil_div(T, BQ);
+  p.units = B * H * p.nqb;
+  p.lse = const_cast<float*>(lse); p.Dbuf = Dbuf; p.err = err;
+  const int grid = std::min(p.units, num_sms());
+  bwd_dkv_kernel<<<grid, THREADS, K_SMEM, s>>>(mq, md, mg, p);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  bwd_dq_kernel<<<grid, BWD_THREADS, DQ_SMEM, s>>>(mq, md, mg, p);
+  bwd_dq_kernel<<<grid, THREADS, Q_SMEM, s>>>(mq, md, mg, p);
   count_launches(1);
   return cudaGetLastError();
 }
