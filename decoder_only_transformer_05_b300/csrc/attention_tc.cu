@@ -29,6 +29,7 @@
 //   (warps w and w + 4 take 64 each): no row reduction is needed once lse and D are known.
 // Rows past T (ragged T) read zeros through the 3-D tensor maps and are never stored.
 #include <cstring>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -71,14 +72,6 @@ __device__ __forceinline__ void stage_row32(uint32_t slice, int r, const float* 
                            pack2_bf16(v[8 * u + 2] * sc, v[8 * u + 3] * sc),
                            pack2_bf16(v[8 * u + 4] * sc, v[8 * u + 5] * sc),
                            pack2_bf16(v[8 * u + 6] * sc, v[8 * u + 7] * sc)));
-}
-// 64 packed bf16 pairs (128 columns) of row r into a K-major operand tile made of two
-// 64-column halves (16 KB apart), 128-byte swizzle
-__device__ __forceinline__ void store_operand_row128(uint32_t tile, int r, const uint32_t* pk) {
-#pragma unroll
-  for (int u = 0; u < 16; ++u)
-    st_shared16(tile + (u >> 3) * TILE + r * 128 + (((u & 7) ^ (r & 7)) << 4),
-                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
 }
 // 32 packed pairs (64 columns) of row r into one 64-column half
 __device__ __forceinline__ void store_operand_row64(uint32_t half_tile, int r, const uint32_t* pk) {
@@ -138,6 +131,7 @@ __device__ __forceinline__ FwdUnit fwd_unit(const Params& p, int u) {
   return w;
 }
 
+// 10 warps: one SM sub-partition holds three of them, so at most 168 registers
 __global__ void __launch_bounds__(THREADS, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_out,
            const Params p) {
@@ -311,43 +305,30 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
         ok = mbar_wait(bar(FB_SFULL + x), par(g), abort_flag, p.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sr[4][32];
+        // pass 1: the block's row maximum, one 32-column chunk of the score row at a time
+        // (causal mask on the diagonal block only)
+        const bool diag = (j == qblk);
+        float mx = -INFINITY;
+        auto row_max = [&](auto diag_tag) {
+          constexpr bool DIAG = decltype(diag_tag)::value;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32_nowait(lane_base + s_col + c * 32, sr[c]);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(FB_SEMPTY + x));
-        if (j == qblk) {   // diagonal block: keys past the query are masked
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c) {
+            uint32_t sr[32];
+            tmem_ld32_nowait(lane_base + s_col + c * 32, sr);
+            tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-              if (c * 32 + e > r) sr[c][e] = __float_as_uint(-INFINITY);
-        }
-        float mx = __uint_as_float(sr[0][0]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+              if (!DIAG || c * 32 + e <= r) mx = fmaxf(mx, __uint_as_float(sr[e]));
+          }
+        };
+        if (diag) row_max(std::true_type{});
+        else row_max(std::false_type{});
         mx *= sl2;
         float alpha = 1.0f;
         if (mx > m + RESCALE_LOG2) {
           alpha = fast_exp2(m - mx);
           m = mx;
         }
-        float sum = 0.f;
-        uint32_t pk[64];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * e]), sl2, -m));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * e + 1]), sl2, -m));
-            sum += p0 + p1;
-            pk[c * 16 + e] = pack2_bf16(p0, p1);
-          }
-        l = l * alpha + sum;
         if (j > 0) {
           // P V of the previous block is complete: O is stable and the P tile free
           ok = mbar_wait(bar(FB_ODONE + x), par(g - 1), abort_flag, p.err);
@@ -370,7 +351,43 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
           if (lane == 0) bulk_wait_read();
           __syncwarp();
         }
-        store_operand_row128(p_tile, r, pk);
+        // pass 2: P = exp2(s sl2 - m) as bf16, straight into the operand tile, and the sum
+        float sum = 0.f;
+        auto exp_pass = [&](auto diag_tag) {
+          constexpr bool DIAG = decltype(diag_tag)::value;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t sr[32], pk[16];
+            tmem_ld32_nowait(lane_base + s_col + c * 32, sr);
+            tmem_wait_ld();
+            if (c == 3) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar(FB_SEMPTY + x));
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * e]), sl2, -m));
+              float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * e + 1]), sl2, -m));
+              if (DIAG) {
+                if (c * 32 + 2 * e > r) p0 = 0.f;
+                if (c * 32 + 2 * e + 1 > r) p1 = 0.f;
+              }
+              sum += p0 + p1;
+              pk[e] = pack2_bf16(p0, p1);
+            }
+            // 32 keys = four 16-byte units of the row in key half c / 2
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int unit = (c & 1) * 4 + u;
+              st_shared16(p_tile + (c >> 1) * TILE + r * 128 + ((unit ^ (r & 7)) << 4),
+                          make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
+            }
+          }
+        };
+        if (diag) exp_pass(std::true_type{});
+        else exp_pass(std::false_type{});
+        l = l * alpha + sum;
         fence_proxy_async();
         tc_fence_before();
         __syncwarp();
@@ -442,6 +459,7 @@ __device__ __forceinline__ void dkv_unit(const Params& p, int u, int& b, int& h,
   n = p.nqb - kb;
 }
 
+// 10 warps: one SM sub-partition holds three of them, so at most 168 registers
 __global__ void __launch_bounds__(THREADS, 1)
 bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_dqkv, const Params p) {
@@ -610,22 +628,23 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
              mbar_wait(bar(KB_SFULL), par(g), abort_flag, p.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sv[2][32], dv[2][32];
-        tmem_ld32_nowait(lane_base + COL_S + c0, sv[0]);
-        tmem_ld32_nowait(lane_base + COL_S + c0 + 32, sv[1]);
-        tmem_ld32_nowait(lane_base + COL_DP + c0, dv[0]);
-        tmem_ld32_nowait(lane_base + COL_DP + c0 + 32, dv[1]);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(KB_SEMPTY));
         const float4* lse4 = reinterpret_cast<const float4*>(sm_ld + s * 256 + c0);
         const float4* D4 = reinterpret_cast<const float4*>(sm_ld + s * 256 + 128 + c0);
         const int q0 = (kb + i) * BQ + c0;              // first query of these columns
-        const bool masked = (i == 0) || (q0 + 64 > p.T);
-        uint32_t pk[32], dk[32];
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
+        // P^T and dS^T of 64 query columns, 32 at a time (S^T, dP^T released after the
+        // second load), each chunk stored as soon as it is computed; the mask (causal on
+        // the diagonal block, past T on the last) only in the blocks that need it
+        auto chunk = [&](int c, auto masked_tag) -> bool {
+          constexpr bool MASKED = decltype(masked_tag)::value;
+          uint32_t sv[32], dv[32], pk[16], dk[16];
+          tmem_ld32_nowait(lane_base + COL_S + c0 + c * 32, sv);
+          tmem_ld32_nowait(lane_base + COL_DP + c0 + c * 32, dv);
+          tmem_wait_ld();
+          if (c == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(KB_SEMPTY));
+          }
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
             const float4 L = lse4[c * 8 + e4], Dd = D4[c * 8 + e4];
@@ -634,9 +653,9 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
               const int e = e4 * 4 + t;
-              float pv = fast_exp2(fmaf(__uint_as_float(sv[c][e]), sl2, -lv[t] * LOG2E));
-              float dsv = pv * (__uint_as_float(dv[c][e]) - dd[t]);
-              if (masked) {
+              float pv = fast_exp2(fmaf(__uint_as_float(sv[e]), sl2, -lv[t] * LOG2E));
+              float dsv = pv * (__uint_as_float(dv[e]) - dd[t]);
+              if (MASKED) {
                 // past T the lse / D entries were never loaded: zero both results outright
                 const int query = q0 + c * 32 + e;
                 if (query < key || query >= p.T) { pv = 0.f; dsv = 0.f; }
@@ -644,24 +663,38 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
               pp[t] = pv;
               ds[t] = dsv;
             }
-            pk[c * 16 + e4 * 2] = pack2_bf16(pp[0], pp[1]);
-            pk[c * 16 + e4 * 2 + 1] = pack2_bf16(pp[2], pp[3]);
-            dk[c * 16 + e4 * 2] = pack2_bf16(ds[0], ds[1]);
-            dk[c * 16 + e4 * 2 + 1] = pack2_bf16(ds[2], ds[3]);
+            pk[e4 * 2] = pack2_bf16(pp[0], pp[1]);
+            pk[e4 * 2 + 1] = pack2_bf16(pp[2], pp[3]);
+            dk[e4 * 2] = pack2_bf16(ds[0], ds[1]);
+            dk[e4 * 2 + 1] = pack2_bf16(ds[2], ds[3]);
           }
-        // the previous block's dV, dK MMAs have read P^T, dS^T (for the first block of a
-        // unit, that is the previous unit's last block, and the slices may still be the
-        // source of its output stores)
-        if (g >= 1) {
-          ok = mbar_wait(bar(KB_DONE), par(g - 1), abort_flag, p.err);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          if (c == 0) {
+            // the previous block's dV, dK MMAs have read P^T, dS^T (for the first block of a
+            // unit, the previous unit's last block; the slices may also still be the source
+            // of that unit's output stores)
+            if (g >= 1) {
+              const bool w_ok = mbar_wait(bar(KB_DONE), par(g - 1), abort_flag, p.err);
+              if (!__all_sync(0xffffffffu, w_ok)) return false;
+            }
+            if (i == 0) {
+              if (lane == 0) bulk_wait_read();
+              __syncwarp();
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t off = half * TILE + r * 128 + (((c * 4 + u) ^ (r & 7)) << 4);
+            st_shared16(base + K_SM_PT + off, make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
+            st_shared16(base + K_SM_DST + off, make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]));
+          }
+          return true;
+        };
+        if (i == 0 || q0 + 64 > p.T) {
+          ok = chunk(0, std::true_type{}) && chunk(1, std::true_type{});
+        } else {
+          ok = chunk(0, std::false_type{}) && chunk(1, std::false_type{});
         }
-        if (i == 0) {
-          if (lane == 0) bulk_wait_read();
-          __syncwarp();
-        }
-        store_operand_row64(base + K_SM_PT + half * TILE, r, pk);
-        store_operand_row64(base + K_SM_DST + half * TILE, r, dk);
+        if (!ok) break;
         fence_proxy_async();
         tc_fence_before();
         __syncwarp();
@@ -732,6 +765,7 @@ __device__ __forceinline__ void dq_unit(const Params& p, int u, int& b, int& h, 
   n = qb + 1;
 }
 
+// 10 warps: one SM sub-partition holds three of them, so at most 168 registers
 __global__ void __launch_bounds__(THREADS, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_dqkv, const Params p) {
@@ -887,31 +921,36 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
         ok = mbar_wait(bar(QB_SFULL), par(g), abort_flag, p.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sv[2][32], dv[2][32];
-        tmem_ld32_nowait(lane_base + COL_S + c0, sv[0]);
-        tmem_ld32_nowait(lane_base + COL_S + c0 + 32, sv[1]);
-        tmem_ld32_nowait(lane_base + COL_DP + c0, dv[0]);
-        tmem_ld32_nowait(lane_base + COL_DP + c0 + 32, dv[1]);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(QB_SEMPTY));
         const int k0 = j * BKV + c0;
-        const bool masked = (j == qb);
         uint32_t dk[32];
+        auto compute = [&](auto masked_tag) {   // causal mask on the diagonal block only
+          constexpr bool MASKED = decltype(masked_tag)::value;
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float ds[2];
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              float pv = fast_exp2(fmaf(__uint_as_float(sv[c][e + t]), sl2, nlse2));
-              if (masked && k0 + c * 32 + e + t > query) pv = 0.f;
-              ds[t] = pv * (__uint_as_float(dv[c][e + t]) - Dr);
+          for (int c = 0; c < 2; ++c) {
+            uint32_t sv[32], dv[32];
+            tmem_ld32_nowait(lane_base + COL_S + c0 + c * 32, sv);
+            tmem_ld32_nowait(lane_base + COL_DP + c0 + c * 32, dv);
+            tmem_wait_ld();
+            if (c == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar(QB_SEMPTY));
             }
-            dk[c * 16 + e / 2] = pack2_bf16(ds[0], ds[1]);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float ds[2];
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                float pv = fast_exp2(fmaf(__uint_as_float(sv[e + t]), sl2, nlse2));
+                if (MASKED && k0 + c * 32 + e + t > query) pv = 0.f;
+                ds[t] = pv * (__uint_as_float(dv[e + t]) - Dr);
+              }
+              dk[c * 16 + e / 2] = pack2_bf16(ds[0], ds[1]);
+            }
           }
+        };
+        if (j == qb) compute(std::true_type{});
+        else compute(std::false_type{});
         if (g >= 1) {
           ok = mbar_wait(bar(QB_DONE), par(g - 1), abort_flag, p.err);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
