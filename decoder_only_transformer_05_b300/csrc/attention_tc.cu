@@ -6,13 +6,13 @@
 //
 // All three kernels are persistent: one 320-thread block per SM walks a fixed list of
 // work units (heaviest first, unit c, c + G, c + 2G, ... for block c of G), and the TMA
-// ring runs on across units so the next unit's tiles load while this one computes.
+// rings run on across units so the next unit's tiles load while this one computes.
 //   warp 0      TMA producer (Q / K / V / dO tiles of 128 rows x 64, 128-byte swizzle)
 //   warp 1      MMA issuer (one thread; tcgen05.mma, fp32 accumulators in tensor memory)
 //   warps 2..9  elementwise: warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31
-// Each elementwise warp stores its own 32 output rows with a TMA store from its own slice
-// of shared memory, so no barrier spans more than one warp. Every mbarrier wait is
-// bounded; on timeout the block records DEV_ERR_TIMEOUT and stops.
+// Each elementwise warp stores its own 32 output rows (a TMA store from its own slice of
+// shared memory), so no barrier spans more than one warp. Every mbarrier wait is bounded;
+// on timeout the block records DEV_ERR_TIMEOUT and stops.
 //
 // Forward (unit = one (batch, head) and two consecutive 128-query tiles A, B):
 //   S_X = Q_X K_j^T (TMEM, 128 columns per tile), softmax by the tile's four warps (thread =
@@ -20,7 +20,8 @@
 //   into shared memory, O_X += P_X V_j (TMEM, 64 columns per tile). m only moves when the
 //   block's maximum exceeds it by more than 8 (P then stays below 2^8), and O is rescaled in
 //   tensor memory when it does. The two tiles' softmax warps run side by side and share
-//   every K, V tile.
+//   every K, V tile; K and V have rings of their own, P is double-buffered per tile, and the
+//   MMA thread issues whichever S or P V group is ready (non-blocking probes).
 // Backward (D = rowsum(dO * O) from a separate kernel; P = exp2(s sl2 - lse log2 e)):
 //   dK/dV unit = (batch, head, 128 keys): S^T = K Q_i^T, dP^T = V dO_i^T, then
 //   dV += P^T dO_i, dK += dS^T Q_i with dS = P (dP - D); dQ unit = (batch, head, 128
@@ -96,24 +97,29 @@ struct Bars {
 
 // =====================================================================================
 // forward
-constexpr int F_KV_STAGES = 3;
-constexpr int F_SM_Q = 0;                                  // [2 units][A, B]
-constexpr int F_SM_KV = F_SM_Q + 4 * TILE;                 // stage s: K at 2s, V at 2s+1
-constexpr int F_SM_P = F_SM_KV + 2 * F_KV_STAGES * TILE;   // [A, B] x two 64-key halves
-constexpr int F_SM_BAR = F_SM_P + 4 * TILE;
+//   shared memory: Q_A, Q_B | K ring (2) | V ring (2) | P_A[2], P_B[2] (double-buffered,
+//   so block j's P is written while P V of block j - 1 still reads the other buffer)
+constexpr int F_RING = 2;
+constexpr int F_SM_Q = 0;                                  // A, B
+constexpr int F_SM_K = F_SM_Q + 2 * TILE;                  // K ring
+constexpr int F_SM_V = F_SM_K + F_RING * TILE;             // V ring
+constexpr int F_SM_P = F_SM_V + F_RING * TILE;             // [tile][buf]: two 64-key halves
+constexpr int F_SM_BAR = F_SM_P + 4 * 2 * TILE;
 constexpr int F_SMEM = F_SM_BAR + 256 + 1024;
 enum {
-  FB_QFULL = 0,              // [2]
-  FB_QEMPTY = 2,             // [2]
-  FB_KVFULL = 4,             // [3]
-  FB_KVEMPTY = 7,            // [3]
-  FB_SFULL = 10,             // [2] per tile
-  FB_SEMPTY = 12,            // [2]
-  FB_PFULL = 14,             // [2]
-  FB_ODONE = 16,             // [2]
-  FB_OFREE = 18,             // [2]
-  FB_FINAL = 20,
-  FB_COUNT = 21
+  FB_QFULL = 0,
+  FB_QEMPTY = 1,
+  FB_KFULL = 2,              // [2]
+  FB_KEMPTY = 4,             // [2]
+  FB_VFULL = 6,              // [2]
+  FB_VEMPTY = 8,             // [2]
+  FB_SFULL = 10,             // [tile]
+  FB_SEMPTY = 12,            // [tile]
+  FB_PFULL = 14,             // [tile][buf]
+  FB_ODONE = 18,             // [tile][buf]
+  FB_OFREE = 22,             // [tile]
+  FB_FINAL = 24,
+  FB_COUNT = 25
 };
 
 struct FwdUnit {
@@ -131,7 +137,6 @@ __device__ __forceinline__ FwdUnit fwd_unit(const Params& p, int u) {
   return w;
 }
 
-// 10 warps: one SM sub-partition holds three of them, so at most 168 registers
 __global__ void __launch_bounds__(THREADS, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_out,
            const Params p) {
@@ -145,17 +150,22 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) { mbar_init(bar(FB_QFULL + i), 1); mbar_init(bar(FB_QEMPTY + i), 1); }
-    for (int s = 0; s < F_KV_STAGES; ++s) {
-      mbar_init(bar(FB_KVFULL + s), 1);
-      mbar_init(bar(FB_KVEMPTY + s), 1);
+    mbar_init(bar(FB_QFULL), 1);
+    mbar_init(bar(FB_QEMPTY), 1);
+    for (int s = 0; s < F_RING; ++s) {
+      mbar_init(bar(FB_KFULL + s), 1);
+      mbar_init(bar(FB_KEMPTY + s), 1);
+      mbar_init(bar(FB_VFULL + s), 1);
+      mbar_init(bar(FB_VEMPTY + s), 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(FB_SFULL + x), 1);
       mbar_init(bar(FB_SEMPTY + x), 4);
-      mbar_init(bar(FB_PFULL + x), 4);
-      mbar_init(bar(FB_ODONE + x), 1);
       mbar_init(bar(FB_OFREE + x), 4);
+      for (int bf = 0; bf < 2; ++bf) {
+        mbar_init(bar(FB_PFULL + 2 * x + bf), 4);
+        mbar_init(bar(FB_ODONE + 2 * x + bf), 1);
+      }
     }
     mbar_init(bar(FB_FINAL), 1);
     *abort_flag = 0;
@@ -173,110 +183,132 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer: Q per unit, then K_j, V_j on their own rings
       bool ok = true;
-      int uc = 0, kv = 0;      // units done, K/V tiles issued (ring position)
+      int uc = 0, kv = 0;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
         const FwdUnit w = fwd_unit(p, u);
-        const int qbuf = uc & 1;
-        if (uc >= 2 && !mbar_wait(bar(FB_QEMPTY + qbuf), par((uc >> 1) - 1), abort_flag, p.err)) {
+        if (uc >= 1 && !mbar_wait(bar(FB_QEMPTY), par(uc - 1), abort_flag, p.err)) {
           ok = false;
           break;
         }
-        const uint32_t qdst = base + F_SM_Q + qbuf * 2 * TILE;
-        mbar_expect_tx(bar(FB_QFULL + qbuf), (w.nB ? 2 : 1) * TILE);
-        tma_load_3d(qdst, &tm_qkv, bar(FB_QFULL + qbuf), w.h * D, w.qa * BQ, w.b);
-        if (w.nB) tma_load_3d(qdst + TILE, &tm_qkv, bar(FB_QFULL + qbuf), w.h * D, (w.qa + 1) * BQ, w.b);
+        mbar_expect_tx(bar(FB_QFULL), (w.nB ? 2 : 1) * TILE);
+        tma_load_3d(base + F_SM_Q, &tm_qkv, bar(FB_QFULL), w.h * D, w.qa * BQ, w.b);
+        if (w.nB)
+          tma_load_3d(base + F_SM_Q + TILE, &tm_qkv, bar(FB_QFULL), w.h * D, (w.qa + 1) * BQ, w.b);
         const int nkv = w.nB ? w.nB : w.nA;
-        for (int j = 0; j < nkv; ++j, ++kv) {
-          const int s = kv % F_KV_STAGES;
-          if (!mbar_wait(bar(FB_KVEMPTY + s), par(kv / F_KV_STAGES) ^ 1u, abort_flag, p.err)) {
-            ok = false;
-            break;
-          }
-          const uint32_t kdst = base + F_SM_KV + 2 * s * TILE;
-          mbar_expect_tx(bar(FB_KVFULL + s), 2 * TILE);
-          tma_load_3d(kdst, &tm_qkv, bar(FB_KVFULL + s), p.C + w.h * D, j * BKV, w.b);
-          tma_load_3d(kdst + TILE, &tm_qkv, bar(FB_KVFULL + s), 2 * p.C + w.h * D, j * BKV, w.b);
+        for (int j = 0; j < nkv && ok; ++j, ++kv) {
+          const int s = kv % F_RING;
+          const uint32_t ph = par(kv / F_RING) ^ 1u;
+          if (!mbar_wait(bar(FB_KEMPTY + s), ph, abort_flag, p.err)) { ok = false; break; }
+          mbar_expect_tx(bar(FB_KFULL + s), TILE);
+          tma_load_3d(base + F_SM_K + s * TILE, &tm_qkv, bar(FB_KFULL + s), p.C + w.h * D, j * BKV, w.b);
+          if (!mbar_wait(bar(FB_VEMPTY + s), ph, abort_flag, p.err)) { ok = false; ++kv; break; }
+          mbar_expect_tx(bar(FB_VFULL + s), TILE);
+          tma_load_3d(base + F_SM_V + s * TILE, &tm_qkv, bar(FB_VFULL + s), 2 * p.C + w.h * D, j * BKV, w.b);
         }
       }
       if (!ok) {   // let issued copies land before the block leaves
-        for (int i = 0; i < 2; ++i)
-          if (uc - i >= 0)
-            mbar_wait(bar(FB_QFULL + ((uc - i) & 1)), par((uc - i) >> 1), abort_flag, nullptr,
-                      false);
-        for (int k = max(0, kv - F_KV_STAGES); k < kv; ++k)
-          mbar_wait(bar(FB_KVFULL + k % F_KV_STAGES), par(k / F_KV_STAGES), abort_flag, nullptr,
-                    false);
+        if (uc >= 0) mbar_wait(bar(FB_QFULL), par(uc), abort_flag, nullptr, false);
+        for (int k = max(0, kv - F_RING); k < kv; ++k) {
+          mbar_wait(bar(FB_KFULL + k % F_RING), par(k / F_RING), abort_flag, nullptr, false);
+          mbar_wait(bar(FB_VFULL + k % F_RING), par(k / F_RING), abort_flag, nullptr, false);
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---------------- MMA issuer
+      // ---------------- MMA issuer: issues whichever of S_A, S_B, P_A V, P_B V is ready
+      // (non-blocking probes), so one tile's slower step never holds up the other's.
       constexpr uint32_t IDESC_S = make_idesc(BQ, BKV, false, false);
       constexpr uint32_t IDESC_O = make_idesc(BQ, D, false, true);
+      // descriptors of the tiles' first 16 columns; a k step adds (bytes >> 4)
+      const uint64_t dq0 = sdesc(base + F_SM_Q, 16, 1024);
+      const uint64_t dk0 = sdesc(base + F_SM_K, 16, 1024);
+      const uint64_t dv0 = sdesc(base + F_SM_V, 16384, 1024);
+      const uint64_t dp0 = sdesc(base + F_SM_P, 16, 1024);
+      constexpr uint64_t TILE16 = TILE >> 4;
       bool ok = true;
-      int uc = 0, kv = 0;
-      int gs[2] = {0, 0};   // S issues per tile so far
-      int gp[2] = {0, 0};   // P V issues per tile so far
-      int uo[2] = {0, 0};   // units finished per tile (for O reuse)
-      auto issue_s = [&](int x, uint32_t qtile, int stage) -> bool {
-        if (gs[x] >= 1 && !mbar_wait(bar(FB_SEMPTY + x), par(gs[x] - 1), abort_flag, p.err))
-          return false;
-        tc_fence_after();
-        const uint32_t kb = base + F_SM_KV + 2 * stage * TILE;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          umma_bf16(tmem + x * BKV, sdesc(qtile + k * 32, 16, 1024), sdesc(kb + k * 32, 16, 1024),
-                    IDESC_S, k > 0 ? 1u : 0u);
-        umma_commit(bar(FB_SFULL + x));
-        ++gs[x];
-        return true;
-      };
-      auto issue_pv = [&](int x, int j, int stage) -> bool {
-        if (!mbar_wait(bar(FB_PFULL + x), par(gp[x]), abort_flag, p.err)) return false;
-        if (j == 0 && uo[x] >= 1 &&
-            !mbar_wait(bar(FB_OFREE + x), par(uo[x] - 1), abort_flag, p.err))
-          return false;
-        tc_fence_after();
-        const uint32_t vb = base + F_SM_KV + (2 * stage + 1) * TILE;
-        const uint32_t pt = base + F_SM_P + x * 2 * TILE;
-#pragma unroll
-        for (int k = 0; k < BKV / 16; ++k)
-          umma_bf16(tmem + 256 + x * D, sdesc(pt + (k >> 2) * TILE + (k & 3) * 32, 16, 1024),
-                    sdesc(vb + k * 2048, 16384, 1024), IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
-        umma_commit(bar(FB_ODONE + x));
-        ++gp[x];
-        return true;
-      };
+      int uc = 0, kvb = 0;               // units done; K/V blocks consumed so far
+      int gs[2] = {0, 0}, gp[2] = {0, 0}, uo[2] = {0, 0};
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
         const FwdUnit w = fwd_unit(p, u);
-        const int qbuf = uc & 1;
-        const uint32_t qA = base + F_SM_Q + qbuf * 2 * TILE, qB = qA + TILE;
-        if (!mbar_wait(bar(FB_QFULL + qbuf), par(uc >> 1), abort_flag, p.err)) { ok = false; break; }
+        const int n[2] = {w.nA, w.nB};
         const int nkv = w.nB ? w.nB : w.nA;
-        // S for key block 0 of both tiles, then one block ahead of P V
-        if (!mbar_wait(bar(FB_KVFULL + kv % F_KV_STAGES), par(kv / F_KV_STAGES), abort_flag, p.err)) {
-          ok = false;
-          break;
-        }
-        ok = issue_s(0, qA, kv % F_KV_STAGES) && (!w.nB || issue_s(1, qB, kv % F_KV_STAGES));
-        for (int j = 0; j < nkv && ok; ++j) {
-          const int st = (kv + j) % F_KV_STAGES;
-          if (j + 1 < nkv) {
-            const int nx = kv + j + 1;
-            if (!mbar_wait(bar(FB_KVFULL + nx % F_KV_STAGES), par(nx / F_KV_STAGES), abort_flag,
-                           p.err)) { ok = false; break; }
-            if (j + 1 < w.nA && !issue_s(0, qA, nx % F_KV_STAGES)) { ok = false; break; }
-            if (j + 1 < w.nB && !issue_s(1, qB, nx % F_KV_STAGES)) { ok = false; break; }
+        int si[2] = {0, 0}, pi[2] = {0, 0};   // next S / P V block per tile in this unit
+        int kr = 0, vr = 0;                    // K / V blocks released so far
+        bool qready = false, qfreed = false;
+        unsigned long long t_last = globaltimer();
+        while (ok) {
+          bool progress = false;
+          if (!qready) qready = mbar_test(bar(FB_QFULL), par(uc));
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            // S_x(j) = Q_x K_j^T: needs Q, K_j, and the tile's S buffer drained
+            const int j = si[x];
+            if (qready && j < n[x]) {
+              const int kb = kvb + j;
+              if (mbar_test(bar(FB_KFULL + kb % F_RING), par(kb / F_RING)) &&
+                  (gs[x] == 0 || mbar_test(bar(FB_SEMPTY + x), par(gs[x] - 1)))) {
+                tc_fence_after();
+                const uint64_t a = dq0 + x * TILE16, bk = dk0 + (kb % F_RING) * TILE16;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)
+                  umma_bf16(tmem + x * BKV, a + 2 * k, bk + 2 * k, IDESC_S, k > 0 ? 1u : 0u);
+                umma_commit(bar(FB_SFULL + x));
+                ++si[x];
+                ++gs[x];
+                progress = true;
+              }
+            }
+            // P_x(j) V_j: needs P_x(j) written, V_j, and (first block) O_x read out
+            const int jp = pi[x];
+            if (jp < si[x]) {
+              const int vb = kvb + jp, bf = gp[x] & 1;
+              if (mbar_test(bar(FB_VFULL + vb % F_RING), par(vb / F_RING)) &&
+                  mbar_test(bar(FB_PFULL + 2 * x + bf), par(gp[x] >> 1)) &&
+                  (jp > 0 || uo[x] == 0 || mbar_test(bar(FB_OFREE + x), par(uo[x] - 1)))) {
+                tc_fence_after();
+                const uint64_t a = dp0 + (2 * x + bf) * 2 * TILE16;
+                const uint64_t bv = dv0 + (vb % F_RING) * TILE16;
+#pragma unroll
+                for (int k = 0; k < BKV / 16; ++k)
+                  umma_bf16(tmem + 256 + x * D, a + (k >> 2) * TILE16 + 2 * (k & 3), bv + 128 * k,
+                            IDESC_O, (jp > 0 || k > 0) ? 1u : 0u);
+                umma_commit(bar(FB_ODONE + 2 * x + bf));
+                ++pi[x];
+                ++gp[x];
+                progress = true;
+              }
+            }
           }
-          if (j < w.nA && !issue_pv(0, j, st)) { ok = false; break; }
-          if (j < w.nB && !issue_pv(1, j, st)) { ok = false; break; }
-          umma_commit(bar(FB_KVEMPTY + st));
+          // release K_j once every tile that needs it has issued S(j); V_j likewise for P V
+          while (kr < nkv && (si[0] > kr || kr >= n[0]) && (si[1] > kr || kr >= n[1])) {
+            umma_commit(bar(FB_KEMPTY + (kvb + kr) % F_RING));
+            ++kr;
+          }
+          while (vr < nkv && (pi[0] > vr || vr >= n[0]) && (pi[1] > vr || vr >= n[1])) {
+            umma_commit(bar(FB_VEMPTY + (kvb + vr) % F_RING));
+            ++vr;
+          }
+          if (!qfreed && si[0] == n[0] && si[1] == n[1]) {
+            // the unit's last S MMAs are issued: Q can be refilled once they complete
+            umma_commit(bar(FB_QEMPTY));
+            qfreed = true;
+          }
+          if (pi[0] == n[0] && pi[1] == n[1]) break;
+          if (progress) {
+            t_last = globaltimer();
+          } else if (*abort_flag) {
+            ok = false;
+          } else if (globaltimer() - t_last > TIMEOUT_NS) {
+            *abort_flag = 1;
+            if (p.err) atomicOr(p.err, DEV_ERR_TIMEOUT);
+            ok = false;
+          }
         }
         if (!ok) break;
-        kv += nkv;
-        umma_commit(bar(FB_QEMPTY + qbuf));
+        kvb += nkv;
         ++uo[0];
         if (w.nB) ++uo[1];
       }
@@ -289,10 +321,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
     const int r = q * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     const uint32_t s_col = x * BKV, o_col = 256 + x * D;
-    const uint32_t p_tile = base + F_SM_P + x * 2 * TILE;
-    const uint32_t slice = p_tile + q * 4096;          // this warp's 32 rows of half 0
     const float sl2 = rsqrtf((float)D) * LOG2E;
     int g = 0;                                          // S / P blocks of this tile so far
+    int last_buf = 0;                                   // P buffer holding the last output staging
     bool ok = true;
     for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
       const FwdUnit w = fwd_unit(p, u);
@@ -305,96 +336,103 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
         ok = mbar_wait(bar(FB_SFULL + x), par(g), abort_flag, p.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        // pass 1: the block's row maximum, one 32-column chunk of the score row at a time
-        // (causal mask on the diagonal block only)
+        // the block's score row (one TMEM round trip) and its maximum (causal mask on
+        // the diagonal block only)
         const bool diag = (j == qblk);
-        float mx = -INFINITY;
-        auto row_max = [&](auto diag_tag) {
-          constexpr bool DIAG = decltype(diag_tag)::value;
+        uint32_t sr[4][32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t sr[32];
-            tmem_ld32_nowait(lane_base + s_col + c * 32, sr);
-            tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) tmem_ld32_nowait(lane_base + s_col + c * 32, sr[c]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(FB_SEMPTY + x));
+        // eight independent partial maxima (no 128-long dependency chain)
+        float mxp[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mxp[t] = -INFINITY;
+        if (diag) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-              if (!DIAG || c * 32 + e <= r) mx = fmaxf(mx, __uint_as_float(sr[e]));
-          }
-        };
-        if (diag) row_max(std::true_type{});
-        else row_max(std::false_type{});
+              if (c * 32 + e <= r) mxp[e & 7] = fmaxf(mxp[e & 7], __uint_as_float(sr[c][e]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mxp[e & 7] = fmaxf(mxp[e & 7], __uint_as_float(sr[c][e]));
+        }
+        float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                         fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
         mx *= sl2;
         float alpha = 1.0f;
         if (mx > m + RESCALE_LOG2) {
           alpha = fast_exp2(m - mx);
           m = mx;
         }
-        if (j > 0) {
-          // P V of the previous block is complete: O is stable and the P tile free
-          ok = mbar_wait(bar(FB_ODONE + x), par(g - 1), abort_flag, p.err);
+        // P buffer g & 1 was last read by P V of block g - 2
+        const int bf = g & 1;
+        if (g >= 2) {
+          ok = mbar_wait(bar(FB_ODONE + 2 * x + bf), par((g - 2) >> 1), abort_flag, p.err);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        }
+        if (lane == 0) bulk_wait_read();   // an output store may still read this warp's slice
+        __syncwarp();
+        const uint32_t p_tile = base + F_SM_P + (2 * x + bf) * 2 * TILE;
+        // P = exp2(s sl2 - m) as bf16, 32 keys at a time straight into the operand tile;
+        // the row sum in eight independent partials
+        float sp[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) sp[t] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float p0 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * e]), sl2, -m));
+            float p1 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * e + 1]), sl2, -m));
+            if (diag) {
+              if (c * 32 + 2 * e > r) p0 = 0.f;
+              if (c * 32 + 2 * e + 1 > r) p1 = 0.f;
+            }
+            sp[(2 * e) & 7] += p0;
+            sp[(2 * e + 1) & 7] += p1;
+            pk[e] = pack2_bf16(p0, p1);
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int unit = (c & 1) * 4 + v;
+            st_shared16(p_tile + (c >> 1) * TILE + r * 128 + ((unit ^ (r & 7)) << 4),
+                        make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]));
+          }
+        }
+        const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+        l = l * alpha + sum;
+        // a moved maximum rescales O in tensor memory, after the previous P V and
+        // before this block's
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+          ok = mbar_wait(bar(FB_ODONE + 2 * x + (bf ^ 1)), par((g - 1) >> 1), abort_flag, p.err);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              uint32_t o[32];
-              tmem_ld32_nowait(lane_base + o_col + c * 32, o);
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              tmem_st32(lane_base + o_col + c * 32, o);
-            }
-            tmem_wait_st();
-          }
-        } else {
-          // the slice may still be the source of the previous unit's output store
-          if (lane == 0) bulk_wait_read();
-          __syncwarp();
-        }
-        // pass 2: P = exp2(s sl2 - m) as bf16, straight into the operand tile, and the sum
-        float sum = 0.f;
-        auto exp_pass = [&](auto diag_tag) {
-          constexpr bool DIAG = decltype(diag_tag)::value;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t sr[32], pk[16];
-            tmem_ld32_nowait(lane_base + s_col + c * 32, sr);
+          for (int c = 0; c < 2; ++c) {
+            uint32_t o[32];
+            tmem_ld32_nowait(lane_base + o_col + c * 32, o);
             tmem_wait_ld();
-            if (c == 3) {
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar(FB_SEMPTY + x));
-            }
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * e]), sl2, -m));
-              float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * e + 1]), sl2, -m));
-              if (DIAG) {
-                if (c * 32 + 2 * e > r) p0 = 0.f;
-                if (c * 32 + 2 * e + 1 > r) p1 = 0.f;
-              }
-              sum += p0 + p1;
-              pk[e] = pack2_bf16(p0, p1);
-            }
-            // 32 keys = four 16-byte units of the row in key half c / 2
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int unit = (c & 1) * 4 + u;
-              st_shared16(p_tile + (c >> 1) * TILE + r * 128 + ((unit ^ (r & 7)) << 4),
-                          make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
-            }
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(lane_base + o_col + c * 32, o);
           }
-        };
-        if (diag) exp_pass(std::true_type{});
-        else exp_pass(std::false_type{});
-        l = l * alpha + sum;
+          tmem_wait_st();
+        }
         fence_proxy_async();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(FB_PFULL + x));
+        if (lane == 0) mbar_arrive(bar(FB_PFULL + 2 * x + bf));
       }
       if (!ok) break;
-      ok = mbar_wait(bar(FB_ODONE + x), par(g - 1), abort_flag, p.err);
+      // the unit's last P V (block g - 1) is done: O is final
+      ok = mbar_wait(bar(FB_ODONE + 2 * x + ((g - 1) & 1)), par((g - 1) >> 1), abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       uint32_t o[2][32];
@@ -404,7 +442,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(FB_OFREE + x));
-      // O / l through this warp's slice (free: the last P V read it), one TMA store
+      // O / l through this warp's rows of the P buffer the last P V read (free now), one
+      // TMA store
+      last_buf = (g - 1) & 1;
+      const uint32_t slice = base + F_SM_P + (2 * x + last_buf) * 2 * TILE + q * 4096;
       stage_row64(slice, lane, reinterpret_cast<const float*>(o), 1.0f / l);
       fence_proxy_async();
       __syncwarp();
@@ -414,6 +455,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
       }
       if (query < p.T) p.lse[((size_t)w.b * p.H + w.h) * p.T + query] = (m + __log2f(l)) * LN2;
     }
+    (void)last_buf;
     if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
@@ -634,17 +676,18 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
         // P^T and dS^T of 64 query columns, 32 at a time (S^T, dP^T released after the
         // second load), each chunk stored as soon as it is computed; the mask (causal on
         // the diagonal block, past T on the last) only in the blocks that need it
+        uint32_t sv[2][32], dv[2][32];
+        tmem_ld32_nowait(lane_base + COL_S + c0, sv[0]);
+        tmem_ld32_nowait(lane_base + COL_DP + c0, dv[0]);
+        tmem_ld32_nowait(lane_base + COL_S + c0 + 32, sv[1]);
+        tmem_ld32_nowait(lane_base + COL_DP + c0 + 32, dv[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(KB_SEMPTY));
         auto chunk = [&](int c, auto masked_tag) -> bool {
           constexpr bool MASKED = decltype(masked_tag)::value;
-          uint32_t sv[32], dv[32], pk[16], dk[16];
-          tmem_ld32_nowait(lane_base + COL_S + c0 + c * 32, sv);
-          tmem_ld32_nowait(lane_base + COL_DP + c0 + c * 32, dv);
-          tmem_wait_ld();
-          if (c == 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(KB_SEMPTY));
-          }
+          uint32_t pk[16], dk[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
             const float4 L = lse4[c * 8 + e4], Dd = D4[c * 8 + e4];
@@ -653,8 +696,8 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
               const int e = e4 * 4 + t;
-              float pv = fast_exp2(fmaf(__uint_as_float(sv[e]), sl2, -lv[t] * LOG2E));
-              float dsv = pv * (__uint_as_float(dv[e]) - dd[t]);
+              float pv = fast_exp2(fmaf(__uint_as_float(sv[c][e]), sl2, -lv[t] * LOG2E));
+              float dsv = pv * (__uint_as_float(dv[c][e]) - dd[t]);
               if (MASKED) {
                 // past T the lse / D entries were never loaded: zero both results outright
                 const int query = q0 + c * 32 + e;
@@ -921,29 +964,29 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
         ok = mbar_wait(bar(QB_SFULL), par(g), abort_flag, p.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
+        uint32_t sv[2][32], dv[2][32];
+        tmem_ld32_nowait(lane_base + COL_S + c0, sv[0]);
+        tmem_ld32_nowait(lane_base + COL_DP + c0, dv[0]);
+        tmem_ld32_nowait(lane_base + COL_S + c0 + 32, sv[1]);
+        tmem_ld32_nowait(lane_base + COL_DP + c0 + 32, dv[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(QB_SEMPTY));
         const int k0 = j * BKV + c0;
         uint32_t dk[32];
         auto compute = [&](auto masked_tag) {   // causal mask on the diagonal block only
           constexpr bool MASKED = decltype(masked_tag)::value;
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            uint32_t sv[32], dv[32];
-            tmem_ld32_nowait(lane_base + COL_S + c0 + c * 32, sv);
-            tmem_ld32_nowait(lane_base + COL_DP + c0 + c * 32, dv);
-            tmem_wait_ld();
-            if (c == 1) {
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar(QB_SEMPTY));
-            }
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
               float ds[2];
 #pragma unroll
               for (int t = 0; t < 2; ++t) {
-                float pv = fast_exp2(fmaf(__uint_as_float(sv[e + t]), sl2, nlse2));
+                float pv = fast_exp2(fmaf(__uint_as_float(sv[c][e + t]), sl2, nlse2));
                 if (MASKED && k0 + c * 32 + e + t > query) pv = 0.f;
-                ds[t] = pv * (__uint_as_float(dv[e + t]) - Dr);
+                ds[t] = pv * (__uint_as_float(dv[c][e + t]) - Dr);
               }
               dk[c * 16 + e / 2] = pack2_bf16(ds[0], ds[1]);
             }
