@@ -458,6 +458,28 @@ cudaError_t splitk_reduce(float* accum, const float* ws, int splits, long long n
   return last();
 }
 
+// accum += sum_k ws[k] in k order, then ws = 0
+__global__ void splitk_fold_kernel(float* __restrict__ accum, float* __restrict__ ws, int splits,
+                                   long long n4, long long n) {
+  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  float4 a = reinterpret_cast<float4*>(accum)[i];
+  for (int k = 0; k < splits; ++k) {
+    float4* wp = reinterpret_cast<float4*>(ws + (size_t)k * n) + i;
+    const float4 w = *wp;
+    a.x += w.x; a.y += w.y; a.z += w.z; a.w += w.w;
+    *wp = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  reinterpret_cast<float4*>(accum)[i] = a;
+}
+
+cudaError_t splitk_fold(float* accum, float* ws, int splits, long long n, cudaStream_t s) {
+  if (n % 4) return cudaErrorInvalidValue;
+  long long n4 = n / 4;
+  splitk_fold_kernel<<<ceil_div(n4, 256), 256, 0, s>>>(accum, ws, splits, n4, n); count_launches(1);
+  return last();
+}
+
 // =====================================================================================
 // Global gradient norm and clip coefficient, on device (no host sync):
 // out[0] = ||g||_2, out[1] = max_norm > 0 ? min(1, max_norm / (||g|| + 1e-6)) : 1.

@@ -50,6 +50,8 @@ struct Params {
   int M, N, K;
   int num_m, num_n, splits, kb_per_split, num_kb;
   int epi;
+  int defer;      // split partials: 0 = summed into accum after the kernel, 1 = added into
+                  // the workspace, which the caller folds in later
   long long ldo;
   const bf16* bias; const bf16* resid; const bf16* aux;
   float scale;
@@ -93,7 +95,7 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const EpiMaps& m
   if (lane == 0) bulk_wait_read();
   __syncwarp();
   if (p.epi == EPI_ACCUM) {
-    stage_row_f32(stg, lane, v, p.splits == 1 ? p.scale : 1.0f);
+    stage_row_f32(stg, lane, v, (p.splits == 1 || p.defer) ? p.scale : 1.0f);
   } else {
     uint32_t w[16];
     if (p.epi == EPI_STORE) {
@@ -126,6 +128,7 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const EpiMaps& m
   if (lane == 0 && row0 < p.M) {   // stores start in range; TMA clips the rest
     if (p.epi == EPI_ACCUM) {
       if (p.splits == 1) tma_reduce_add_2d(&maps.out, stg, col0, row0);
+      else if (p.defer) tma_reduce_add_3d(&maps.out, stg, col0, row0, split);
       else tma_store_3d(&maps.out, stg, col0, row0, split);
     } else {
       tma_store_2d(&maps.out, stg, col0, row0);
@@ -367,6 +370,7 @@ static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
   p.kb_per_split = ceil_div(p.num_kb, p.splits);
   p.splits = ceil_div(p.num_kb, p.kb_per_split);
   p.epi = g.epi;
+  p.defer = g.defer_partials;
   p.ldo = g.ldo;
   p.bias = (const bf16*)g.bias; p.resid = (const bf16*)g.resid;
   p.aux = (const bf16*)g.aux;
@@ -399,7 +403,8 @@ static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
   gemm_kernel<BN, AMN, BMN><<<grid, THREADS, Cf::SMEM, s>>>(ma, mb, maps, p); count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (p.splits > 1) return splitk_reduce(g.accum, g.workspace, p.splits, (long long)g.M * g.N, g.scale, s);
+  if (p.splits > 1 && !p.defer)
+    return splitk_reduce(g.accum, g.workspace, p.splits, (long long)g.M * g.N, g.scale, s);
   return cudaSuccess;
 }
 

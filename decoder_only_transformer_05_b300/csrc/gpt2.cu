@@ -119,12 +119,26 @@ struct gpt2 {
   // backward scratch
   void *dres = nullptr, *dln = nullptr, *datt = nullptr, *dqkv = nullptr, *dfch = nullptr;
   float* Dbuf = nullptr;
-  float *ln_partials = nullptr, *colsum_partials = nullptr, *splitk_ws = nullptr;
+  float* splitk_ws = nullptr;
   float* norm_partials = nullptr;
   void* enc_scratch = nullptr;
   int* d_err = nullptr;
   float* d_loss = nullptr;
   float* d_norm = nullptr;
+
+  // Deferred gradient partial sums. The backward adds each micro-batch's per-block or
+  // per-split sums into these buffers (each element receives one addition per micro-batch,
+  // so the result does not depend on scheduling); flush_grads() folds them into the flat
+  // gradient buffer and clears them, once per optimiser step or when gradients are read.
+  struct DefWgrad { float* grad; float* ws; int splits; size_t n; };   // split-K weight grads
+  struct DefLN { float* dw; float* db; float* dproj; float* part; };   // LayerNorm (+ bias)
+  struct DefCol { float* db; float* part; int N; };                    // bias column sums
+  std::vector<DefWgrad> def_wg;   // [layer * 4 + kind], kinds: qkv, attproj, fc, fcproj
+  std::vector<DefLN> def_ln;      // LN1 [0, L), LN2 [L, 2L), lnf 2L
+  std::vector<DefCol> def_col;    // fc bias [0, L), qkv bias [L, 2L)
+  char* dmem = nullptr;
+  size_t dmem_bytes = 0;
+  bool grads_pending = false;
 
   // state
   int last_B = 0, last_T = 0;
@@ -327,20 +341,12 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   size_t o_logits = plan(M * (size_t)h->Vp * es), o_losses = plan(M * 4), o_argmax = plan(M * 4);
   size_t o_dres = plan(M * C * es), o_dln = plan(M * C * es), o_datt = plan(M * C * es);
   size_t o_dqkv = plan(M * 3 * C * es), o_dfch = plan(M * 4 * C * es), o_D = plan(BHT * 4);
-  size_t o_lnp = plan(layernorm_backward_partials_floats((int)M, (int)C, true) * 4);
-  size_t o_csp = plan(std::max(colsum_partials_floats((int)M, 3 * (int)C),
-                               colsum_partials_floats((int)M, 4 * (int)C)) * 4);
+  // split-K workspace for a tied lm_head gradient that needed one (it does not at these
+  // shapes; the per-layer weight gradients use the deferred buffers below)
   size_t ws = 0;
   if (h->is_bf16) {
-    const int sms = gemm_tc_num_sms();
-    const int shapes[4][2] = {{3 * (int)C, (int)C}, {(int)C, (int)C}, {4 * (int)C, (int)C},
-                              {(int)C, 4 * (int)C}};
-    for (auto& s : shapes) {
-      int sp = gemm_tc_pick_splits(s[0], s[1], (int)M, sms);
-      if (sp > 1) ws = std::max(ws, (size_t)sp * s[0] * s[1] * 4);
-    }
-    int sp = gemm_tc_pick_splits(h->Vp, (int)C, (int)M, sms);
-    if (sp > 1) ws = std::max(ws, (size_t)sp * h->Vp * C * 4);
+    int sp = gemm_tc_pick_splits(h->Vp, (int)C, (int)M, gemm_tc_num_sms());
+    if (sp > 1) ws = (size_t)sp * h->Vp * C * 4;
   }
   size_t o_ws = plan(ws + 256);
   size_t o_np = plan((size_t)norm_partials_count() * 4);
@@ -369,14 +375,71 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   h->logits = a + o_logits; h->losses = (float*)(a + o_losses); h->argmax = (int*)(a + o_argmax);
   h->dres = a + o_dres; h->dln = a + o_dln; h->datt = a + o_datt; h->dqkv = a + o_dqkv;
   h->dfch = a + o_dfch; h->Dbuf = (float*)(a + o_D);
-  h->ln_partials = (float*)(a + o_lnp); h->colsum_partials = (float*)(a + o_csp);
   h->splitk_ws = (float*)(a + o_ws); h->norm_partials = (float*)(a + o_np);
   h->enc_scratch = a + o_enc;
   h->d_err = (int*)(a + o_err); h->d_loss = (float*)(a + o_loss); h->d_norm = (float*)(a + o_norm);
 
+  // ---- deferred gradient partials (zeroed; see the handle)
+  {
+    size_t dneed = 0;
+    auto dplan = [&](size_t floats) { size_t o = dneed; dneed += align256(floats * 4); return o; };
+    struct WgPlan { int id; int N, K; };
+    const WgPlan kinds[4] = {{T_QKVW, 3 * (int)C, (int)C}, {T_ATTPROJW, (int)C, (int)C},
+                             {T_FCW, 4 * (int)C, (int)C}, {T_FCPROJW, (int)C, 4 * (int)C}};
+    std::vector<size_t> o_wg(4 * L, 0), o_ln(2 * L + 1), o_col(2 * L, 0);
+    std::vector<int> sp_wg(4 * L, 1);
+    for (size_t l = 0; l < L; ++l)
+      for (int k = 0; k < 4; ++k) {
+        int sp = h->is_bf16 ? gemm_tc_pick_splits(kinds[k].N, kinds[k].K, (int)M, gemm_tc_num_sms()) : 1;
+        sp_wg[l * 4 + k] = sp;
+        if (sp > 1) o_wg[l * 4 + k] = dplan((size_t)sp * kinds[k].N * kinds[k].K);
+      }
+    for (size_t i = 0; i < 2 * L + 1; ++i) o_ln[i] = dplan(layernorm_deferred_partials_floats((int)C, true));
+    if (h->bias)
+      for (size_t l = 0; l < L; ++l) {
+        o_col[l] = dplan(colsum_deferred_partials_floats((int)M, 4 * (int)C));
+        o_col[L + l] = dplan(colsum_deferred_partials_floats((int)M, 3 * (int)C));
+      }
+    h->dmem_bytes = dneed + 256;
+    if (cudaError_t e = cudaMalloc(&h->dmem, h->dmem_bytes); e != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(h->amem);
+      cudaFree(h->pmem);
+      delete h;
+      return fail(e == cudaErrorMemoryAllocation ? GPT2_ERR_OOM : GPT2_ERR_CUDA,
+                  "cudaMalloc of %zu bytes for gradient partials failed: %s", dneed,
+                  cudaGetErrorString(e));
+    }
+    char* d = h->dmem;
+    for (size_t l = 0; l < L; ++l)
+      for (int k = 0; k < 4; ++k) {
+        const int i = (int)(l * 4 + k);
+        h->def_wg.push_back({h->gw(kinds[k].id, (int)l), sp_wg[i] > 1 ? (float*)(d + o_wg[i]) : nullptr,
+                             sp_wg[i], (size_t)kinds[k].N * kinds[k].K});
+      }
+    auto bias_or_null = [&](int id, int layer) -> float* {
+      return (h->bias && layer >= 0) ? h->gw(id, layer) : nullptr;
+    };
+    for (size_t l = 0; l < L; ++l)   // LN1 of layer l feeds fcproj's bias of layer l - 1
+      h->def_ln.push_back({h->gw(T_LN1W, (int)l), h->gw(T_LN1B, (int)l),
+                           bias_or_null(T_FCPROJB, (int)l - 1), (float*)(d + o_ln[l])});
+    for (size_t l = 0; l < L; ++l)   // LN2 of layer l feeds attproj's bias of layer l
+      h->def_ln.push_back({h->gw(T_LN2W, (int)l), h->gw(T_LN2B, (int)l),
+                           bias_or_null(T_ATTPROJB, (int)l), (float*)(d + o_ln[L + l])});
+    h->def_ln.push_back({h->gw(T_LNFW), h->gw(T_LNFB), bias_or_null(T_FCPROJB, (int)L - 1),
+                         (float*)(d + o_ln[2 * L])});
+    if (h->bias) {
+      for (size_t l = 0; l < L; ++l)
+        h->def_col.push_back({h->gw(T_FCB, (int)l), (float*)(d + o_col[l]), 4 * (int)C});
+      for (size_t l = 0; l < L; ++l)
+        h->def_col.push_back({h->gw(T_QKVB, (int)l), (float*)(d + o_col[L + l]), 3 * (int)C});
+    }
+  }
+
   // ---- initial values
   int rc = GPT2_OK;
-  if (cudaMemset(h->pmem, 0, pbytes) != cudaSuccess || cudaMemset(h->amem, 0, need) != cudaSuccess)
+  if (cudaMemset(h->pmem, 0, pbytes) != cudaSuccess || cudaMemset(h->amem, 0, need) != cudaSuccess ||
+      cudaMemset(h->dmem, 0, h->dmem_bytes) != cudaSuccess)
     rc = fail(GPT2_ERR_CUDA, "cudaMemset failed");
   if (rc == GPT2_OK && cfg.init) {
     std::vector<float> host(P, 0.0f);
@@ -390,6 +453,7 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
       rc = fail(GPT2_ERR_CUDA, "bf16 copy failed");
   }
   if (rc != GPT2_OK) {
+    cudaFree(h->dmem);
     cudaFree(h->amem);
     cudaFree(h->pmem);
     delete h;
@@ -402,6 +466,7 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
 extern "C" void gpt2_destroy(gpt2_handle h) {
   if (!h) return;
   for (auto& p : h->prof) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
+  if (h->dmem) cudaFree(h->dmem);
   if (h->amem) cudaFree(h->amem);
   if (h->pmem) cudaFree(h->pmem);
   delete h;
@@ -428,12 +493,21 @@ static int check_device_errors(gpt2* h) {
   return GPT2_OK;
 }
 
-static cudaError_t run_gemm(gpt2* h, GemmArgs g) {
+static cudaError_t run_gemm(gpt2* h, GemmArgs g, const gpt2::DefWgrad* def = nullptr) {
   g.err = h->d_err;
   size_t pi = prof_begin(h, PC_GEMM);
   cudaError_t e;
   if (h->is_bf16) {
-    if (g.epi == EPI_ACCUM) { g.splits = 0; g.workspace = h->splitk_ws; }
+    if (g.epi == EPI_ACCUM) {
+      if (def && def->splits > 1) {   // partial sums stay in the layer's own workspace
+        g.splits = def->splits;
+        g.workspace = def->ws;
+        g.defer_partials = 1;
+      } else {
+        g.splits = 0;
+        g.workspace = h->splitk_ws;
+      }
+    }
     e = gemm_bf16_tc(g, h->stream);
   } else {
     e = gemm_f32(g, h->stream);
@@ -469,6 +543,21 @@ static GemmArgs linear_wgrad(int M, int N, int K, const void* dY, const void* X,
   g.B = X; g.ldb = K; g.b_mn = true;
   g.epi = EPI_ACCUM; g.accum = dW; g.ldo = K; g.scale = scale;
   return g;
+}
+
+// Fold the deferred partial sums into the gradient buffer (and clear them).
+static cudaError_t flush_grads(gpt2* h) {
+  if (!h->grads_pending) return cudaSuccess;
+  cudaStream_t s = h->stream;
+  cudaError_t e = cudaSuccess;
+  for (auto& d : h->def_wg)
+    if (e == cudaSuccess && d.splits > 1) e = splitk_fold(d.grad, d.ws, d.splits, (long long)d.n, s);
+  for (auto& d : h->def_ln)
+    if (e == cudaSuccess) e = layernorm_fold(d.dw, d.db, d.dproj, d.part, h->C, s);
+  for (auto& d : h->def_col)
+    if (e == cudaSuccess) e = bias_grad_fold(d.db, d.part, h->Bmax * h->T, d.N, s);
+  if (e == cudaSuccess) h->grads_pending = false;
+  return e;
 }
 
 #define CKL(x)                                                                              \
@@ -565,14 +654,19 @@ extern "C" int gpt2_backward(gpt2_handle h, float loss_scale) {
   CKL(run_gemm(h, linear_wgrad(M, Vp, C, h->logits, h->lnf, h->gw(T_WTE), sc)));
   // The column sums of each residual-stream gradient that a LayerNorm backward writes are
   // the bias gradient of the projection that fed that stream: lnf -> fcproj of layer L-1,
-  // LN2 of layer l -> attproj of layer l, LN1 of layer l -> fcproj of layer l-1.
-  auto proj_bias = [&](int id, int layer) -> float* {
-    return (h->bias && layer >= 0) ? h->gw(id, layer) : nullptr;
+  // LN2 of layer l -> attproj of layer l, LN1 of layer l -> fcproj of layer l-1 (the
+  // def_ln entries carry those targets). LayerNorm, bias and split weight-gradient sums
+  // go to the deferred partial buffers.
+  h->grads_pending = true;
+  auto ln_bwd = [&](int i, int acc, const void* x, int wid, int layer, const float* mean,
+                    const float* rstd) -> cudaError_t {
+    const gpt2::DefLN& d = h->def_ln[i];
+    return layernorm_backward(dt, h->dres, acc, d.dw, d.db, d.dproj, h->dln, x, h->pw(wid, layer),
+                              mean, rstd, M, C, sc, d.part, 1, s);
   };
+  auto wg = [&](int layer, int kind) { return &h->def_wg[layer * 4 + kind]; };
   pi = prof_begin(h, PC_LN);
-  CKL(layernorm_backward(dt, h->dres, 0, h->gw(T_LNFW), h->gw(T_LNFB), proj_bias(T_FCPROJB, L - 1),
-                         h->dln, h->x[L], h->pw(T_LNFW), h->lnf_mean, h->lnf_rstd, M, C, sc,
-                         h->ln_partials, s));
+  CKL(ln_bwd(2 * L, 0, h->x[L], T_LNFW, 0, h->lnf_mean, h->lnf_rstd));
   prof_end(h, pi, (double)M * C * es * 3);
   for (int l = L - 1; l >= 0; --l) {
     // x[l+1] = xmid + gelu(fch) Wp^T + bp  (bp's gradient came with dres, above)
@@ -580,39 +674,35 @@ extern "C" int gpt2_backward(gpt2_handle h, float loss_scale) {
     g.epi = EPI_GELU_BWD;
     g.aux = h->fch[l];
     CKL(run_gemm(h, g));
-    CKL(run_gemm(h, linear_wgrad(M, C, 4 * C, h->dres, h->fcg[l], h->gw(T_FCPROJW, l), sc)));
+    CKL(run_gemm(h, linear_wgrad(M, C, 4 * C, h->dres, h->fcg[l], h->gw(T_FCPROJW, l), sc), wg(l, 3)));
     // fch = ln2 Wfc^T + bfc
     CKL(run_gemm(h, linear_dgrad(M, 4 * C, C, h->dfch, h->pw(T_FCW, l), h->dln)));
-    CKL(run_gemm(h, linear_wgrad(M, 4 * C, C, h->dfch, h->ln2[l], h->gw(T_FCW, l), sc)));
+    CKL(run_gemm(h, linear_wgrad(M, 4 * C, C, h->dfch, h->ln2[l], h->gw(T_FCW, l), sc), wg(l, 2)));
     if (h->bias) {
       pi = prof_begin(h, PC_OTHER);
-      CKL(bias_grad(dt, h->gw(T_FCB, l), h->dfch, M, 4 * C, sc, h->colsum_partials, s));
+      CKL(bias_grad(dt, h->gw(T_FCB, l), h->dfch, M, 4 * C, sc, h->def_col[l].part, 1, s));
       prof_end(h, pi, (double)M * 4 * C * es);
     }
     pi = prof_begin(h, PC_LN);
-    CKL(layernorm_backward(dt, h->dres, 1, h->gw(T_LN2W, l), h->gw(T_LN2B, l),
-                           proj_bias(T_ATTPROJB, l), h->dln, h->xmid[l], h->pw(T_LN2W, l),
-                           h->ln2_mean[l], h->ln2_rstd[l], M, C, sc, h->ln_partials, s));
+    CKL(ln_bwd(L + l, 1, h->xmid[l], T_LN2W, l, h->ln2_mean[l], h->ln2_rstd[l]));
     prof_end(h, pi, (double)M * C * es * 4);
     // xmid = x + att Wo^T + bo  (bo's gradient came with dres, above)
     CKL(run_gemm(h, linear_dgrad(M, C, C, h->dres, h->pw(T_ATTPROJW, l), h->datt)));
-    CKL(run_gemm(h, linear_wgrad(M, C, C, h->dres, h->att[l], h->gw(T_ATTPROJW, l), sc)));
+    CKL(run_gemm(h, linear_wgrad(M, C, C, h->dres, h->att[l], h->gw(T_ATTPROJW, l), sc), wg(l, 1)));
     pi = prof_begin(h, PC_ATTN);
     CKL(attention_backward(dt, h->dqkv, h->Dbuf, h->datt, h->att[l], h->qkv[l], h->lse[l], B, T,
                            C, H, h->d_err, s));
     prof_end(h, pi, 2.5 * 2.0 * 2.0 * B * H * (double)T * (T + 1) / 2 * (C / H));
     // qkv = ln1 Wqkv^T + bqkv
     CKL(run_gemm(h, linear_dgrad(M, 3 * C, C, h->dqkv, h->pw(T_QKVW, l), h->dln)));
-    CKL(run_gemm(h, linear_wgrad(M, 3 * C, C, h->dqkv, h->ln1[l], h->gw(T_QKVW, l), sc)));
+    CKL(run_gemm(h, linear_wgrad(M, 3 * C, C, h->dqkv, h->ln1[l], h->gw(T_QKVW, l), sc), wg(l, 0)));
     if (h->bias) {
       pi = prof_begin(h, PC_OTHER);
-      CKL(bias_grad(dt, h->gw(T_QKVB, l), h->dqkv, M, 3 * C, sc, h->colsum_partials, s));
+      CKL(bias_grad(dt, h->gw(T_QKVB, l), h->dqkv, M, 3 * C, sc, h->def_col[L + l].part, 1, s));
       prof_end(h, pi, (double)M * 3 * C * es);
     }
     pi = prof_begin(h, PC_LN);
-    CKL(layernorm_backward(dt, h->dres, 1, h->gw(T_LN1W, l), h->gw(T_LN1B, l),
-                           proj_bias(T_FCPROJB, l - 1), h->dln, h->x[l], h->pw(T_LN1W, l),
-                           h->ln1_mean[l], h->ln1_rstd[l], M, C, sc, h->ln_partials, s));
+    CKL(ln_bwd(l, 1, h->x[l], T_LN1W, l, h->ln1_mean[l], h->ln1_rstd[l]));
     prof_end(h, pi, (double)M * C * es * 4);
   }
   pi = prof_begin(h, PC_ENC);
@@ -625,6 +715,8 @@ extern "C" int gpt2_backward(gpt2_handle h, float loss_scale) {
 extern "C" int gpt2_zero_grad(gpt2_handle h) {
   if (!h) return fail(GPT2_ERR_ARG, "null handle");
   CK(cudaMemsetAsync(h->grads, 0, h->P * 4, h->stream));
+  if (h->grads_pending) CK(cudaMemsetAsync(h->dmem, 0, h->dmem_bytes, h->stream));
+  h->grads_pending = false;
   return GPT2_OK;
 }
 
@@ -632,6 +724,7 @@ extern "C" int gpt2_zero_grad(gpt2_handle h) {
 extern "C" int gpt2_adamw_step(gpt2_handle h, float lr, float beta1, float beta2, float eps,
                                float weight_decay, float grad_clip, float* h_grad_norm) {
   if (!h) return fail(GPT2_ERR_ARG, "null handle");
+  CKL(flush_grads(h));
   h->step += 1;
   cudaStream_t s = h->stream;
   const bool norm = grad_clip > 0.f || h_grad_norm;
@@ -691,6 +784,10 @@ extern "C" int gpt2_num_params(gpt2_handle h, size_t* n_model, size_t* n_buffer)
 
 static int region(gpt2* h, int r, void** p, size_t* bytes) {
   const size_t M = (size_t)(h->last_B ? h->last_B * h->last_T : h->Bmax * h->T);
+  if (r == GPT2_REGION_GRADS) {
+    cudaError_t e = flush_grads(h);
+    if (e != cudaSuccess) return fail(GPT2_ERR_CUDA, "gradient fold failed: %s", cudaGetErrorString(e));
+  }
   switch (r) {
     case GPT2_REGION_PARAMS: *p = h->params; *bytes = h->P * 4; return GPT2_OK;
     case GPT2_REGION_GRADS: *p = h->grads; *bytes = h->P * 4; return GPT2_OK;

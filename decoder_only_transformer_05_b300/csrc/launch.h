@@ -39,6 +39,10 @@ struct GemmArgs {
   float scale = 1.0f;
   int splits = 1;                           // EPI_ACCUM split-K count (tensor-core path)
   float* workspace = nullptr;               // splits * M * N fp32 when splits > 1
+  // split-K partials of EPI_ACCUM: 0 = summed into accum right after the kernel (workspace
+  // contents overwritten); 1 = scaled and added into the workspace, which holds the running
+  // sums until the caller folds them in with splitk_fold (which also clears them)
+  int defer_partials = 0;
   int* err = nullptr;                       // device error word
 };
 
@@ -53,6 +57,8 @@ int gemm_tc_pick_splits(int M, int N, int K, int num_sms);
 // Sum of split-K partials into the fp32 accumulator: accum += scale * sum_s ws[s].
 cudaError_t splitk_reduce(float* accum, const float* ws, int splits, long long n,
                           float scale, cudaStream_t s);
+// accum += sum_s ws[s] (fixed order), then ws = 0: folds deferred split-K partials.
+cudaError_t splitk_fold(float* accum, float* ws, int splits, long long n, cudaStream_t s);
 int gemm_tc_num_sms();
 
 // ---------------------------------------------------------------- elementwise
@@ -71,12 +77,19 @@ cudaError_t layernorm_forward(DType t, void* y, float* mean, float* rstd, const 
 // is non-null, dproj += scale * column sums of the dres this call writes (the bias
 // gradient of the projection that produced the residual stream). Two deterministic
 // stages; partials: layernorm_backward_partials_floats(M, C, dproj != nullptr) floats.
+// defer = 1 leaves the scaled per-block sums added into `partials` (which must start at
+// zero and have room for LNB_MAX_BLOCKS blocks) for a later layernorm_fold.
 int layernorm_backward_blocks(int M);
 size_t layernorm_backward_partials_floats(int M, int C, bool dproj);
+size_t layernorm_deferred_partials_floats(int C, bool dproj);
 cudaError_t layernorm_backward(DType t, void* dres, int accumulate, float* dw, float* db,
                                float* dproj, const void* dy, const void* x, const void* w,
                                const float* mean, const float* rstd, int M, int C, float scale,
-                               float* partials, cudaStream_t s);
+                               float* partials, int defer, cudaStream_t s);
+// dw += sum of the deferred partials' first C columns, db the next C, dproj (if non-null)
+// the last C; the partials are cleared.
+cudaError_t layernorm_fold(float* dw, float* db, float* dproj, float* partials, int C,
+                           cudaStream_t s);
 
 // Fused classifier over the logits rows: per row loss = lse - z[y] over the first V
 // columns; in place, logits become dlogits = (softmax - onehot) / M (0 in pad columns).
@@ -89,10 +102,14 @@ cudaError_t argmax_rows(DType t, int* out, const void* logits, int M, int V, int
                         cudaStream_t s);
 
 // Bias gradient: db[n] += scale * sum_m dy[m, n] (two deterministic stages);
-// partials: colsum_partials_floats(M, N) floats.
+// partials: colsum_partials_floats(M, N) floats. defer = 1 leaves the scaled chunk sums
+// added into `partials` (zero-initialised, colsum_deferred_partials_floats(M_max, N)
+// floats) for a later bias_grad_fold.
 size_t colsum_partials_floats(int M, int N);
+size_t colsum_deferred_partials_floats(int M_max, int N);
 cudaError_t bias_grad(DType t, float* db, const void* dy, int M, int N, float scale,
-                      float* partials, cudaStream_t s);
+                      float* partials, int defer, cudaStream_t s);
+cudaError_t bias_grad_fold(float* db, float* partials, int M_max, int N, cudaStream_t s);
 
 // ---------------------------------------------------------------- attention
 // qkv [B, T, 3C] -> out [B, T, C], lse [B, H, T] (natural log). The bf16 path runs the

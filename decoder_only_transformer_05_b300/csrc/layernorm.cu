@@ -138,6 +138,9 @@ int layernorm_backward_blocks(int M) {
 size_t layernorm_backward_partials_floats(int M, int C, bool dproj) {
   return (size_t)layernorm_backward_blocks(M) * (dproj ? 3 : 2) * (size_t)C;
 }
+size_t layernorm_deferred_partials_floats(int C, bool dproj) {
+  return (size_t)LNB_MAX_BLOCKS * (dproj ? 3 : 2) * (size_t)C;
+}
 
 // Two blocks per SM while the per-lane column sums fit in 128 registers (C <= 768 bf16).
 template <typename T, int MAXV, bool DPROJ>
@@ -145,7 +148,7 @@ __global__ void __launch_bounds__(LNB_THREADS, (MAXV * (int)sizeof(T) <= 6 ? 2 :
 ln_bwd_kernel(T* __restrict__ dres, int accumulate, float* __restrict__ partials,
               const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ w,
               const float* __restrict__ mean, const float* __restrict__ rstd, int M, int C,
-              int stages) {
+              int stages, int defer, float pscale) {
   constexpr int VE = 16 / sizeof(T);
   extern __shared__ __align__(16) uint8_t lnb_smem[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -263,23 +266,24 @@ ln_bwd_kernel(T* __restrict__ dres, int accumulate, float* __restrict__ partials
     float s = 0.f;
 #pragma unroll
     for (int k = 0; k < LNB_ROWS; ++k) s += red[(size_t)k * nk * C + c];
-    outp[c] = s;
+    outp[c] = defer ? outp[c] + pscale * s : s;   // deferred: this block's running sum
   }
 }
 
 // out_k[c] += scale * sum_{b < nparts} partials[b * stride + k * N + c]  for the k with
-// out_k non-null. Block: 32 columns x 8 row groups; group g adds parts g, g + 8, ... in
-// order, then the 8 groups are added in order.
+// out_k non-null (and, with clear, the partials are zeroed after being read). Block: 32
+// columns x 8 row groups; group g adds parts g, g + 8, ... in order, then the 8 groups
+// are added in order.
 __global__ void __launch_bounds__(256)
 column_reduce_kernel(float* __restrict__ out0, float* __restrict__ out1, float* __restrict__ out2,
-                     const float* __restrict__ partials, int nparts, int N, int nk, int stride,
-                     float scale) {
+                     float* __restrict__ partials, int nparts, int N, int nk, int stride,
+                     float scale, int clear) {
   __shared__ float sh[8][33];
   const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
   const int col = blockIdx.x * 32 + lane;   // over nk * N
   float s = 0.f;
   if (col < nk * N) {
-    const float* p = partials + col;
+    float* p = partials + col;
     int b = g;
     for (; b + 24 < nparts; b += 32) {
       float a0 = p[(size_t)b * stride], a1 = p[(size_t)(b + 8) * stride];
@@ -287,6 +291,8 @@ column_reduce_kernel(float* __restrict__ out0, float* __restrict__ out1, float* 
       s += a0; s += a1; s += a2; s += a3;
     }
     for (; b < nparts; b += 8) s += p[(size_t)b * stride];
+    if (clear)
+      for (b = g; b < nparts; b += 8) p[(size_t)b * stride] = 0.f;
   }
   sh[g][lane] = s;
   __syncthreads();
@@ -300,11 +306,11 @@ column_reduce_kernel(float* __restrict__ out0, float* __restrict__ out1, float* 
   }
 }
 
-static cudaError_t column_reduce(float* o0, float* o1, float* o2, const float* partials,
+static cudaError_t column_reduce(float* o0, float* o1, float* o2, float* partials,
                                  int nparts, int N, int nk, int stride, float scale,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, int clear = 0) {
   column_reduce_kernel<<<ceil_div((long long)nk * N, 32), 256, 0, s>>>(o0, o1, o2, partials, nparts,
-                                                                       N, nk, stride, scale);
+                                                                       N, nk, stride, scale, clear);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -313,7 +319,7 @@ template <typename T>
 static cudaError_t ln_bwd_dispatch(T* dres, int acc, float* dw, float* db, float* dproj,
                                    const T* dy, const T* x, const T* w, const float* mean,
                                    const float* rstd, int M, int C, float scale,
-                                   float* partials, cudaStream_t s) {
+                                   float* partials, int defer, cudaStream_t s) {
   constexpr int VE = 16 / sizeof(T);
   if (!aligned16(dres) || !aligned16(dy) || !aligned16(x) || !aligned16(w))
     return cudaErrorInvalidValue;
@@ -331,7 +337,7 @@ static cudaError_t ln_bwd_dispatch(T* dres, int acc, float* dw, float* db, float
                                          (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<blocks, LNB_THREADS, smem, s>>>(dres, acc, partials, dy, x, w, mean, rstd, M, C,
-                                           stages);
+                                           stages, defer, scale);
     count_launches(1);
     return cudaGetLastError();
   };
@@ -350,24 +356,31 @@ static cudaError_t ln_bwd_dispatch(T* dres, int acc, float* dw, float* db, float
   }
 #undef LNB_CASE
   if (e != cudaSuccess) return e;
+  if (defer) return cudaSuccess;
   return column_reduce(dw, db, dproj, partials, blocks, C, nk, nk * C, scale, s);
+}
+
+cudaError_t layernorm_fold(float* dw, float* db, float* dproj, float* partials, int C,
+                           cudaStream_t s) {
+  const int nk = dproj ? 3 : 2;
+  return column_reduce(dw, db, dproj, partials, LNB_MAX_BLOCKS, C, nk, nk * C, 1.0f, s, 1);
 }
 
 cudaError_t layernorm_backward(DType t, void* dres, int accumulate, float* dw, float* db,
                                float* dproj, const void* dy, const void* x, const void* w,
                                const float* mean, const float* rstd, int M, int C, float scale,
-                               float* partials, cudaStream_t s) {
+                               float* partials, int defer, cudaStream_t s) {
   if (M <= 0 || C <= 0) return cudaErrorInvalidValue;
   if (t == DType::BF16) {
     if (C % 8) return cudaErrorInvalidValue;
     return ln_bwd_dispatch<bf16>((bf16*)dres, accumulate, dw, db, dproj, (const bf16*)dy,
                                  (const bf16*)x, (const bf16*)w, mean, rstd, M, C, scale,
-                                 partials, s);
+                                 partials, defer, s);
   }
   if (C % 4) return cudaErrorInvalidValue;
   return ln_bwd_dispatch<float>((float*)dres, accumulate, dw, db, dproj, (const float*)dy,
                                 (const float*)x, (const float*)w, mean, rstd, M, C, scale,
-                                partials, s);
+                                partials, defer, s);
 }
 
 // =====================================================================================
@@ -386,17 +399,20 @@ static void colsum_shape(int M, int N, int ve, int* strips, int* chunks, int* rp
   *chunks = ceil_div(M, *rpc);
 }
 
-size_t colsum_partials_floats(int M, int N) {
-  int strips, chunks, rpc;
-  colsum_shape(M, N, 8, &strips, &chunks, &rpc);
-  size_t a = (size_t)chunks * N;
+static int colsum_max_chunks(int M, int N) {
+  int strips, chunks, rpc, c8;
+  colsum_shape(M, N, 8, &strips, &c8, &rpc);
   colsum_shape(M, N, 4, &strips, &chunks, &rpc);
-  return std::max(a, (size_t)chunks * N);
+  return std::max(c8, chunks);
 }
+size_t colsum_partials_floats(int M, int N) { return (size_t)colsum_max_chunks(M, N) * N; }
+// chunk counts only shrink with M, so a buffer sized for M_max serves every M <= M_max
+size_t colsum_deferred_partials_floats(int M_max, int N) { return colsum_partials_floats(M_max, N); }
 
 template <typename T>
 __global__ void __launch_bounds__(COLSUM_THREADS)
-colsum_kernel(float* __restrict__ partials, const T* __restrict__ dy, int M, int N, int rpc) {
+colsum_kernel(float* __restrict__ partials, const T* __restrict__ dy, int M, int N, int rpc,
+              int defer, float pscale) {
   constexpr int VE = 16 / sizeof(T);
   __shared__ float sh[COLSUM_THREADS / 32][32 * VE];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -431,12 +447,13 @@ colsum_kernel(float* __restrict__ partials, const T* __restrict__ dy, int M, int
     float s = 0.f;
 #pragma unroll
     for (int k = 0; k < COLSUM_THREADS / 32; ++k) s += sh[k][i];
-    partials[(size_t)blockIdx.y * N + col] = s;
+    float* o = partials + (size_t)blockIdx.y * N + col;
+    *o = defer ? *o + pscale * s : s;   // deferred: this chunk's running sum
   }
 }
 
 cudaError_t bias_grad(DType t, float* db, const void* dy, int M, int N, float scale,
-                      float* partials, cudaStream_t s) {
+                      float* partials, int defer, cudaStream_t s) {
   if (M <= 0 || N <= 0) return cudaErrorInvalidValue;
   const int ve = t == DType::BF16 ? 8 : 4;
   if (N % ve || !aligned16(dy)) return cudaErrorInvalidValue;
@@ -444,13 +461,20 @@ cudaError_t bias_grad(DType t, float* db, const void* dy, int M, int N, float sc
   colsum_shape(M, N, ve, &strips, &chunks, &rpc);
   dim3 grid(strips, chunks);
   if (t == DType::BF16)
-    colsum_kernel<bf16><<<grid, COLSUM_THREADS, 0, s>>>(partials, (const bf16*)dy, M, N, rpc);
+    colsum_kernel<bf16><<<grid, COLSUM_THREADS, 0, s>>>(partials, (const bf16*)dy, M, N, rpc,
+                                                        defer, scale);
   else
-    colsum_kernel<float><<<grid, COLSUM_THREADS, 0, s>>>(partials, (const float*)dy, M, N, rpc);
+    colsum_kernel<float><<<grid, COLSUM_THREADS, 0, s>>>(partials, (const float*)dy, M, N, rpc,
+                                                         defer, scale);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || defer) return e;
   return column_reduce(db, nullptr, nullptr, partials, chunks, N, 1, N, scale, s);
+}
+
+cudaError_t bias_grad_fold(float* db, float* partials, int M_max, int N, cudaStream_t s) {
+  return column_reduce(db, nullptr, nullptr, partials, colsum_max_chunks(M_max, N), N, 1, N, 1.0f,
+                       s, 1);
 }
 
 }  // namespace gpt2k

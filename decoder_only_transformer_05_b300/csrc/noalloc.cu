@@ -80,7 +80,7 @@ extern "C" int gpt2_op_layernorm_backward_noalloc(int precision, void* dres, int
   // reduction reads it, so the previous call's contents never need clearing.
   cudaError_t e = layernorm_backward(precision == GPT2_BF16 ? DType::BF16 : DType::F32, dres,
                                      accumulate, dw, db, nullptr, dy, x, w, mean, rstd, M, C,
-                                     scale, scratch, (cudaStream_t)stream);
+                                     scale, scratch, 0, (cudaStream_t)stream);
   if (e == cudaSuccess) return GPT2_OK;
   if (e == cudaErrorInvalidValue)
     return gpt2_set_error(GPT2_ERR_ARG, "unsupported shape, alignment or argument");

@@ -71,7 +71,7 @@ extern "C" int gpt2_op_layernorm_backward(int precision, void* dres, int accumul
                                           int M, int C, float scale, float* partials,
                                           void* stream) {
   return status(layernorm_backward(dtype(precision), dres, accumulate, dw, db, nullptr, dy, x,
-                                   w, mean, rstd, M, C, scale, partials, (cudaStream_t)stream));
+                                   w, mean, rstd, M, C, scale, partials, 0, (cudaStream_t)stream));
 }
 
 extern "C" int gpt2_op_classifier(int precision, void* logits, float* losses,

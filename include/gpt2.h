@@ -123,12 +123,18 @@ int gpt2_forward(gpt2_handle h, const int32_t* d_tokens, const int32_t* d_target
 
 /*
  * Backward pass of the last forward (which must have had targets). Adds
- * loss_scale * d(mean loss)/d(param) to the gradient region (gradients accumulate, as
- * in PyTorch; use loss_scale = 1/accum for gradient accumulation).
+ * loss_scale * d(mean loss)/d(param) to the gradients (gradients accumulate, as in
+ * PyTorch; use loss_scale = 1/accum for gradient accumulation). The bf16 path needs
+ * T % 4 == 0 (GPT2_ERR_ARG otherwise).
+ * Some contributions (the LayerNorm and bias gradients' per-block sums, the split-K
+ * partial sums of the weight gradients) are kept in library-owned buffers across calls and
+ * folded into GPT2_REGION_GRADS, in a fixed order, when the gradients are next read:
+ * gpt2_adamw_step, gpt2_copy_region / gpt2_region_ptr of GPT2_REGION_GRADS. Read the
+ * gradients through those calls, not through a pointer obtained before a backward.
  */
 int gpt2_backward(gpt2_handle h, float loss_scale);
 
-/* Set every gradient to zero. */
+/* Set every gradient (and every pending partial sum) to zero. */
 int gpt2_zero_grad(gpt2_handle h);
 
 /*
@@ -165,7 +171,8 @@ int gpt2_num_params(gpt2_handle h, size_t* n_model, size_t* n_buffer);
  */
 int gpt2_copy_region(gpt2_handle h, int region, size_t offset, void* h_buf, size_t bytes,
                      int to_device);
-/* Device address and size in bytes of a region (no copy, no wait). */
+/* Device address and size in bytes of a region (no copy, no wait; for GPT2_REGION_GRADS
+   the pending partial sums are first folded in, queued on the stream). */
 int gpt2_region_ptr(gpt2_handle h, int region, void** d_ptr, size_t* bytes);
 
 /* AdamW step counter (for checkpoint/resume together with PARAMS, M and V). */
