@@ -140,6 +140,14 @@ struct gpt2 {
   size_t dmem_bytes = 0;
   bool grads_pending = false;
 
+  // gpt2_forward_backward: token/target copies and one CUDA graph of the micro-batch per
+  // (B, T, loss scale)
+  int32_t *mb_tok = nullptr, *mb_tgt = nullptr;
+  struct MicroGraph { int B, T; float scale; cudaGraphExec_t exec; long long launches; };
+  std::vector<MicroGraph> graphs;
+  bool graph_mode = true;
+  cudaStream_t cap_stream = nullptr;
+
   // state
   int last_B = 0, last_T = 0;
   bool have_targets = false;
@@ -352,6 +360,7 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   size_t o_np = plan((size_t)norm_partials_count() * 4);
   size_t o_enc = plan(encoder_backward_scratch_bytes((int)M, h->Vp));
   size_t o_err = plan(64), o_loss = plan(64), o_norm = plan(64);
+  size_t o_mbtok = plan(M * 4), o_mbtgt = plan(M * 4);
   h->amem_bytes = need;
   if (cudaError_t e = cudaMalloc(&h->amem, need); e != cudaSuccess) {
     cudaGetLastError();
@@ -378,6 +387,7 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   h->splitk_ws = (float*)(a + o_ws); h->norm_partials = (float*)(a + o_np);
   h->enc_scratch = a + o_enc;
   h->d_err = (int*)(a + o_err); h->d_loss = (float*)(a + o_loss); h->d_norm = (float*)(a + o_norm);
+  h->mb_tok = (int32_t*)(a + o_mbtok); h->mb_tgt = (int32_t*)(a + o_mbtgt);
 
   // ---- deferred gradient partials (zeroed; see the handle)
   {
@@ -466,6 +476,8 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
 extern "C" void gpt2_destroy(gpt2_handle h) {
   if (!h) return;
   for (auto& p : h->prof) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
+  for (auto& g : h->graphs) cudaGraphExecDestroy(g.exec);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   if (h->dmem) cudaFree(h->dmem);
   if (h->amem) cudaFree(h->amem);
   if (h->pmem) cudaFree(h->pmem);
@@ -709,6 +721,88 @@ extern "C" int gpt2_backward(gpt2_handle h, float loss_scale) {
   CKL(encoder_backward(dt, h->gw(T_WTE), h->gw(T_WPE), h->dres, h->last_tokens, B, T, C, Vp, sc,
                        h->enc_scratch, s));
   prof_end(h, pi, (double)M * C * es * 2);
+  return GPT2_OK;
+}
+
+// ------------------------------------------------------------------ micro-batch as a graph
+// The ~275 launches of a forward + backward are recorded once per (B, T, loss scale) into
+// a CUDA graph on a private capturing stream and replayed on the handle's stream, which
+// removes the per-launch host work and most of the gaps between dependent kernels. The
+// graph reads tokens and targets from the handle's own buffers, so every replay works on
+// whatever the caller copied in last; all other buffers have fixed addresses.
+static int microbatch_eager(gpt2* h, int B, int T, float scale) {
+  int rc = gpt2_forward(h, h->mb_tok, h->mb_tgt, B, T, nullptr);
+  return rc ? rc : gpt2_backward(h, scale);
+}
+
+static int microbatch_capture(gpt2* h, int B, int T, float scale) {
+  if (!h->cap_stream) CK(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
+  const long long n0 = launch_counter();
+  cudaStream_t user = h->stream;
+  h->stream = h->cap_stream;
+  CK(cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
+  const int rc = microbatch_eager(h, B, T, scale);   // recorded, not executed
+  cudaGraph_t graph = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(h->cap_stream, &graph);
+  h->stream = user;
+  const long long launches = launch_counter() - n0;
+  launch_counter() = n0;
+  if (rc || e != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    if (rc) return rc;
+    return fail(GPT2_ERR_CUDA, "stream capture of the micro-batch failed: %s",
+                cudaGetErrorString(e));
+  }
+  cudaGraphExec_t exec = nullptr;
+  const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (ei != cudaSuccess)
+    return fail(GPT2_ERR_CUDA, "cudaGraphInstantiate: %s", cudaGetErrorString(ei));
+  if (h->graphs.size() >= 8) {
+    cudaGraphExecDestroy(h->graphs.front().exec);
+    h->graphs.erase(h->graphs.begin());
+  }
+  h->graphs.push_back({B, T, scale, exec, launches});
+  return GPT2_OK;
+}
+
+extern "C" int gpt2_forward_backward(gpt2_handle h, const int32_t* tokens,
+                                     const int32_t* targets, int32_t B, int32_t T,
+                                     float loss_scale) {
+  if (!h || !tokens || !targets) return fail(GPT2_ERR_ARG, "null argument");
+  if (B <= 0 || T <= 0) return fail(GPT2_ERR_ARG, "B and T must be positive");
+  if (T > h->T || B > h->Bmax)
+    return fail(GPT2_ERR_SEQ_TOO_LONG, "T=%d > block_size=%d or B=%d > batch_size=%d", T, h->T,
+                B, h->Bmax);
+  if (h->is_bf16 && T % 4)
+    return fail(GPT2_ERR_ARG, "the bf16 backward needs T %% 4 == 0 (T = %d)", T);
+  const size_t bytes = (size_t)B * T * sizeof(int32_t);
+  CK(cudaMemcpyAsync(h->mb_tok, tokens, bytes, cudaMemcpyDefault, h->stream));
+  CK(cudaMemcpyAsync(h->mb_tgt, targets, bytes, cudaMemcpyDefault, h->stream));
+  // timed launches (gpt2_profile_enable) need the events between kernels: run eagerly
+  if (!h->graph_mode || h->prof_mask) return microbatch_eager(h, B, T, loss_scale);
+  for (const auto& g : h->graphs) {
+    if (g.B != B || g.T != T || g.scale != loss_scale) continue;
+    CK(cudaGraphLaunch(g.exec, h->stream));
+    count_launches((int)g.launches);
+    // host-side state the recorded forward and backward leave behind
+    h->have_targets = true;
+    h->last_B = B; h->last_T = T; h->last_tokens = h->mb_tok;
+    h->grads_pending = true;
+    return GPT2_OK;
+  }
+  // first call with this shape: run it, then record it for the next calls
+  int rc = microbatch_eager(h, B, T, loss_scale);
+  return rc ? rc : microbatch_capture(h, B, T, loss_scale);
+}
+
+extern "C" int gpt2_set_graph_mode(gpt2_handle h, int enabled) {
+  if (!h) return fail(GPT2_ERR_ARG, "null handle");
+  h->graph_mode = enabled != 0;
+  if (!h->graph_mode) {
+    for (auto& g : h->graphs) cudaGraphExecDestroy(g.exec);
+    h->graphs.clear();
+  }
   return GPT2_OK;
 }
 

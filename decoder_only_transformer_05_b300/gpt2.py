@@ -57,6 +57,8 @@ SIGNATURES = {
     "gpt2_forward": (_I, [_P, _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(_F)]),
     "gpt2_backward": (_I, [_P, _F]),
     "gpt2_zero_grad": (_I, [_P]),
+    "gpt2_forward_backward": (_I, [_P, _P, _P, ctypes.c_int32, ctypes.c_int32, _F]),
+    "gpt2_set_graph_mode": (_I, [_P, _I]),
     "gpt2_adamw_step": (_I, [_P, _F, _F, _F, _F, _F, _F, ctypes.POINTER(_F)]),
     "gpt2_get_loss": (_I, [_P, ctypes.POINTER(_F)]),
     "gpt2_sync": (_I, [_P]),
@@ -210,6 +212,18 @@ class GPT2:
 
     def backward(self, loss_scale=1.0):
         _check(self.lib.gpt2_backward(self._h, loss_scale))
+
+    def forward_backward(self, tokens, targets, B=None, T=None, loss_scale=1.0):
+        """forward(tokens, targets) then backward(loss_scale); tokens and targets may live on
+        the device or in (pinned) host memory. Replayed as a CUDA graph after the first call
+        of each shape unless set_graph_mode(False)."""
+        if B is None:
+            B, T = tokens.shape
+        _check(self.lib.gpt2_forward_backward(self._h, ptr(tokens), ptr(targets), B, T,
+                                              loss_scale))
+
+    def set_graph_mode(self, enabled):
+        _check(self.lib.gpt2_set_graph_mode(self._h, int(bool(enabled))))
 
     def zero_grad(self):
         _check(self.lib.gpt2_zero_grad(self._h))

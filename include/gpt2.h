@@ -28,7 +28,7 @@
  *   - work is queued on the stream given to gpt2_set_stream (default: the legacy default
  *     stream). Calls never synchronise unless they write a host result (h_loss,
  *     h_grad_norm, gpt2_get_loss, gpt2_copy_region);
- *   - nothing is allocated after gpt2_create;
+ *   - no device memory is allocated after gpt2_create;
  *   - after any error the handle can still be passed to gpt2_destroy.
  */
 #ifndef GPT2_H
@@ -133,6 +133,27 @@ int gpt2_forward(gpt2_handle h, const int32_t* d_tokens, const int32_t* d_target
  * gradients through those calls, not through a pointer obtained before a backward.
  */
 int gpt2_backward(gpt2_handle h, float loss_scale);
+
+/*
+ * One micro-batch: gpt2_forward with targets, then gpt2_backward(loss_scale), with the same
+ * results and the same state afterwards (the loss stays on the device for gpt2_get_loss).
+ * tokens and targets [B, T] int32 may be device or host pointers: they are copied with
+ * cudaMemcpyAsync into library-owned buffers on the handle's stream (pinned host memory
+ * keeps the copy asynchronous). Not in the pages: it is the host-side launch machinery.
+ * Graph mode (the default, gpt2_set_graph_mode): the first call for a given
+ * (B, T, loss_scale) runs eagerly and then records the forward and backward launches into a
+ * CUDA graph on a private stream; later calls with the same triple replay that graph on the
+ * handle's stream. Up to 8 graphs are kept (least recently created dropped first);
+ * instantiating one takes driver resources but no device buffer. While profiling is enabled
+ * (gpt2_profile_enable with a non-zero mask) the call runs eagerly so the events can
+ * bracket each launch. Errors as gpt2_forward / gpt2_backward; a capture or instantiation
+ * failure returns GPT2_ERR_CUDA after the micro-batch itself has run.
+ */
+int gpt2_forward_backward(gpt2_handle h, const int32_t* tokens, const int32_t* targets,
+                          int32_t B, int32_t T, float loss_scale);
+/* Turn graph recording and replay in gpt2_forward_backward on (1) or off (0: every call
+ * runs eagerly; the recorded graphs are destroyed). */
+int gpt2_set_graph_mode(gpt2_handle h, int enabled);
 
 /* Set every gradient (and every pending partial sum) to zero. */
 int gpt2_zero_grad(gpt2_handle h);

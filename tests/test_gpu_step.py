@@ -232,6 +232,60 @@ def test_bf16_deterministic():
     m.close()
 
 
+def test_forward_backward_graph_replay_matches_eager():
+    """gpt2_forward_backward records the micro-batch as a CUDA graph on its first call and
+    replays it afterwards: losses and accumulated gradients equal those of separate
+    forward/backward calls bit for bit, for device and pinned-host token buffers."""
+    m, params, cfg, w = make("char-bf16", B=8)
+    batches = [tokens_for(w, 8, index=i) for i in range(4)]
+
+    def run(use_fb, graph=True):
+        m.set_params(params)
+        m.set_graph_mode(graph)
+        m.zero_grad()
+        losses = []
+        for i, (tok, tgt, dtok, dtgt) in enumerate(batches):
+            if use_fb:
+                if i % 2:   # pinned host buffers, copied in by the library
+                    ht = torch.from_numpy(np.ascontiguousarray(tok)).pin_memory()
+                    hg = torch.from_numpy(np.ascontiguousarray(tgt)).pin_memory()
+                    m.forward_backward(ht, hg, 8, w["T"], 0.25)
+                else:
+                    m.forward_backward(dtok, dtgt, 8, w["T"], 0.25)
+            else:
+                m.forward(dtok, dtgt)
+                m.backward(0.25)
+            losses.append(m.get_loss())
+        return losses, m.read_region("grads", np.float32)
+
+    l_eager, g_eager = run(False)
+    l_graph, g_graph = run(True)
+    l_off, g_off = run(True, graph=False)
+    assert len(set(l_eager)) == len(l_eager)     # the batches differ
+    assert l_graph == l_eager and l_off == l_eager
+    assert np.array_equal(g_graph, g_eager) and np.array_equal(g_off, g_eager)
+    # profiling forces the eager path (events between launches); results unchanged
+    m.set_graph_mode(True)
+    m.profile_enable(("gemm",), capacity=4096)
+    l_prof, g_prof = run(True)
+    n, ms, flops = m.profile_read("gemm", reset=True)
+    m.profile_enable((), capacity=0)
+    assert n > 0 and l_prof == l_eager and np.array_equal(g_prof, g_eager)
+    m.close()
+
+
+def test_forward_backward_rejects_bad_shapes():
+    m, params, cfg, w = make("char-bf16", B=8)
+    tok, tgt, dtok, dtgt = tokens_for(w, 8)
+    with pytest.raises(G.GPT2Error):
+        m.forward_backward(dtok, dtgt, 9, w["T"], 1.0)        # B > batch_size
+    with pytest.raises(G.GPT2Error):
+        m.forward_backward(dtok, dtgt, 8, w["T"] + 4, 1.0)    # T > block_size
+    with pytest.raises(G.GPT2Error):
+        m.forward_backward(dtok, dtgt, 8, w["T"] - 2, 1.0)    # bf16 backward: T % 4
+    m.close()
+
+
 def test_bf16_zero_logits_give_ln_vocab():
     """lnf gamma = beta = 0 makes every logit exactly 0: the loss is ln V over the real
     vocabulary (the padded columns are masked)."""
