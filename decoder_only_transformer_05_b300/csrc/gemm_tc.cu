@@ -6,9 +6,14 @@
 // (m or n contiguous). Forward GEMMs are K-major x K-major, dgrad GEMMs K-major x
 // MN-major, wgrad GEMMs MN-major x MN-major.
 //
-// Structure (one persistent block of 320 threads per SM):
+// Structure (one persistent block of 320 threads per SM, blocks paired in clusters of 2):
 //   warp 0      TMA producer: 128x64 A and BNx64 B tiles, 128-byte swizzle, into a
-//               ring of shared-memory stages (mbarrier full/empty handshake)
+//               ring of shared-memory stages (mbarrier full/empty handshake). The two
+//               blocks of a cluster work on vertically adjacent tiles (same columns), so
+//               they need the same B tile: each loads one half of it and multicasts it
+//               into both blocks' shared memory, which cuts the L2-to-SM operand traffic
+//               by a third. A stage is free once both blocks' MMAs have read it (each
+//               MMA completion arrives on the empty barrier of both blocks).
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN, K=16) into a
 //               fp32 accumulator in tensor memory; two accumulators alternate so the
 //               epilogue of one tile overlaps the main loop of the next
@@ -21,6 +26,7 @@
 // issuing work, waits for its own copies and MMAs and frees its tensor memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -37,11 +43,11 @@ constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int STG_BYTES = 4096;   // per epilogue warp: 32 rows x 128 B
 
 template <int BN> struct Cfg {
-  static constexpr int A_BYTES = BM * BK * 2;   // 16 KB
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int A_BYTES = BM * BK * 2;         // 16 KB: this block's 128 rows of A
+  static constexpr int B_BYTES = (BN / 2) * BK * 2;   // this block's half of the B tile
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
-  static constexpr int TMEM_COLS = 2 * BN;      // two accumulators
+  static constexpr int STAGES = BN == 256 ? 6 : 8;    // 192 KB of operands in flight
+  static constexpr int TMEM_COLS = 2 * BN;            // two accumulators
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM = STAGES * STAGE + EPI_WARPS * STG_BYTES + 1024 + BAR_BYTES;
 };
@@ -144,7 +150,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ EpiMaps maps, const Params p) {
   using Cf = Cfg<BN>;
-  constexpr uint32_t IDESC = make_idesc(BM, BN, AMN, BMN);
+  // the pair MMA: M = 256 (128 rows per block), N = BN
+  constexpr uint32_t IDESC = make_idesc(2 * BM, BN, AMN, BMN);
+  constexpr uint16_t PAIR = 0x3;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -152,7 +160,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   const uint32_t staging = base + Cf::STAGES * Cf::STAGE;
   const uint32_t bars = staging + EPI_WARPS * STG_BYTES;
   uint8_t* bars_ptr = base_ptr + Cf::STAGES * Cf::STAGE + EPI_WARPS * STG_BYTES;
-  // barrier layout: full[S] empty[S] tfull[2] tempty[2] final, then tmem slot, abort flag
+  // barrier layout (the same in both blocks): full[S] empty[S] tfull[2] tempty[2] final,
+  // then the tmem slot and the abort flag. full, tempty and final are used in the even
+  // (MMA-issuing) block only.
   auto full = [&](int s) { return bars + 8u * s; };
   auto empty = [&](int s) { return bars + 8u * (Cf::STAGES + s); };
   auto tfull = [&](int a) { return bars + 8u * (2 * Cf::STAGES + a); };
@@ -163,74 +173,84 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   volatile int* abort_flag = (volatile int*)(bars_ptr + 8 * (2 * Cf::STAGES + 6));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cf::STAGES; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), EPI_WARPS); }
+    for (int a = 0; a < 2; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), 2 * EPI_WARPS); }
     mbar_init(final_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) {
-    tmem_alloc(slot, Cf::TMEM_COLS);
-    tmem_relinquish();
+  if (warp == 1) {   // one warp of each block, collectively
+    tmem_alloc_pair(slot, Cf::TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();   // both blocks' barriers and tensor memory exist before either is used
   tc_fence_after();
   const uint32_t tmem_base = *slot_ptr;
 
-  const int tiles = p.num_m * p.num_n * p.splits;
-  auto decode = [&](int tile, int& mb, int& nb, int& sp) {
-    mb = tile % p.num_m;
-    int r = tile / p.num_m;
+  // work unit = a pair of vertically adjacent 128 x BN tiles; this block takes row tile
+  // 2 mp + rank (past the last row tile when num_m is odd: its loads read zeros and
+  // nothing is stored)
+  const int num_mp = (p.num_m + 1) / 2;
+  const int units = num_mp * p.num_n * p.splits;
+  const int first = blockIdx.x >> 1, stride = gridDim.x >> 1;
+  auto decode = [&](int unit, int& mb, int& nb, int& sp) {
+    mb = 2 * (unit % num_mp) + (int)rank;
+    int r = unit / num_mp;
     nb = r % p.num_n;
     sp = r / p.num_n;
   };
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer (both blocks): this block's rows of A and its half
+      // of the B columns, completing on the even block's full barrier
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      for (int unit = first; unit < units && ok; unit += stride) {
         int mb, nb, sp;
-        decode(tile, mb, nb, sp);
-        const int m0 = mb * BM, n0 = nb * BN;
+        decode(unit, mb, nb, sp);
+        const int m0 = mb * BM, n0 = nb * BN + (int)rank * (BN / 2);
         const int kb0 = sp * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % Cf::STAGES;
           const uint32_t ph = (uint32_t)(it / Cf::STAGES) & 1u;
           if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, p.err)) { ok = false; break; }
           const uint32_t a_dst = base + s * Cf::STAGE, b_dst = a_dst + Cf::A_BYTES;
-          mbar_expect_tx(full(s), Cf::STAGE);
+          if (leader) mbar_expect_tx(full(s), 2 * Cf::STAGE);   // both blocks' bytes
+          const uint32_t fb = mapa_shared(full(s), 0);
           if (AMN) {
-            tma_load_2d(a_dst, &tmA, full(s), m0, kb * BK);
-            tma_load_2d(a_dst + 8192, &tmA, full(s), m0 + 64, kb * BK);
+            tma_load_2d_pair(a_dst, &tmA, fb, m0, kb * BK);
+            tma_load_2d_pair(a_dst + 8192, &tmA, fb, m0 + 64, kb * BK);
           } else {
-            tma_load_2d(a_dst, &tmA, full(s), kb * BK, m0);
+            tma_load_2d_pair(a_dst, &tmA, fb, kb * BK, m0);
           }
           if (BMN) {
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i) tma_load_2d(b_dst + i * 8192, &tmB, full(s), n0 + i * 64, kb * BK);
+            for (int i = 0; i < BN / 128; ++i)
+              tma_load_2d_pair(b_dst + i * 8192, &tmB, fb, n0 + i * 64, kb * BK);
           } else {
-            tma_load_2d(b_dst, &tmB, full(s), kb * BK, n0);
+            tma_load_2d_pair(b_dst, &tmB, fb, kb * BK, n0);
           }
         }
       }
-      if (!ok) {
+      if (!ok && leader) {
         // let the copies already issued land before the block exits
         for (int j = max(0, it - Cf::STAGES); j < it; ++j)
           mbar_wait(full(j % Cf::STAGES), (uint32_t)(j / Cf::STAGES) & 1u, abort_flag, nullptr, false);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (even block): M = 256 MMAs over both blocks' stages
       int it = 0, tcount = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++tcount) {
+      for (int unit = first; unit < units && ok; unit += stride, ++tcount) {
         int mb, nb, sp;
-        decode(tile, mb, nb, sp);
+        decode(unit, mb, nb, sp);
         const int kb0 = sp * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         const int acc = tcount & 1;
         const uint32_t aph = (uint32_t)(tcount >> 1) & 1u;
@@ -249,29 +269,29 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                                     : sdesc(a_base + k * 32, 16, 1024);
             const uint64_t bd = BMN ? sdesc(b_base + k * 2048, 8192, 1024)
                                     : sdesc(b_base + k * 32, 16, 1024);
-            umma_bf16(d, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+            umma_bf16_pair(d, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
           }
-          umma_commit(empty(s));
+          umma_commit_pair_mc(empty(s), PAIR);   // the stage is free in both blocks
         }
         if (!ok) break;
-        umma_commit(tfull(acc));
+        umma_commit_pair_mc(tfull(acc), PAIR);   // both blocks' accumulators are ready
       }
       // all issued MMAs complete before tensor memory is released
-      umma_commit(final_bar);
+      umma_commit_pair(final_bar);
       mbar_wait(final_bar, 0, abort_flag, nullptr, false);
     }
   } else {
-    // ---------------- epilogue warps 2..9; warp % 4 selects the TMEM lane quarter, and
-    // warps w, w + 4 split the tile's 32-column chunks between them (even / odd)
+    // ---------------- epilogue warps 2..9 of both blocks; warp % 4 selects the TMEM lane
+    // quarter, and warps w, w + 4 split the tile's 32-column chunks between them
     const int q = warp & 3, ew = warp - 2, half = ew >> 2;
     const uint32_t stg = staging + ew * STG_BYTES;
     if (p.epi == EPI_GELU_FWD && lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"((unsigned long long)&maps.pre) : "memory");
     }
     int tcount = 0;
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tcount) {
+    for (int unit = first; unit < units; unit += stride, ++tcount) {
       int mb, nb, sp;
-      decode(tile, mb, nb, sp);
+      decode(unit, mb, nb, sp);
       const int acc = tcount & 1;
       const uint32_t aph = (uint32_t)(tcount >> 1) & 1u;
       bool ok = mbar_wait(tfull(acc), aph, abort_flag, p.err);
@@ -288,16 +308,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty(acc));
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty(acc), 0));
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
-  __syncthreads();
+  // neither block leaves (or frees tensor memory) while the pair's MMAs, copies or
+  // arrivals may still reach it
+  cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, Cf::TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, Cf::TMEM_COLS);
   }
 }
 
@@ -359,7 +381,7 @@ static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
   bool ok = AMN ? make_map_bf16(&ma, g.A, g.M, g.K, g.lda, 64, 64)
                 : make_map_bf16(&ma, g.A, g.K, g.M, g.lda, 64, BM);
   ok = ok && (BMN ? make_map_bf16(&mb, g.B, g.N, g.K, g.ldb, 64, 64)
-                  : make_map_bf16(&mb, g.B, g.K, g.N, g.ldb, 64, BN));
+                  : make_map_bf16(&mb, g.B, g.K, g.N, g.ldb, 64, BN / 2));
   if (!ok) return cudaErrorInvalidValue;
   Params p;
   p.M = g.M; p.N = g.N; p.K = g.K;
@@ -398,10 +420,29 @@ static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
                                   CU_TENSOR_MAP_SWIZZLE_64B);
   }
   if (!ok) return cudaErrorInvalidValue;
-  const int tiles = p.num_m * p.num_n * p.splits;
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  gemm_kernel<BN, AMN, BMN><<<grid, THREADS, Cf::SMEM, s>>>(ma, mb, maps, p); count_launches(1);
-  cudaError_t e = cudaGetLastError();
+  // clusters of two blocks; as many as can be resident at once (persistent)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = Cf::SMEM;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_clusters = 0;
+  if (!max_clusters) {
+    cfg.gridDim = dim3(2 * (num_sms / 2));
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, gemm_kernel<BN, AMN, BMN>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (max_clusters <= 0) return cudaErrorInvalidConfiguration;
+  }
+  const int units = ceil_div(p.num_m, 2) * p.num_n * p.splits;
+  cfg.gridDim = dim3(2 * std::min(units, max_clusters));
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel<BN, AMN, BMN>, ma, mb, maps, p);
+  count_launches(1);
   if (e != cudaSuccess) return e;
   if (p.splits > 1 && !p.defer)
     return splitk_reduce(g.accum, g.workspace, p.splits, (long long)g.M * g.N, g.scale, s);
