@@ -74,13 +74,6 @@ __device__ __forceinline__ void stage_row32(uint32_t slice, int r, const float* 
                            pack2_bf16(v[8 * u + 4] * sc, v[8 * u + 5] * sc),
                            pack2_bf16(v[8 * u + 6] * sc, v[8 * u + 7] * sc)));
 }
-// 32 packed pairs (64 columns) of row r into one 64-column half
-__device__ __forceinline__ void store_operand_row64(uint32_t half_tile, int r, const uint32_t* pk) {
-#pragma unroll
-  for (int u = 0; u < 8; ++u)
-    st_shared16(half_tile + r * 128 + ((u ^ (r & 7)) << 4),
-                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
-}
 
 struct Params {
   int B, T, H, C, nqb, units;
@@ -470,26 +463,25 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
 
 // =====================================================================================
 // backward: dK, dV
-constexpr int K_QD_STAGES = 2;
+constexpr int K_QD_STAGES = 4;
 constexpr int K_SM_KV = 0;                                  // [2 units]: K, V
 constexpr int K_SM_QD = K_SM_KV + 4 * TILE;                 // stage s: Q at 2s, dO at 2s+1
-constexpr int K_SM_PT = K_SM_QD + 2 * K_QD_STAGES * TILE;   // P^T (two 64-query halves)
-constexpr int K_SM_DST = K_SM_PT + 2 * TILE;                // dS^T
-constexpr int K_SM_LD = K_SM_DST + 2 * TILE;                // stage s: lse[128], D[128]
+constexpr int K_SM_STG = K_SM_QD + 2 * K_QD_STAGES * TILE;  // 8 warps x 2 KB output staging
+constexpr int K_SM_LD = K_SM_STG + TILE;                    // stage s: lse[128], D[128]
 constexpr int K_SM_BAR = K_SM_LD + K_QD_STAGES * 1024;
 constexpr int K_SMEM = K_SM_BAR + 256 + 1024;
 enum {
   KB_KVFULL = 0,    // [2]
   KB_KVEMPTY = 2,   // [2]
-  KB_QDFULL = 4,    // [2]
-  KB_QDEMPTY = 6,   // [2]
-  KB_SFULL = 8,
-  KB_SEMPTY = 9,
-  KB_PFULL = 10,
-  KB_DONE = 11,
-  KB_ACCFREE = 12,
-  KB_FINAL = 13,
-  KB_COUNT = 14
+  KB_QDFULL = 4,    // [K_QD_STAGES]
+  KB_QDEMPTY = 4 + K_QD_STAGES,
+  KB_SFULL = 4 + 2 * K_QD_STAGES,
+  KB_SEMPTY,
+  KB_PFULL,
+  KB_DONE,
+  KB_ACCFREE,
+  KB_FINAL,
+  KB_COUNT
 };
 
 __device__ __forceinline__ void dkv_unit(const Params& p, int u, int& b, int& h, int& kb, int& n) {
@@ -519,6 +511,8 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(KB_KVFULL + i), 1);
       mbar_init(bar(KB_KVEMPTY + i), 1);
+    }
+    for (int i = 0; i < K_QD_STAGES; ++i) {
       mbar_init(bar(KB_QDFULL + i), 1);
       mbar_init(bar(KB_QDEMPTY + i), 1);
     }
@@ -539,7 +533,10 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot_ptr;
-  constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 320;
+  // S^T, dP^T fp32; the dV, dK accumulators; P^T, dS^T as bf16 pairs (the A operands of
+  // the dV, dK MMAs, read from tensor memory)
+  constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 320, COL_PT = 384,
+                     COL_DST = 448;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -631,11 +628,10 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
             const uint32_t qa = base + K_SM_QD + 2 * s * TILE, da = qa + TILE;
 #pragma unroll
             for (int k = 0; k < BQ / 16; ++k) {
-              const uint32_t off = (k >> 2) * TILE + (k & 3) * 32;
-              umma_bf16(tmem + COL_DV, sdesc(base + K_SM_PT + off, 16, 1024),
-                        sdesc(da + k * 2048, 16384, 1024), IDESC_G, (ib > 0 || k > 0) ? 1u : 0u);
-              umma_bf16(tmem + COL_DK, sdesc(base + K_SM_DST + off, 16, 1024),
-                        sdesc(qa + k * 2048, 16384, 1024), IDESC_G, (ib > 0 || k > 0) ? 1u : 0u);
+              umma_bf16_ts(tmem + COL_DV, tmem + COL_PT + k * 8, sdesc(da + k * 2048, 16384, 1024),
+                           IDESC_G, (ib > 0 || k > 0) ? 1u : 0u);
+              umma_bf16_ts(tmem + COL_DK, tmem + COL_DST + k * 8, sdesc(qa + k * 2048, 16384, 1024),
+                           IDESC_G, (ib > 0 || k > 0) ? 1u : 0u);
             }
             umma_commit(bar(KB_DONE));
             umma_commit(bar(KB_QDEMPTY + s));
@@ -654,9 +650,8 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
     const int q = warp & 3, half = (warp - 2) >> 2;
     const int r = q * 32 + lane, c0 = half * 64;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    // this warp's 32 rows of its P^T / dS^T half: the staging slices for dK / dV
-    const uint32_t slice_k = base + K_SM_PT + half * TILE + q * 4096;
-    const uint32_t slice_v = base + K_SM_DST + half * TILE + q * 4096;
+    // this warp's output staging slice (32 rows x 32 columns bf16), dK then dV
+    const uint32_t slice = base + K_SM_STG + (warp - 2) * 2048;
     const float sl2 = rsqrtf((float)D) * LOG2E;
     int it = 0, g = 0;
     bool ok = true;
@@ -712,24 +707,15 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
             dk[e4 * 2 + 1] = pack2_bf16(ds[2], ds[3]);
           }
           if (c == 0) {
-            // the previous block's dV, dK MMAs have read P^T, dS^T (for the first block of a
-            // unit, the previous unit's last block; the slices may also still be the source
-            // of that unit's output stores)
+            // the previous block's dV, dK MMAs have read P^T, dS^T from tensor memory (for
+            // the first block of a unit, the previous unit's last block)
             if (g >= 1) {
               const bool w_ok = mbar_wait(bar(KB_DONE), par(g - 1), abort_flag, p.err);
               if (!__all_sync(0xffffffffu, w_ok)) return false;
             }
-            if (i == 0) {
-              if (lane == 0) bulk_wait_read();
-              __syncwarp();
-            }
           }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t off = half * TILE + r * 128 + (((c * 4 + u) ^ (r & 7)) << 4);
-            st_shared16(base + K_SM_PT + off, make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
-            st_shared16(base + K_SM_DST + off, make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]));
-          }
+          tmem_st16(lane_base + COL_PT + half * 32 + c * 16, pk);
+          tmem_st16(lane_base + COL_DST + half * 32 + c * 16, dk);
           return true;
         };
         if (i == 0 || q0 + 64 > p.T) {
@@ -738,7 +724,7 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
           ok = chunk(0, std::false_type{}) && chunk(1, std::false_type{});
         }
         if (!ok) break;
-        fence_proxy_async();
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(KB_PFULL));
@@ -754,15 +740,20 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(KB_ACCFREE));
-      stage_row32(slice_k, lane, reinterpret_cast<const float*>(kv2[0]), rsqrtf((float)D));
-      stage_row32(slice_v, lane, reinterpret_cast<const float*>(kv2[1]), 1.0f);
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) {
-        const int row = kb * BKV + q * 32;
-        tma_store_3d(&tm_dqkv, slice_k, p.C + h * D + half * 32, row, b);
-        tma_store_3d(&tm_dqkv, slice_v, 2 * p.C + h * D + half * 32, row, b);
-        bulk_commit();
+      // dK, then dV, through the warp's 2 KB slice (free once the previous store read it)
+      const int row = kb * BKV + q * 32;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+        stage_row32(slice, lane, reinterpret_cast<const float*>(kv2[t]),
+                    t == 0 ? rsqrtf((float)D) : 1.0f);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tm_dqkv, slice, (t == 0 ? p.C : 2 * p.C) + h * D + half * 32, row, b);
+          bulk_commit();
+        }
       }
     }
     if (lane == 0) bulk_wait_all();
@@ -779,24 +770,24 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
 
 // =====================================================================================
 // backward: dQ
-constexpr int Q_KV_STAGES = 3;
+constexpr int Q_KV_STAGES = 4;
 constexpr int Q_SM_QD = 0;                                   // [2 units]: Q, dO
 constexpr int Q_SM_KV = Q_SM_QD + 4 * TILE;                  // stage s: K at 2s, V at 2s+1
-constexpr int Q_SM_DS = Q_SM_KV + 2 * Q_KV_STAGES * TILE;    // dS (two 64-key halves)
-constexpr int Q_SM_BAR = Q_SM_DS + 2 * TILE;
+constexpr int Q_SM_STG = Q_SM_KV + 2 * Q_KV_STAGES * TILE;   // 8 warps x 2 KB output staging
+constexpr int Q_SM_BAR = Q_SM_STG + TILE;
 constexpr int Q_SMEM = Q_SM_BAR + 256 + 1024;
 enum {
   QB_QFULL = 0,     // [2]
   QB_QEMPTY = 2,    // [2]
-  QB_KVFULL = 4,    // [3]
-  QB_KVEMPTY = 7,   // [3]
-  QB_SFULL = 10,
-  QB_SEMPTY = 11,
-  QB_PFULL = 12,
-  QB_DONE = 13,
-  QB_ACCFREE = 14,
-  QB_FINAL = 15,
-  QB_COUNT = 16
+  QB_KVFULL = 4,    // [Q_KV_STAGES]
+  QB_KVEMPTY = 4 + Q_KV_STAGES,
+  QB_SFULL = 4 + 2 * Q_KV_STAGES,
+  QB_SEMPTY,
+  QB_PFULL,
+  QB_DONE,          // [2]: one per dS buffer
+  QB_ACCFREE = QB_DONE + 2,
+  QB_FINAL,
+  QB_COUNT
 };
 
 __device__ __forceinline__ void dq_unit(const Params& p, int u, int& b, int& h, int& qb, int& n) {
@@ -831,6 +822,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
     mbar_init(bar(QB_SEMPTY), 8);
     mbar_init(bar(QB_PFULL), 8);
     mbar_init(bar(QB_DONE), 1);
+    mbar_init(bar(QB_DONE + 1), 1);
     mbar_init(bar(QB_ACCFREE), 8);
     mbar_init(bar(QB_FINAL), 1);
     *abort_flag = 0;
@@ -844,7 +836,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot_ptr;
-  constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256;
+  // S, dP fp32; the dQ accumulator; dS as bf16 pairs, double-buffered (the A operand of the
+  // dQ MMA, read from tensor memory)
+  constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256, COL_DS = 320;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -925,11 +919,12 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
             }
             tc_fence_after();
             const uint32_t ka = base + Q_SM_KV + 2 * s * TILE;
+            const uint32_t ds = tmem + COL_DS + (uint32_t)(gp & 1) * 64;
 #pragma unroll
             for (int k = 0; k < BKV / 16; ++k)
-              umma_bf16(tmem + COL_DQ, sdesc(base + Q_SM_DS + (k >> 2) * TILE + (k & 3) * 32, 16, 1024),
-                        sdesc(ka + k * 2048, 16384, 1024), IDESC_G, (jb > 0 || k > 0) ? 1u : 0u);
-            umma_commit(bar(QB_DONE));
+              umma_bf16_ts(tmem + COL_DQ, ds + k * 8, sdesc(ka + k * 2048, 16384, 1024), IDESC_G,
+                           (jb > 0 || k > 0) ? 1u : 0u);
+            umma_commit(bar(QB_DONE + (gp & 1)));
             umma_commit(bar(QB_KVEMPTY + s));
             ++gp;
           }
@@ -946,7 +941,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
     const int q = warp & 3, half = (warp - 2) >> 2;
     const int r = q * 32 + lane, c0 = half * 64;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    const uint32_t slice = base + Q_SM_DS + half * TILE + q * 4096;
+    const uint32_t slice = base + Q_SM_STG + (warp - 2) * 2048;   // output staging
     const float sl2 = rsqrtf((float)D) * LOG2E;
     int g = 0;
     bool ok = true;
@@ -994,22 +989,26 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
         };
         if (j == qb) compute(std::true_type{});
         else compute(std::false_type{});
-        if (g >= 1) {
-          ok = mbar_wait(bar(QB_DONE), par(g - 1), abort_flag, p.err);
+        // dS buffer g & 1 was last read by the dQ MMAs of block g - 2
+        if (g >= 2) {
+          ok = mbar_wait(bar(QB_DONE + (g & 1)), par((g >> 1) - 1), abort_flag, p.err);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         }
-        if (j == 0) {
-          if (lane == 0) bulk_wait_read();
-          __syncwarp();
+        {
+          const uint32_t dst = lane_base + COL_DS + (uint32_t)(g & 1) * 64 + half * 32;
+          uint32_t lo[16], hi[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) { lo[e] = dk[e]; hi[e] = dk[16 + e]; }
+          tmem_st16(dst, lo);
+          tmem_st16(dst + 16, hi);
         }
-        store_operand_row64(base + Q_SM_DS + half * TILE, r, dk);
-        fence_proxy_async();
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(QB_PFULL));
       }
       if (!ok) break;
-      ok = mbar_wait(bar(QB_DONE), par(g - 1), abort_flag, p.err);
+      ok = mbar_wait(bar(QB_DONE + ((g - 1) & 1)), par((g - 1) >> 1), abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       uint32_t v[32];
@@ -1018,6 +1017,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(QB_ACCFREE));
+      if (lane == 0) bulk_wait_read();   // the slice's previous store has read it
+      __syncwarp();
       stage_row32(slice, lane, reinterpret_cast<const float*>(v), rsqrtf((float)D));
       fence_proxy_async();
       __syncwarp();
