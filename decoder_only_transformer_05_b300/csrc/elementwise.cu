@@ -459,16 +459,24 @@ cudaError_t splitk_reduce(float* accum, const float* ws, int splits, long long n
 }
 
 // accum += sum_k ws[k] in k order, then ws = 0
+// (all of a thread's loads are issued before its first store, so they overlap)
+template <int S>
 __global__ void splitk_fold_kernel(float* __restrict__ accum, float* __restrict__ ws, int splits,
                                    long long n4, long long n) {
   long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n4) return;
   float4 a = reinterpret_cast<float4*>(accum)[i];
-  for (int k = 0; k < splits; ++k) {
-    float4* wp = reinterpret_cast<float4*>(ws + (size_t)k * n) + i;
-    const float4 w = *wp;
-    a.x += w.x; a.y += w.y; a.z += w.z; a.w += w.w;
-    *wp = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < splits; k0 += S) {
+    float4 w[S];
+#pragma unroll
+    for (int k = 0; k < S; ++k)
+      if (k0 + k < splits) w[k] = __ldcs(reinterpret_cast<const float4*>(ws + (size_t)(k0 + k) * n) + i);
+#pragma unroll
+    for (int k = 0; k < S; ++k)
+      if (k0 + k < splits) {
+        a.x += w[k].x; a.y += w[k].y; a.z += w[k].z; a.w += w[k].w;
+        __stcs(reinterpret_cast<float4*>(ws + (size_t)(k0 + k) * n) + i, make_float4(0.f, 0.f, 0.f, 0.f));
+      }
   }
   reinterpret_cast<float4*>(accum)[i] = a;
 }
@@ -476,7 +484,7 @@ __global__ void splitk_fold_kernel(float* __restrict__ accum, float* __restrict_
 cudaError_t splitk_fold(float* accum, float* ws, int splits, long long n, cudaStream_t s) {
   if (n % 4) return cudaErrorInvalidValue;
   long long n4 = n / 4;
-  splitk_fold_kernel<<<ceil_div(n4, 256), 256, 0, s>>>(accum, ws, splits, n4, n); count_launches(1);
+  splitk_fold_kernel<8><<<ceil_div(n4, 256), 256, 0, s>>>(accum, ws, splits, n4, n); count_launches(1);
   return last();
 }
 

@@ -56,6 +56,8 @@ struct Params {
   int M, N, K;
   int num_m, num_n, splits, kb_per_split, num_kb;
   int epi;
+  int n_fast;     // unit order: column tile fastest (few column tiles: the tiles that share
+                  // a row block of A run at the same time, so A streams from DRAM once)
   int defer;      // split partials: 0 = summed into accum after the kernel, 1 = added into
                   // the workspace, which the caller folds in later
   long long ldo;
@@ -198,10 +200,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   const int units = num_mp * p.num_n * p.splits;
   const int first = blockIdx.x >> 1, stride = gridDim.x >> 1;
   auto decode = [&](int unit, int& mb, int& nb, int& sp) {
-    mb = 2 * (unit % num_mp) + (int)rank;
-    int r = unit / num_mp;
-    nb = r % p.num_n;
-    sp = r / p.num_n;
+    int r;
+    if (p.n_fast) {
+      nb = unit % p.num_n;
+      r = unit / p.num_n;
+      mb = 2 * (r % num_mp) + (int)rank;
+      sp = r / num_mp;
+    } else {
+      mb = 2 * (unit % num_mp) + (int)rank;
+      r = unit / num_mp;
+      nb = r % p.num_n;
+      sp = r / p.num_n;
+    }
   };
 
   if (warp == 0) {
@@ -390,6 +400,7 @@ static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
   p.num_kb = g.K / BK;
   p.splits = (g.epi == EPI_ACCUM && g.splits > 1) ? g.splits : 1;
   p.kb_per_split = ceil_div(p.num_kb, p.splits);
+  p.n_fast = p.num_n <= 4;
   p.splits = ceil_div(p.num_kb, p.kb_per_split);
   p.epi = g.epi;
   p.defer = g.defer_partials;

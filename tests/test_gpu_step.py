@@ -203,6 +203,12 @@ def test_bf16_gpt2_124m_one_sequence():
     bf16_step_check("gpt2-124m-micro", B=1)
 
 
+def test_bf16_gpt2_350m_shape_one_sequence():
+    """The 350M shape (L = 24, H = 16, C = 1024, T = 1024) on one sequence against the
+    oracle: loss and every gradient tensor."""
+    bf16_step_check("gpt2-350m-shape", B=1)
+
+
 def test_bf16_gpt2_124m_full_batch_sampled_rows():
     """At the full micro-batch (B = 12, as timed by the benchmark), per-position losses of
     sampled rows against the oracle run on those rows alone."""
