@@ -12,8 +12,8 @@
 //
 // Two implementations:
 //  * fp32: one warp per (batch, head, row), plain FMA (parity path).
-//  * bf16, head size 64: flash-attention tiles of 64 queries x 64 keys on mma.sync
-//    tensor-core instructions, online softmax in registers.
+//  * bf16, head size 64: the tcgen05 flash-attention kernels of attention_tc.cu; this file
+//    keeps the D = rowsum(dO * O) kernel they read.
 #include "common.cuh"
 #include "launch.h"
 
@@ -143,139 +143,23 @@ __global__ void attn_bwd_dkv_f32_kernel(float* __restrict__ dqkv, const float* _
 }
 
 // =====================================================================================
-// bf16 flash path, head size 64, tiles of 64 rows; 4 warps per block, 16 rows per warp.
+// bf16 path, head size 64: D for the tensor-core backward (attention_tc.cu)
 namespace fa {
 
 constexpr int D = 64;
-constexpr int BR = 64;             // rows per tile
-constexpr int THREADS = 128;
-constexpr int TILE_BYTES = BR * D * 2;   // 8 KB, 128 B per row
-constexpr float LOG2E = 1.4426950408889634f;
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-// byte offset of 16-byte chunk `ch` of row `r` in a swizzled 64x64 bf16 tile
-__device__ __forceinline__ uint32_t swz(int r, int ch) {
-  return (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4));
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
-  int sz = pred ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz));
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N> __device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
-// async copy of rows [r0, r0+64) (predicated on r < T) of a row-major bf16 matrix with
-// row stride `ld` elements, columns [col, col+64), into a swizzled tile
-__device__ __forceinline__ void load_tile(uint32_t tile, const bf16* g, int r0, int T, long long ld,
-                                          int col) {
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    int idx = it * THREADS + threadIdx.x;
-    int r = idx >> 3, ch = idx & 7;
-    bool ok = (r0 + r) < T;
-    const bf16* src = g + (size_t)(ok ? r0 + r : 0) * ld + col + ch * 8;
-    cp_async16(tile + swz(r, ch), src, ok);
-  }
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c,
-                                        uint32_t& d) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c,
-                                          uint32_t& d) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// A fragments (16 rows x 64 cols, 4 k-steps) of rows [row0, row0+16) of a tile
-__device__ __forceinline__ void load_a_frags(uint32_t tile, int row0, uint32_t (&a)[4][4]) {
-  const int l = threadIdx.x & 31;
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    int r = row0 + (l & 15), ch = kk * 2 + (l >> 4);
-    ldsm_x4(tile + swz(r, ch), a[kk][0], a[kk][1], a[kk][2], a[kk][3]);
-  }
-}
-
-// acc[8][4] (16 x 64) += A (16 x 64, fragments) * X^T where X is a 64x64 tile stored
-// [n][k] (the B operand's n index is the tile row): "non-transposed" B
-__device__ __forceinline__ void mma_abt(float (&acc)[8][4], const uint32_t (&a)[4][4],
-                                        uint32_t tile) {
-  const int l = threadIdx.x & 31;
-#pragma unroll
-  for (int np = 0; np < 4; ++np) {
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      int r = np * 16 + ((l >> 4) << 3) + (l & 7), ch = kk * 2 + ((l >> 3) & 1);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(tile + swz(r, ch), b0, b1, b2, b3);
-      mma16816(acc[2 * np], a[kk], b0, b1);
-      mma16816(acc[2 * np + 1], a[kk], b2, b3);
-    }
-  }
-}
-
-// acc[8][4] (16 x 64) += A (16 x 64 over k = tile rows) * X where X is a 64x64 tile
-// stored [k][n]: "transposed" B
-__device__ __forceinline__ void mma_ab(float (&acc)[8][4], const uint32_t (&a)[4][4],
-                                       uint32_t tile) {
-  const int l = threadIdx.x & 31;
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-    for (int dp = 0; dp < 4; ++dp) {
-      int r = kk * 16 + (((l >> 3) & 1) << 3) + (l & 7), ch = dp * 2 + (l >> 4);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(tile + swz(r, ch), b0, b1, b2, b3);
-      mma16816(acc[2 * dp], a[kk], b0, b1);
-      mma16816(acc[2 * dp + 1], a[kk], b2, b3);
-    }
-  }
-}
-
-// convert a 16x64 fp32 accumulator (C layout) into bf16 A fragments
-__device__ __forceinline__ void acc_to_a(const float (&s)[8][4], uint32_t (&a)[4][4]) {
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    a[kk][0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-    a[kk][1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-    a[kk][2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-    a[kk][3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-  }
-}
-
-__device__ __forceinline__ void zero(float (&a)[8][4]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) a[i][j] = 0.f;
-}
-
-// D_i = dO_i . O_i, one thread per (b, t, h)
+// D_i = dO_i . O_i, one thread per (b, h, t), t fastest: each thread reads one 128-byte row
+// slice of dO and of O, and the writes to D [B, H, T] are contiguous across the warp
 __global__ void bwd_D_kernel(float* __restrict__ Dbuf, const bf16* __restrict__ dout,
                              const bf16* __restrict__ out, int B, int T, int C, int H) {
   long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)B * T * H) return;
-  int h = (int)(i % H);
-  long long bt = i / H;
-  int t = (int)(bt % T), b = (int)(bt / T);
-  const bf16* a = dout + (size_t)bt * C + h * D;
-  const bf16* c = out + (size_t)bt * C + h * D;
+  const int t = (int)(i % T);
+  const long long bh = i / T;
+  const int h = (int)(bh % H), b = (int)(bh / H);
+  const size_t bt = (size_t)b * T + t;
+  const bf16* a = dout + bt * C + h * D;
+  const bf16* c = out + bt * C + h * D;
   float s = 0.f;
 #pragma unroll
   for (int k = 0; k < D; k += 8) {
@@ -283,193 +167,7 @@ __global__ void bwd_D_kernel(float* __restrict__ Dbuf, const bf16* __restrict__ 
 #pragma unroll
     for (int e = 0; e < 8; ++e) s += to_f32(x.e[e]) * to_f32(y.e[e]);
   }
-  Dbuf[((size_t)b * H + h) * T + t] = s;
-}
-
-// dK, dV for one block of 64 keys; loops over the query blocks at or after it.
-__global__ void __launch_bounds__(THREADS)
-bwd_dkv_kernel(bf16* __restrict__ dqkv, const float* __restrict__ Dbuf,
-               const bf16* __restrict__ dout, const bf16* __restrict__ qkv,
-               const float* __restrict__ lse, int T, int C, int H) {
-  extern __shared__ __align__(1024) uint8_t sm[];   // 6 tiles
-  __shared__ float s_lse[2][BR], s_D[2][BR];
-  const uint32_t Ks = smem_u32(sm), Vs = Ks + TILE_BYTES, Qs0 = Ks + 2 * TILE_BYTES,
-                 Os0 = Ks + 4 * TILE_BYTES;
-  const int nb = gridDim.x;
-  const int kb = blockIdx.x;   // key block; q blocks kb..nb-1
-  const int bh = blockIdx.y, b = bh / H, h = bh % H;
-  const long long ld = 3LL * C;
-  const bf16* base = qkv + (size_t)b * T * ld;
-  const bf16* dbase = dout + (size_t)b * T * C;
-  const float* lse_bh = lse + ((size_t)b * H + h) * T;
-  const float* D_bh = Dbuf + ((size_t)b * H + h) * T;
-  const int l = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int g = l >> 2, tq = l & 3;
-  const float sl2 = rsqrtf((float)D) * LOG2E;
-
-  load_tile(Ks, base, kb * BR, T, ld, C + h * D);
-  load_tile(Vs, base, kb * BR, T, ld, 2 * C + h * D);
-  load_tile(Qs0, base, kb * BR, T, ld, h * D);
-  load_tile(Os0, dbase, kb * BR, T, C, h * D);
-  if (threadIdx.x < BR) {
-    int r = kb * BR + threadIdx.x;
-    s_lse[0][threadIdx.x] = r < T ? lse_bh[r] * LOG2E : 0.f;
-    s_D[0][threadIdx.x] = r < T ? D_bh[r] : 0.f;
-  }
-  cp_commit();
-
-  uint32_t ka[4][4], va[4][4];
-  float dk[8][4], dv[8][4];
-  zero(dk);
-  zero(dv);
-  const int key0 = kb * BR + w * 16 + g;   // this thread's keys key0, key0 + 8
-  for (int qb = kb; qb < nb; ++qb) {
-    const int buf = (qb - kb) & 1;
-    if (qb + 1 < nb) {
-      load_tile(Qs0 + (buf ^ 1) * TILE_BYTES, base, (qb + 1) * BR, T, ld, h * D);
-      load_tile(Os0 + (buf ^ 1) * TILE_BYTES, dbase, (qb + 1) * BR, T, C, h * D);
-      if (threadIdx.x < BR) {
-        int r = (qb + 1) * BR + threadIdx.x;
-        s_lse[buf ^ 1][threadIdx.x] = r < T ? lse_bh[r] * LOG2E : 0.f;
-        s_D[buf ^ 1][threadIdx.x] = r < T ? D_bh[r] : 0.f;
-      }
-      cp_commit();
-      cp_wait<1>();
-    } else {
-      cp_wait<0>();
-    }
-    __syncthreads();
-    if (qb == kb) { load_a_frags(Ks, w * 16, ka); load_a_frags(Vs, w * 16, va); }
-    const uint32_t Qs = Qs0 + buf * TILE_BYTES, Os = Os0 + buf * TILE_BYTES;
-    // S^T = K Q^T (rows: keys, cols: queries)
-    float st[8][4];
-    zero(st);
-    mma_abt(st, ka, Qs);
-    // P^T = exp(S^T / sqrt(d) - lse[q]), zero where q < key
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        int qi = nt * 8 + tq * 2 + (e & 1);
-        int q = qb * BR + qi;
-        int key = key0 + (e >> 1) * 8;
-        float p = fast_exp2(st[nt][e] * sl2 - s_lse[buf][qi]);
-        st[nt][e] = (q >= key && q < T) ? p : 0.f;
-      }
-    uint32_t pa[4][4];
-    acc_to_a(st, pa);
-    mma_ab(dv, pa, Os);              // dV += P^T dO
-    float dpt[8][4];
-    zero(dpt);
-    mma_abt(dpt, va, Os);            // dP^T = V dO^T
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        int qi = nt * 8 + tq * 2 + (e & 1);
-        dpt[nt][e] = st[nt][e] * (dpt[nt][e] - s_D[buf][qi]);   // dS^T
-      }
-    uint32_t da[4][4];
-    acc_to_a(dpt, da);
-    mma_ab(dk, da, Qs);              // dK += dS^T Q
-    __syncthreads();
-  }
-  const float scale = rsqrtf((float)D);
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int key = key0 + r * 8;
-    if (key >= T) continue;
-    bf16* dst = dqkv + ((size_t)b * T + key) * ld;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      int d = nt * 8 + tq * 2;
-      *reinterpret_cast<uint32_t*>(dst + C + h * D + d) =
-          pack_bf16(dk[nt][2 * r] * scale, dk[nt][2 * r + 1] * scale);
-      *reinterpret_cast<uint32_t*>(dst + 2 * C + h * D + d) =
-          pack_bf16(dv[nt][2 * r], dv[nt][2 * r + 1]);
-    }
-  }
-}
-
-// dQ for one block of 64 queries; loops over the key blocks up to the diagonal.
-__global__ void __launch_bounds__(THREADS)
-bwd_dq_kernel(bf16* __restrict__ dqkv, const float* __restrict__ Dbuf,
-              const bf16* __restrict__ dout, const bf16* __restrict__ qkv,
-              const float* __restrict__ lse, int T, int C, int H) {
-  extern __shared__ __align__(1024) uint8_t sm[];   // 6 tiles
-  const uint32_t Qs = smem_u32(sm), Os = Qs + TILE_BYTES, Ks0 = Qs + 2 * TILE_BYTES,
-                 Vs0 = Qs + 4 * TILE_BYTES;
-  const int nb = gridDim.x;
-  const int qb = nb - 1 - blockIdx.x;
-  const int bh = blockIdx.y, b = bh / H, h = bh % H;
-  const long long ld = 3LL * C;
-  const bf16* base = qkv + (size_t)b * T * ld;
-  const bf16* dbase = dout + (size_t)b * T * C;
-  const int l = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int g = l >> 2, tq = l & 3;
-  const float sl2 = rsqrtf((float)D) * LOG2E;
-  const int r0 = qb * BR + w * 16 + g;
-  float lse2[2], Dr[2];
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    int row = r0 + r * 8;
-    size_t ri = ((size_t)b * H + h) * T + (row < T ? row : 0);
-    lse2[r] = lse[ri] * LOG2E;
-    Dr[r] = Dbuf[ri];
-  }
-  load_tile(Qs, base, qb * BR, T, ld, h * D);
-  load_tile(Os, dbase, qb * BR, T, C, h * D);
-  load_tile(Ks0, base, 0, T, ld, C + h * D);
-  load_tile(Vs0, base, 0, T, ld, 2 * C + h * D);
-  cp_commit();
-  uint32_t qa[4][4], oa[4][4];
-  float dq[8][4];
-  zero(dq);
-  const int nkv = qb + 1;
-  for (int kb = 0; kb < nkv; ++kb) {
-    const int buf = kb & 1;
-    if (kb + 1 < nkv) {
-      load_tile(Ks0 + (buf ^ 1) * TILE_BYTES, base, (kb + 1) * BR, T, ld, C + h * D);
-      load_tile(Vs0 + (buf ^ 1) * TILE_BYTES, base, (kb + 1) * BR, T, ld, 2 * C + h * D);
-      cp_commit();
-      cp_wait<1>();
-    } else {
-      cp_wait<0>();
-    }
-    __syncthreads();
-    if (kb == 0) { load_a_frags(Qs, w * 16, qa); load_a_frags(Os, w * 16, oa); }
-    const uint32_t Ks = Ks0 + buf * TILE_BYTES, Vs = Vs0 + buf * TILE_BYTES;
-    float s[8][4], dp[8][4];
-    zero(s);
-    zero(dp);
-    mma_abt(s, qa, Ks);      // S = Q K^T
-    mma_abt(dp, oa, Vs);     // dP = dO V^T
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        int key = kb * BR + nt * 8 + tq * 2 + (e & 1);
-        int row = r0 + (e >> 1) * 8;
-        float p = fast_exp2(s[nt][e] * sl2 - lse2[e >> 1]);
-        p = (key <= row) ? p : 0.f;
-        s[nt][e] = p * (dp[nt][e] - Dr[e >> 1]);   // dS
-      }
-    uint32_t da[4][4];
-    acc_to_a(s, da);
-    mma_ab(dq, da, Ks);      // dQ += dS K
-    __syncthreads();
-  }
-  const float scale = rsqrtf((float)D);
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int row = r0 + r * 8;
-    if (row >= T) continue;
-    bf16* dst = dqkv + ((size_t)b * T + row) * ld + h * D;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-      *reinterpret_cast<uint32_t*>(dst + nt * 8 + tq * 2) =
-          pack_bf16(dq[nt][2 * r] * scale, dq[nt][2 * r + 1] * scale);
-  }
+  Dbuf[i] = s;
 }
 
 }  // namespace fa

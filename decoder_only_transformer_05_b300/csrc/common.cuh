@@ -58,6 +58,16 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // ------------------------------------------------------------ exp2 / tanh
 // Hardware base-2 exponential (PTX ex2.approx.ftz.f32), used by the online softmax.
+// Two bf16 packed in one word (the lower-indexed one in the low half) -> fp32 pair, exactly;
+// and an fp32 pair -> two bf16 (round to nearest even) in one word.
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+__device__ __forceinline__ uint32_t pack2_bf16_rn(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -14,6 +14,8 @@
 // Every sum runs in a fixed order: rows are dealt to blocks and warps by a fixed rule,
 // each block's warps are combined in warp order, and the per-block partials are added in
 // block order by column_reduce, so repeated runs give bit-identical results.
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -46,6 +48,63 @@ __global__ void ln_fwd_kernel(T* __restrict__ y, float* __restrict__ mean, float
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
+  if constexpr (std::is_same<T, bf16>::value) {
+    // bf16: pairs of columns as float2 on the packed two-lane fp32 instructions
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * C);
+    float2 v[MAXV][4];
+    float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+      const int c = j * 32 + lane;
+      if (c * 8 < C) {
+        const uint4 a = xr[c];
+        v[j][0] = bf2_to_f2(a.x); v[j][1] = bf2_to_f2(a.y);
+        v[j][2] = bf2_to_f2(a.z); v[j][3] = bf2_to_f2(a.w);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[j][q] = make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) s2 = __fadd2_rn(s2, v[j][q]);
+    }
+    const float mu = warp_sum(s2.x + s2.y) / C;
+    const float2 nmu = make_float2(-mu, -mu);
+    float2 q2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+      if ((j * 32 + lane) * 8 < C) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 d = __fadd2_rn(v[j][q], nmu);
+          q2 = __ffma2_rn(d, d, q2);
+        }
+      }
+    }
+    const float rs = rsqrtf(warp_sum(q2.x + q2.y) / C + 1e-5f);
+    // y = (v - mu) rs w + b = v (rs w) + (b - mu rs w)
+    uint4* yr = reinterpret_cast<uint4*>(y + (size_t)row * C);
+    const float2 rs2 = make_float2(rs, rs);
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+      const int c = j * 32 + lane;
+      if (c * 8 < C) {
+        const uint4 wq = reinterpret_cast<const uint4*>(w)[c];
+        const uint4 bq = reinterpret_cast<const uint4*>(b)[c];
+        const uint32_t ww[4] = {wq.x, wq.y, wq.z, wq.w}, bw[4] = {bq.x, bq.y, bq.z, bq.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 sw = __fmul2_rn(rs2, bf2_to_f2(ww[q]));
+          const float2 sh = __ffma2_rn(nmu, sw, bf2_to_f2(bw[q]));
+          const float2 r = __ffma2_rn(v[j][q], sw, sh);
+          o[q] = pack2_bf16_rn(r.x, r.y);
+        }
+        yr[c] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+    if (lane == 0) { mean[row] = mu; rstd[row] = rs; }
+    return;
+  }
   const T* xr = x + (size_t)row * C;
   float v[MAXV][VE];
   float s = 0.f;
@@ -174,7 +233,9 @@ ln_bwd_kernel(T* __restrict__ dres, int accumulate, float* __restrict__ partials
     cp_commit();   // possibly empty: keeps the group count uniform
   };
 
-  // weights, packed, and the running column sums
+  // weights, packed, and the running column sums (bf16: as fp32 pairs, so that the
+  // arithmetic runs on the packed two-lane fp32 instructions)
+  constexpr bool BF = std::is_same<T, bf16>::value;
   Vec16<T> wv[MAXV];
   float dw[MAXV][VE], db[MAXV][VE], dp[MAXV][VE];
 #pragma unroll
@@ -194,7 +255,72 @@ ln_bwd_kernel(T* __restrict__ dres, int accumulate, float* __restrict__ partials
     issue(ci + (stages - 1) * gridDim.x, (it + stages - 1) % stages);
     cp_wait_dyn(stages - 1);
     __syncthreads();
-    if (row < M) {
+    if (BF && row < M) {
+      // bf16: a 16-byte vector is 4 words of two bf16 (the lower column in the low half); a
+      // bf16 widens to fp32 by a shift or a mask, and pairs of columns run as float2
+      const uint8_t* st = lnb_smem + (it % stages) * stage_bytes + wid * row_bytes;
+      const uint4* sdy = reinterpret_cast<const uint4*>(st);
+      const uint4* sx = reinterpret_cast<const uint4*>(st + tens_bytes);
+      const uint4* sres = reinterpret_cast<const uint4*>(st + 2 * tens_bytes);
+      const float2 rs2 = make_float2(rs, rs), nmr2 = make_float2(-mu * rs, -mu * rs);
+      float2 sg2 = make_float2(0.f, 0.f), sgx2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < MAXV; ++j) {
+        const int v = j * 32 + lane;
+        if (v * 8 < C) {
+          const uint4 a = sdy[v], b = sx[v];
+          const uint4 wq = *reinterpret_cast<const uint4*>(&wv[j]);
+          const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+          const uint32_t ww[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 d = bf2_to_f2(aw[q]);
+            const float2 xh = __ffma2_rn(bf2_to_f2(bw[q]), rs2, nmr2);
+            const float2 g = __fmul2_rn(d, bf2_to_f2(ww[q]));
+            sg2 = __fadd2_rn(sg2, g);
+            sgx2 = __ffma2_rn(g, xh, sgx2);
+            float2 dwv = make_float2(dw[j][2 * q], dw[j][2 * q + 1]);
+            float2 dbv = make_float2(db[j][2 * q], db[j][2 * q + 1]);
+            dwv = __ffma2_rn(d, xh, dwv);
+            dbv = __fadd2_rn(dbv, d);
+            dw[j][2 * q] = dwv.x; dw[j][2 * q + 1] = dwv.y;
+            db[j][2 * q] = dbv.x; db[j][2 * q + 1] = dbv.y;
+          }
+        }
+      }
+      const float sg = warp_sum(sg2.x + sg2.y), sgx = warp_sum(sgx2.x + sgx2.y);
+      // dx = rs (g - mg - xh mgx) = g rs + xh (-rs mgx) + (-rs mg)
+      const float mg = sg / C, mgx = sgx / C;
+      const float2 kx = make_float2(-rs * mgx, -rs * mgx), k0 = make_float2(-rs * mg, -rs * mg);
+      uint4* out = reinterpret_cast<uint4*>(dres + (size_t)row * C);
+#pragma unroll
+      for (int j = 0; j < MAXV; ++j) {
+        const int v = j * 32 + lane;
+        if (v * 8 < C) {
+          const uint4 a = sdy[v], b = sx[v];
+          uint4 r = make_uint4(0u, 0u, 0u, 0u);
+          if (accumulate) r = sres[v];
+          const uint4 wq = *reinterpret_cast<const uint4*>(&wv[j]);
+          const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+          const uint32_t ww[4] = {wq.x, wq.y, wq.z, wq.w}, rw[4] = {r.x, r.y, r.z, r.w};
+          uint32_t ow[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 xh = __ffma2_rn(bf2_to_f2(bw[q]), rs2, nmr2);
+            const float2 g = __fmul2_rn(bf2_to_f2(aw[q]), bf2_to_f2(ww[q]));
+            const float2 dx = __ffma2_rn(xh, kx, __ffma2_rn(g, rs2, k0));
+            const float2 o = __fadd2_rn(bf2_to_f2(rw[q]), dx);
+            ow[q] = pack2_bf16_rn(o.x, o.y);
+            if (DPROJ) {
+              const float2 ob = bf2_to_f2(ow[q]);
+              dp[j][2 * q] += ob.x;
+              dp[j][2 * q + 1] += ob.y;
+            }
+          }
+          out[v] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        }
+      }
+    } else if (!BF && row < M) {
       const uint8_t* st = lnb_smem + (it % stages) * stage_bytes + wid * row_bytes;
       const T* sdy = (const T*)st;
       const T* sx = (const T*)(st + tens_bytes);
