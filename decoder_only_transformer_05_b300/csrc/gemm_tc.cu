@@ -93,41 +93,44 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const EpiMaps& m
     for (int i = 0; i < 4; ++i)
       inp[i] = __ldg(reinterpret_cast<const uint4*>(src + (size_t)row * p.ldo + col0) + i);
   }
-  float v[32];
-  tmem_ld32(taddr, v);
+  // the accumulator as 16 column pairs (packed two-lane fp32 arithmetic below)
+  float2 v[16];
+  tmem_ld32(taddr, reinterpret_cast<float (&)[32]>(v));
   if (p.bias && p.epi != EPI_ACCUM) {
-    const bf16* b = reinterpret_cast<const bf16*>(bia);
+    const uint32_t* b = reinterpret_cast<const uint32_t*>(bia);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) v[e] += __bfloat162float(b[e]);
+    for (int e = 0; e < 16; ++e) v[e] = __fadd2_rn(v[e], bf2_to_f2(b[e]));
   }
   if (lane == 0) bulk_wait_read();
   __syncwarp();
   if (p.epi == EPI_ACCUM) {
-    stage_row_f32(stg, lane, v, (p.splits == 1 || p.defer) ? p.scale : 1.0f);
+    stage_row_f32(stg, lane, reinterpret_cast<const float (&)[32]>(v),
+                  (p.splits == 1 || p.defer) ? p.scale : 1.0f);
   } else {
     uint32_t w[16];
+    const uint32_t* in = reinterpret_cast<const uint32_t*>(inp);
     if (p.epi == EPI_STORE) {
       if (src) {
-        const bf16* r = reinterpret_cast<const bf16*>(inp);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] += __bfloat162float(r[e]);
+        for (int e = 0; e < 16; ++e) v[e] = __fadd2_rn(v[e], bf2_to_f2(in[e]));
       }
 #pragma unroll
-      for (int e = 0; e < 16; ++e) w[e] = pack2_bf16(v[2 * e], v[2 * e + 1]);
+      for (int e = 0; e < 16; ++e) w[e] = pack2_bf16(v[e].x, v[e].y);
     } else if (p.epi == EPI_GELU_FWD) {
       uint32_t u[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        u[e] = pack2_bf16(v[2 * e], v[2 * e + 1]);
-        w[e] = pack2_bf16(gelu_tanh_fast(v[2 * e]), gelu_tanh_fast(v[2 * e + 1]));
+        u[e] = pack2_bf16(v[e].x, v[e].y);
+        const float2 g = gelu_tanh_fast2(v[e]);
+        w[e] = pack2_bf16(g.x, g.y);
       }
       stage_row_bf16(stg + 2048, lane, u);
     } else {   // EPI_GELU_BWD
-      const bf16* a = reinterpret_cast<const bf16*>(inp);
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
-        w[e] = pack2_bf16(v[2 * e] * gelu_tanh_grad_fast(__bfloat162float(a[2 * e])),
-                          v[2 * e + 1] * gelu_tanh_grad_fast(__bfloat162float(a[2 * e + 1])));
+      for (int e = 0; e < 16; ++e) {
+        const float2 g = __fmul2_rn(v[e], gelu_tanh_grad_fast2(bf2_to_f2(in[e])));
+        w[e] = pack2_bf16(g.x, g.y);
+      }
     }
     stage_row_bf16(stg, lane, w);
   }
