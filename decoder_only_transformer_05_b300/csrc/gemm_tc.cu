@@ -400,7 +400,7 @@ static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
   p.M = g.M; p.N = g.N; p.K = g.K;
   p.num_m = ceil_div(g.M, BM);
   p.num_n = ceil_div(g.N, BN);
-  p.num_kb = g.K / BK;
+  p.num_kb = ceil_div(g.K, BK);   // a ragged last k-block reads zeros past K
   p.splits = (g.epi == EPI_ACCUM && g.splits > 1) ? g.splits : 1;
   p.kb_per_split = ceil_div(p.num_kb, p.splits);
   p.n_fast = p.num_n <= 4;
@@ -486,7 +486,7 @@ static int pick_bn(int N) {
 int gemm_tc_pick_splits(int M, int N, int K, int num_sms) {
   const int bn = pick_bn(N);
   const int tiles = ceil_div(M, tc::BM) * ceil_div(N, bn);
-  const int nkb = K / tc::BK;
+  const int nkb = ceil_div(K, tc::BK);
   if (tiles >= num_sms) return 1;
   int s = num_sms / tiles;
   while (s > 1 && nkb / s < 8) --s;
@@ -494,7 +494,9 @@ int gemm_tc_pick_splits(int M, int N, int K, int num_sms) {
 }
 
 cudaError_t gemm_bf16_tc(const GemmArgs& g, cudaStream_t s) {
-  if (g.M <= 0 || g.N <= 0 || g.K <= 0 || g.N % 64 || g.K % 64) return cudaErrorInvalidValue;
+  // N: whole 64-column epilogue chunk pairs. Any K: a K that is not a multiple of 64 ends in
+  // a block that reads zeros past K (the tensor maps check the 16-byte row pitches).
+  if (g.M <= 0 || g.N <= 0 || g.K <= 0 || g.N % 64) return cudaErrorInvalidValue;
   const int sms = gemm_tc_num_sms();
   GemmArgs a = g;
   if (a.epi == EPI_ACCUM && a.splits <= 0) a.splits = gemm_tc_pick_splits(a.M, a.N, a.K, sms);

@@ -49,7 +49,7 @@ struct GemmArgs {
 // fp32 SIMT GEMM (all operands float).
 cudaError_t gemm_f32(const GemmArgs& g, cudaStream_t s);
 // bf16 tcgen05 GEMM (A, B, out, bias, resid, pre, aux bf16; accum fp32).
-// Needs M, N, K > 0, N % 64 == 0, K % 64 == 0, 16-byte aligned pointers and leading
+// Needs M, N, K > 0, N % 64 == 0, 16-byte aligned pointers and leading
 // dimensions that are multiples of 8 elements.
 cudaError_t gemm_bf16_tc(const GemmArgs& g, cudaStream_t s);
 // Largest split-K factor gemm_bf16_tc would choose for an EPI_ACCUM call of this shape.

@@ -30,7 +30,7 @@ enum {
  * dimension ldo (out, pre, aux, resid, accum). This is every Linear layer of the model:
  * forward Y = X W^T (K-major x K-major), dgrad dX = dY W (K-major x MN-major), wgrad
  * dW += dY^T X (MN-major x MN-major). GPT2_BF16 runs the tcgen05 tensor-core kernel and
- * needs N % 64 == 0, K % 64 == 0, 16-byte aligned pointers and leading dimensions that
+ * needs N % 64 == 0 (any K), 16-byte aligned pointers and leading dimensions that
  * are multiples of 8; GPT2_EPI_ACCUM may then split K (splits = 0: automatic, needs
  * `workspace` of splits * M * N floats; 1: no split).
  */

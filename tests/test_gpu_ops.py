@@ -47,7 +47,8 @@ def cosine(a, r):
 
 # ------------------------------------------------------------------------ GEMM
 # (M, N, K): several tiles, ragged M, both BN widths (N % 256 == 0 -> 256, else 128)
-SHAPES = [(256, 384, 192), (200, 256, 128), (384, 768, 256), (130, 128, 64)]
+SHAPES = [(256, 384, 192), (200, 256, 128), (384, 768, 256), (130, 128, 64),
+          (200, 256, 136)]   # ragged K: the last k-block reads zeros past K
 
 
 def gemm_ref(A, B_, a_mn, b_mn):
@@ -109,7 +110,7 @@ def test_gemm_gelu_fwd_and_bwd(prec):
 
 
 @pytest.mark.parametrize("splits", [1, 3, 0])
-@pytest.mark.parametrize("shape", [(384, 256, 1024), (768, 768, 4096)])
+@pytest.mark.parametrize("shape", [(384, 256, 1024), (768, 768, 4096), (384, 256, 300)])
 def test_gemm_wgrad_accumulate_bf16(splits, shape):
     """dW[N, K] += scale * dY^T X with both operands MN-major, split-K partials reduced in
     a fixed order."""
