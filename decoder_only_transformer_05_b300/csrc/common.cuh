@@ -134,4 +134,22 @@ __device__ __forceinline__ float2 gelu_tanh_grad_fast2(float2 x) {
   return __ffma2_rn(a, __ffma2_rn(k3, x2, k0), __ffma2_rn(h, t, h));
 }
 
+// gelu_tanh(x) and, in `grad`, gelu_tanh'(x) from one tanh
+__device__ __forceinline__ float2 gelu_tanh_and_grad_fast2(float2 x, float2& grad) {
+  const float2 k0 = make_float2(0.7978845608028654f, 0.7978845608028654f);
+  const float2 k1 = make_float2(0.044715f * 0.7978845608028654f, 0.044715f * 0.7978845608028654f);
+  const float2 k3 = make_float2(3.0f * 0.044715f * 0.7978845608028654f,
+                                3.0f * 0.044715f * 0.7978845608028654f);
+  const float2 h = make_float2(0.5f, 0.5f), one = make_float2(1.0f, 1.0f);
+  const float2 x2 = __fmul2_rn(x, x);
+  const float2 u = __fmul2_rn(x, __ffma2_rn(k1, x2, k0));
+  const float2 t = make_float2(tanh_approx(u.x), tanh_approx(u.y));
+  const float2 nt = make_float2(-t.x, -t.y);
+  const float2 hx = __fmul2_rn(h, x);
+  // 0.5 (1 + t) + 0.5 x (1 - t^2) (k0 + 3 k1 x^2)
+  grad = __ffma2_rn(__fmul2_rn(hx, __ffma2_rn(nt, t, one)), __ffma2_rn(k3, x2, k0),
+                    __ffma2_rn(h, t, h));
+  return __ffma2_rn(hx, t, hx);
+}
+
 __host__ __device__ inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }

@@ -65,11 +65,11 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(GemmArgs g) {
           break;
         case EPI_GELU_FWD:
           if (g.bias) v += ((const float*)g.bias)[n];
-          ((float*)g.pre)[o] = v;
+          ((float*)g.pre)[o] = gelu_tanh_grad(v);
           ((float*)g.out)[o] = gelu_tanh(v);
           break;
         case EPI_GELU_BWD:
-          ((float*)g.out)[o] = v * gelu_tanh_grad(((const float*)g.aux)[o]);
+          ((float*)g.out)[o] = v * ((const float*)g.aux)[o];
           break;
         case EPI_ACCUM:
           g.accum[o] += g.scale * v;

@@ -681,7 +681,8 @@ extern "C" int gpt2_backward(gpt2_handle h, float loss_scale) {
   CKL(ln_bwd(2 * L, 0, h->x[L], T_LNFW, 0, h->lnf_mean, h->lnf_rstd));
   prof_end(h, pi, (double)M * C * es * 3);
   for (int l = L - 1; l >= 0; --l) {
-    // x[l+1] = xmid + gelu(fch) Wp^T + bp  (bp's gradient came with dres, above)
+    // x[l+1] = xmid + gelu(u) Wp^T + bp with u the fc pre-activation, whose derivative
+    // gelu'(u) the forward kept in fch  (bp's gradient came with dres, above)
     GemmArgs g = linear_dgrad(M, C, 4 * C, h->dres, h->pw(T_FCPROJW, l), h->dfch);
     g.epi = EPI_GELU_BWD;
     g.aux = h->fch[l];

@@ -20,8 +20,8 @@ enum class DType : int { F32 = 0, BF16 = 1 };
 // and one of these epilogues on the fp32 accumulator v = C(m, n):
 enum GemmEpi : int {
   EPI_STORE = 0,     // out = v (+ bias[n]) (+ resid[m, n])
-  EPI_GELU_FWD = 1,  // pre = v + bias[n]; out = gelu_tanh(pre)
-  EPI_GELU_BWD = 2,  // out = v * gelu_tanh'(aux[m, n])
+  EPI_GELU_FWD = 1,  // u = v + bias[n]; out = gelu_tanh(u); pre = gelu_tanh'(u)
+  EPI_GELU_BWD = 2,  // out = v * aux[m, n]  (aux: the pre of EPI_GELU_FWD)
   EPI_ACCUM = 3,     // accum[m, n] += scale * v   (fp32; wgrad into the grad buffer)
 };
 
@@ -33,8 +33,8 @@ struct GemmArgs {
   void* out = nullptr; long long ldo = 0;   // element type = the path's activation type
   const void* bias = nullptr;               // [N], activation type
   const void* resid = nullptr;              // [M, ldo]
-  void* pre = nullptr;                      // EPI_GELU_FWD pre-activation [M, ldo]
-  const void* aux = nullptr;                // EPI_GELU_BWD pre-activation [M, ldo]
+  void* pre = nullptr;                      // EPI_GELU_FWD: gelu'(pre-activation) [M, ldo]
+  const void* aux = nullptr;                // EPI_GELU_BWD: that gelu' [M, ldo]
   float* accum = nullptr;                   // EPI_ACCUM target [M, ldo] fp32
   float scale = 1.0f;
   int splits = 1;                           // EPI_ACCUM split-K count (tensor-core path)

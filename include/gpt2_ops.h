@@ -18,8 +18,8 @@ extern "C" {
 
 enum {
   GPT2_EPI_STORE = 0,    /* out = v (+ bias[n]) (+ resid[m, n]) */
-  GPT2_EPI_GELU_FWD = 1, /* pre = v + bias[n]; out = gelu_tanh(pre) */
-  GPT2_EPI_GELU_BWD = 2, /* out = v * gelu_tanh'(aux[m, n]) */
+  GPT2_EPI_GELU_FWD = 1, /* u = v + bias[n]; out = gelu_tanh(u); pre = gelu_tanh'(u) */
+  GPT2_EPI_GELU_BWD = 2, /* out = v * aux[m, n] (aux: the pre of GPT2_EPI_GELU_FWD) */
   GPT2_EPI_ACCUM = 3     /* accum[m, n] += scale * v (fp32) */
 };
 
