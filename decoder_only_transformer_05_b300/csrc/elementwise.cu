@@ -226,7 +226,33 @@ encoder_segsum_kernel(float* __restrict__ dwte, const T* __restrict__ dx, int C,
   for (int j = 0; j < MAXV; ++j)
 #pragma unroll
     for (int e = 0; e < VE; ++e) acc[j][e] = 0.f;
-  for (int r = r0; r < r1; ++r) {
+  // four rows per step, all loads issued before the adds (the frequent tokens have segments of
+  // hundreds of rows); the adds stay in row order
+  int r = r0;
+  for (; r + 4 <= r1; r += 4) {
+    int pos[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) pos[k] = sc.pos0[r + k];
+    Vec16<T> v[4][MAXV];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int j = 0; j < MAXV; ++j) {
+        const int c = (j * 32 + lane) * VE;
+        if (c < C) v[k][j] = ld16(dx + (size_t)pos[k] * C + c);
+      }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int j = 0; j < MAXV; ++j) {
+        const int c = (j * 32 + lane) * VE;
+        if (c < C) {
+#pragma unroll
+          for (int e = 0; e < VE; ++e) acc[j][e] += to_f32(v[k][j].e[e]);
+        }
+      }
+  }
+  for (; r < r1; ++r) {
     const T* row = dx + (size_t)sc.pos0[r] * C;
 #pragma unroll
     for (int j = 0; j < MAXV; ++j) {
