@@ -73,9 +73,14 @@ cudaError_t encoder_forward(DType t, void* x, const int* tokens, const void* wte
 constexpr int SORT_THREADS = 1024;
 constexpr int SORT_WARPS = SORT_THREADS / 32;
 
+// Segments (runs of one token id in the sorted order) longer than ENC_BIG rows are summed by a
+// wider block of their own (the frequent ids of a skewed stream have hundreds of rows).
+constexpr int ENC_BIG = 64;
+constexpr int ENC_BIG_THREADS = 512;
 struct EncScratch {
-  int* key0; int* pos0; int* key1; int* pos1; int* seg_start; int* nseg;
+  int* key0; int* pos0; int* key1; int* pos1; int* seg_start; int* nseg; int* big;
 };
+static int enc_max_big(int M) { return M / (ENC_BIG + 1) + 1; }
 static EncScratch enc_scratch(void* base, int M) {
   char* p = (char*)base;
   auto take = [&](size_t bytes) { char* r = p; p += (bytes + 255) / 256 * 256; return (int*)r; };
@@ -83,13 +88,15 @@ static EncScratch enc_scratch(void* base, int M) {
   s.key0 = take(sizeof(int) * M); s.pos0 = take(sizeof(int) * M);
   s.key1 = take(sizeof(int) * M); s.pos1 = take(sizeof(int) * M);
   s.seg_start = take(sizeof(int) * (M + 1)); s.nseg = take(sizeof(int) * 4);
+  s.big = take(sizeof(int) * enc_max_big(M));
   return s;
 }
 size_t encoder_backward_scratch_bytes(int M, int Vp) {
   (void)Vp;
   size_t a = ((size_t)M * 4 + 255) / 256 * 256;
   size_t b = ((size_t)(M + 1) * 4 + 255) / 256 * 256;
-  return 4 * a + b + 256;
+  size_t c = ((size_t)enc_max_big(M) * 4 + 255) / 256 * 256;
+  return 4 * a + b + 256 + c;
 }
 
 // Exclusive scan of one int per thread over the block; returns the total in *total.
@@ -205,44 +212,126 @@ encoder_sort_kernel(const int* __restrict__ tokens, int M, int Vp, EncScratch sc
     nseg_total += total;
   }
   if (threadIdx.x == 0) { sc.seg_start[nseg_total] = M; sc.nseg[0] = nseg_total; }
+  __syncthreads();
+  // the long segments, in segment order
+  int nbig = 0;
+  for (int base = 0; base < nseg_total; base += blockDim.x) {
+    const int g = base + threadIdx.x;
+    const int flag = g < nseg_total && sc.seg_start[g + 1] - sc.seg_start[g] > ENC_BIG;
+    int total;
+    const int off = block_exclusive_scan(flag, scan_sh, &total);
+    if (flag) sc.big[nbig + off] = g;
+    nbig += total;
+  }
+  if (threadIdx.x == 0) sc.nseg[1] = nbig;
 }
 
+// One warp per segment of at most ENC_BIG rows: the warp sums the segment's rows in order
+// (four per step when registers permit, all loads issued before the adds) and adds the sum to
+// that token's row of dwte, of which it is the only writer.
 template <typename T, int MAXV>
 __global__ void __launch_bounds__(256)
 encoder_segsum_kernel(float* __restrict__ dwte, const T* __restrict__ dx, int C, float scale,
                       EncScratch sc) {
   constexpr int VE = 16 / sizeof(T);
-  __shared__ float part[MAXV * 32 * VE];   // warps' partial rows, combined in warp order
-  const int seg = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int seg = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (seg >= sc.nseg[0]) return;
   const int start = sc.seg_start[seg], end = sc.seg_start[seg + 1];
+  if (end - start > ENC_BIG) return;   // encoder_bigseg_kernel
   const int id = sc.key0[start];
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int n = end - start;
-  const int per = (n + 7) / 8;
-  const int r0 = start + min(n, w * per), r1 = start + min(n, (w + 1) * per);
   float acc[MAXV][VE];
 #pragma unroll
   for (int j = 0; j < MAXV; ++j)
 #pragma unroll
     for (int e = 0; e < VE; ++e) acc[j][e] = 0.f;
-  // four rows per step, all loads issued before the adds (the frequent tokens have segments of
-  // hundreds of rows); the adds stay in row order
-  int r = r0;
-  for (; r + 4 <= r1; r += 4) {
-    int pos[4];
+  int r = start;
+  constexpr int RB = MAXV <= 4 ? 4 : 1;
+  for (; r + RB <= end; r += RB) {
+    int pos[RB];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) pos[k] = sc.pos0[r + k];
-    Vec16<T> v[4][MAXV];
+    for (int k = 0; k < RB; ++k) pos[k] = sc.pos0[r + k];
+    Vec16<T> v[RB][MAXV];
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+    for (int k = 0; k < RB; ++k)
 #pragma unroll
       for (int j = 0; j < MAXV; ++j) {
         const int c = (j * 32 + lane) * VE;
         if (c < C) v[k][j] = ld16(dx + (size_t)pos[k] * C + c);
       }
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+    for (int k = 0; k < RB; ++k)
+#pragma unroll
+      for (int j = 0; j < MAXV; ++j) {
+        const int c = (j * 32 + lane) * VE;
+        if (c < C) {
+#pragma unroll
+          for (int e = 0; e < VE; ++e) acc[j][e] += to_f32(v[k][j].e[e]);
+        }
+      }
+  }
+  for (; r < end; ++r) {
+    const T* row = dx + (size_t)sc.pos0[r] * C;
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+      const int c = (j * 32 + lane) * VE;
+      if (c < C) {
+        Vec16<T> v = ld16(row + c);
+#pragma unroll
+        for (int e = 0; e < VE; ++e) acc[j][e] += to_f32(v.e[e]);
+      }
+    }
+  }
+  float* out = dwte + (size_t)id * C;
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    const int c = (j * 32 + lane) * VE;
+    if (c < C) {
+#pragma unroll
+      for (int e = 0; e < VE; ++e) out[c + e] += scale * acc[j][e];
+    }
+  }
+}
+
+// One block of 16 warps per long segment: warp w sums its fixed share of the segment's rows
+// (four rows per step, in row order) into shared memory; thread c then adds the 16 warp rows
+// of column c in warp order: a fixed order, so the result is bit-reproducible.
+template <typename T, int MAXV>
+__global__ void __launch_bounds__(ENC_BIG_THREADS)
+encoder_bigseg_kernel(float* __restrict__ dwte, const T* __restrict__ dx, int C, float scale,
+                      EncScratch sc) {
+  constexpr int VE = 16 / sizeof(T);
+  constexpr int NW = ENC_BIG_THREADS / 32;
+  extern __shared__ float bpart[];   // [NW][C]
+  if ((int)blockIdx.x >= sc.nseg[1]) return;
+  const int seg = sc.big[blockIdx.x];
+  const int start = sc.seg_start[seg], end = sc.seg_start[seg + 1];
+  const int id = sc.key0[start];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int n = end - start;
+  const int per = (n + NW - 1) / NW;
+  const int r0 = start + min(n, w * per), r1 = start + min(n, (w + 1) * per);
+  float acc[MAXV][VE];
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j)
+#pragma unroll
+    for (int e = 0; e < VE; ++e) acc[j][e] = 0.f;
+  int r = r0;
+  constexpr int RB = MAXV <= 4 ? 4 : 1;   // rows per step (registers permitting)
+  for (; r + RB <= r1; r += RB) {
+    int pos[RB];
+#pragma unroll
+    for (int k = 0; k < RB; ++k) pos[k] = sc.pos0[r + k];
+    Vec16<T> v[RB][MAXV];
+#pragma unroll
+    for (int k = 0; k < RB; ++k)
+#pragma unroll
+      for (int j = 0; j < MAXV; ++j) {
+        const int c = (j * 32 + lane) * VE;
+        if (c < C) v[k][j] = ld16(dx + (size_t)pos[k] * C + c);
+      }
+#pragma unroll
+    for (int k = 0; k < RB; ++k)
 #pragma unroll
       for (int j = 0; j < MAXV; ++j) {
         const int c = (j * 32 + lane) * VE;
@@ -256,7 +345,7 @@ encoder_segsum_kernel(float* __restrict__ dwte, const T* __restrict__ dx, int C,
     const T* row = dx + (size_t)sc.pos0[r] * C;
 #pragma unroll
     for (int j = 0; j < MAXV; ++j) {
-      int c = (j * 32 + lane) * VE;
+      const int c = (j * 32 + lane) * VE;
       if (c < C) {
         Vec16<T> v = ld16(row + c);
 #pragma unroll
@@ -264,20 +353,21 @@ encoder_segsum_kernel(float* __restrict__ dwte, const T* __restrict__ dx, int C,
       }
     }
   }
-  for (int k = 0; k < 8; ++k) {
-    if (w == k) {
 #pragma unroll
-      for (int j = 0; j < MAXV; ++j)
+  for (int j = 0; j < MAXV; ++j) {
+    const int c = (j * 32 + lane) * VE;
+    if (c < C) {
 #pragma unroll
-        for (int e = 0; e < VE; ++e) {
-          int c = (j * 32 + lane) * VE + e;
-          part[c] = (k == 0 ? 0.f : part[c]) + acc[j][e];
-        }
+      for (int e = 0; e < VE; ++e) bpart[(size_t)w * C + c + e] = acc[j][e];
     }
-    __syncthreads();
   }
-  for (int c = threadIdx.x; c < C; c += blockDim.x)
-    dwte[(size_t)id * C + c] += scale * part[c];
+  __syncthreads();
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    float t = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < NW; ++k) t += bpart[(size_t)k * C + c];
+    dwte[(size_t)id * C + c] += scale * t;
+  }
 }
 
 template <typename T>
@@ -290,6 +380,18 @@ __global__ void encoder_wpe_kernel(float* __restrict__ dwpe, const T* __restrict
   dwpe[i] += scale * s;
 }
 
+template <typename T>
+static cudaError_t launch_bigseg(void (*kern)(float*, const T*, int, float, EncScratch), float* dwte,
+                                const void* dx, int C, int M, float scale, EncScratch sc,
+                                cudaStream_t s) {
+  const size_t smem = (size_t)(ENC_BIG_THREADS / 32) * C * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<enc_max_big(M), ENC_BIG_THREADS, smem, s>>>(dwte, (const T*)dx, C, scale, sc);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 cudaError_t encoder_backward(DType t, float* dwte, float* dwpe, const void* dx, const int* tokens,
                              int B, int T_, int C, int Vp, float scale, void* scratch,
                              cudaStream_t s) {
@@ -298,17 +400,27 @@ cudaError_t encoder_backward(DType t, float* dwte, float* dwpe, const void* dx, 
   encoder_sort_kernel<<<1, SORT_THREADS, 0, s>>>(tokens, M, Vp, sc); count_launches(1);
   if (t == DType::BF16) {
     if (C > 2048 || C % 8) return cudaErrorInvalidValue;
-    if (C <= 256) { encoder_segsum_kernel<bf16, 1><<<M, 256, 0, s>>>(dwte, (const bf16*)dx, C, scale, sc); count_launches(1); }
-    else if (C <= 512) { encoder_segsum_kernel<bf16, 2><<<M, 256, 0, s>>>(dwte, (const bf16*)dx, C, scale, sc); count_launches(1); }
-    else if (C <= 1024) { encoder_segsum_kernel<bf16, 4><<<M, 256, 0, s>>>(dwte, (const bf16*)dx, C, scale, sc); count_launches(1); }
-    else { encoder_segsum_kernel<bf16, 8><<<M, 256, 0, s>>>(dwte, (const bf16*)dx, C, scale, sc); count_launches(1); }
+    if (C <= 256) { encoder_segsum_kernel<bf16, 1><<<ceil_div(M, 8), 256, 0, s>>>(dwte, (const bf16*)dx, C, scale, sc); count_launches(1); }
+    else if (C <= 512) { encoder_segsum_kernel<bf16, 2><<<ceil_div(M, 8), 256, 0, s>>>(dwte, (const bf16*)dx, C, scale, sc); count_launches(1); }
+    else if (C <= 1024) { encoder_segsum_kernel<bf16, 4><<<ceil_div(M, 8), 256, 0, s>>>(dwte, (const bf16*)dx, C, scale, sc); count_launches(1); }
+    else { encoder_segsum_kernel<bf16, 8><<<ceil_div(M, 8), 256, 0, s>>>(dwte, (const bf16*)dx, C, scale, sc); count_launches(1); }
+    cudaError_t e = C <= 256    ? launch_bigseg(encoder_bigseg_kernel<bf16, 1>, dwte, dx, C, M, scale, sc, s)
+                    : C <= 512  ? launch_bigseg(encoder_bigseg_kernel<bf16, 2>, dwte, dx, C, M, scale, sc, s)
+                    : C <= 1024 ? launch_bigseg(encoder_bigseg_kernel<bf16, 4>, dwte, dx, C, M, scale, sc, s)
+                                : launch_bigseg(encoder_bigseg_kernel<bf16, 8>, dwte, dx, C, M, scale, sc, s);
+    if (e != cudaSuccess) return e;
     encoder_wpe_kernel<bf16><<<ceil_div((long long)T_ * C, 256), 256, 0, s>>>(dwpe, (const bf16*)dx, B, T_, C, scale); count_launches(1);
   } else {
     if (C > 1024 || C % 4) return cudaErrorInvalidValue;
-    if (C <= 128) { encoder_segsum_kernel<float, 1><<<M, 256, 0, s>>>(dwte, (const float*)dx, C, scale, sc); count_launches(1); }
-    else if (C <= 256) { encoder_segsum_kernel<float, 2><<<M, 256, 0, s>>>(dwte, (const float*)dx, C, scale, sc); count_launches(1); }
-    else if (C <= 512) { encoder_segsum_kernel<float, 4><<<M, 256, 0, s>>>(dwte, (const float*)dx, C, scale, sc); count_launches(1); }
-    else { encoder_segsum_kernel<float, 8><<<M, 256, 0, s>>>(dwte, (const float*)dx, C, scale, sc); count_launches(1); }
+    if (C <= 128) { encoder_segsum_kernel<float, 1><<<ceil_div(M, 8), 256, 0, s>>>(dwte, (const float*)dx, C, scale, sc); count_launches(1); }
+    else if (C <= 256) { encoder_segsum_kernel<float, 2><<<ceil_div(M, 8), 256, 0, s>>>(dwte, (const float*)dx, C, scale, sc); count_launches(1); }
+    else if (C <= 512) { encoder_segsum_kernel<float, 4><<<ceil_div(M, 8), 256, 0, s>>>(dwte, (const float*)dx, C, scale, sc); count_launches(1); }
+    else { encoder_segsum_kernel<float, 8><<<ceil_div(M, 8), 256, 0, s>>>(dwte, (const float*)dx, C, scale, sc); count_launches(1); }
+    cudaError_t e = C <= 128   ? launch_bigseg(encoder_bigseg_kernel<float, 1>, dwte, dx, C, M, scale, sc, s)
+                    : C <= 256 ? launch_bigseg(encoder_bigseg_kernel<float, 2>, dwte, dx, C, M, scale, sc, s)
+                    : C <= 512 ? launch_bigseg(encoder_bigseg_kernel<float, 4>, dwte, dx, C, M, scale, sc, s)
+                               : launch_bigseg(encoder_bigseg_kernel<float, 8>, dwte, dx, C, M, scale, sc, s);
+    if (e != cudaSuccess) return e;
     encoder_wpe_kernel<float><<<ceil_div((long long)T_ * C, 256), 256, 0, s>>>(dwpe, (const float*)dx, B, T_, C, scale); count_launches(1);
   }
   return last();
