@@ -33,6 +33,11 @@ METRIC = "GPT-2 124M training tokens/sec on 1 B300; MFU vs dense BF16 tensor pea
 WORKLOAD = "gpt2-124m-step"
 
 
+# from the ncu launch list in profiles/gpt2_124m_step_launches.md (re-take it, or set this to
+# None, whenever the GEMM kernel changes)
+GEMM_DRAM_BYTES_PER_LAUNCH = 109.5e6
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -326,7 +331,10 @@ def run_ours(args, w):
                          "peak_kind": f"bf16 sustained ({pk['source']})",
                          "launches": g_n, "avg_launch_ms": g_ms / g_n if g_n else None,
                          "timed_launches": "every GEMM of each timed step's first micro-batch",
-                         "traffic": None},
+                         # DRAM bytes read + written per GEMM launch, averaged over the 588
+                         # GEMM launches of an ncu launch list of this bench (2 steps x 2
+                         # micro-batches; profiles/gpt2_124m_step_launches.md)
+                         "traffic": GEMM_DRAM_BYTES_PER_LAUNCH},
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
