@@ -115,6 +115,29 @@ def dist_setup():
     return world, rank, local
 
 
+def rank_token_batches(w, rank, n):
+    """The rank's own token stream, n batches of [B, T+1] ids: each replica trains on
+    different data (weak scaling, no collective on the data path)."""
+    return np.stack([S.token_stream(w["tok_seed"], rank * 1_000_000 + i, w["B"], w["T"], w["V"],
+                                    w["dist"], w["s"]) for i in range(n)])
+
+
+def max_over_ranks(x, device):
+    """The slowest replica's value: the job's time is the maximum over ranks."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, steps, B, T, accum, seconds):
+    """Whole-job throughput: the tokens every replica processed over the slowest one's time."""
+    return world * steps * B * T * accum / seconds
+
+
 def oracle_sample(w, params_seed, seq_index, steps_label):
     """The CPU oracle on a bounded sample of the workload: one 1024-token sequence,
     forward + backward, then AdamW over every parameter. Returns (tokens, seconds)."""
@@ -215,8 +238,7 @@ def run_ours(args, w):
     # token batches for every step, generated up front and resident in HBM
     W, K = args.warmup, args.steps
     nb = (W + K) * accum
-    ids = np.stack([S.token_stream(w["tok_seed"], rank * 1_000_000 + i, B, T, w["V"], w["dist"],
-                                   w["s"]) for i in range(nb)])
+    ids = rank_token_batches(w, rank, nb)
     dtok = torch.tensor(ids[:, :, :T]).cuda().contiguous()
     dtgt = torch.tensor(ids[:, :, 1:]).cuda().contiguous()
 
@@ -264,12 +286,8 @@ def run_ours(args, w):
     loss = m.get_loss()
     g_n, g_ms, g_flops = m.profile_read("gemm", reset=True)
     m.profile_enable((), capacity=0)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-    tokens = world * K * B * T * accum
-    value = tokens / (elapsed_ms / 1000.0)
+    elapsed_ms = max_over_ranks(elapsed_ms, "cuda")
+    value = job_tokens_per_s(world, K, B, T, accum, elapsed_ms / 1000.0)
 
     # ---------------- end to end: host (pinned) tokens copied in, loss read back, per step
     e2e = None
@@ -293,12 +311,8 @@ def run_ours(args, w):
             step_e2e(si)
         torch.cuda.synchronize()
         barrier()
-        e2e_s = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([e2e_s], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = {"value": tokens / e2e_s, "unit": "tokens/s",
+        e2e_s = max_over_ranks(time.perf_counter() - t0, "cuda")
+        e2e = {"value": job_tokens_per_s(world, K, B, T, accum, e2e_s), "unit": "tokens/s",
                "h2d_bytes_per_step": int(accum * 2 * B * T * 4), "d2h_bytes_per_step": 4}
 
     pk = peaks()
