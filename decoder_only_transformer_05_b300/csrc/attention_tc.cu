@@ -28,6 +28,9 @@
 //   queries): S = Q K_j^T, dP = dO V_j^T, dQ += dS K_j. Each output row belongs to one
 //   unit, so the result is deterministic. The eight elementwise warps split the columns
 //   (warps w and w + 4 take 64 each): no row reduction is needed once lse and D are known.
+//   P^T, dS^T (dK/dV) and dS (dQ, double-buffered) go back into tensor memory as bf16 pairs
+//   and are the A operand of the second-stage MMAs (tcgen05.mma with A in tensor memory), so
+//   they never touch shared memory; the Q/dO and K/V rings have four stages.
 // Rows past T (ragged T) read zeros through the 3-D tensor maps and are never stored.
 #include <cstring>
 #include <type_traits>

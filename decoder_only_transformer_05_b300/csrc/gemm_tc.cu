@@ -6,22 +6,26 @@
 // (m or n contiguous). Forward GEMMs are K-major x K-major, dgrad GEMMs K-major x
 // MN-major, wgrad GEMMs MN-major x MN-major.
 //
-// Structure (one persistent block of 320 threads per SM, blocks paired in clusters of 2):
-//   warp 0      TMA producer: 128x64 A and BNx64 B tiles, 128-byte swizzle, into a
-//               ring of shared-memory stages (mbarrier full/empty handshake). The two
-//               blocks of a cluster work on vertically adjacent tiles (same columns), so
-//               they need the same B tile: each loads one half of it and multicasts it
-//               into both blocks' shared memory, which cuts the L2-to-SM operand traffic
-//               by a third. A stage is free once both blocks' MMAs have read it (each
-//               MMA completion arrives on the empty barrier of both blocks).
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN, K=16) into a
-//               fp32 accumulator in tensor memory; two accumulators alternate so the
-//               epilogue of one tile overlaps the main loop of the next
-//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).. (the rows of its quarter),
-//               warps w and w+4 take alternate 32-column chunks of the tile. Per chunk:
-//               tcgen05.ld, the epilogue arithmetic, the result into a swizzled
-//               shared-memory staging buffer, then one TMA bulk-tensor store (or, for
-//               gradient accumulation, a TMA bulk-tensor reduce-add) of the 32x32 chunk.
+// Structure (one persistent block of 320 threads per SM, blocks paired in clusters of 2; a
+// work unit is two vertically adjacent 128 x BN output tiles, one per block):
+//   warp 0      TMA producer (both blocks): the block's 128 x 64 rows of A and its half
+//               (BN/2 x 64) of the B tile, 128-byte swizzle, into a ring of shared-memory
+//               stages; both blocks' bytes complete on the even block's full barrier.
+//   warp 1      MMA issuer (one thread of the even block): tcgen05.mma.cta_group::2 with
+//               M = 256, N = BN, K = 16 reads the A rows and the B half each block holds and
+//               writes each block's 128 rows of the fp32 accumulator into that block's
+//               tensor memory; its commits free a stage, or hand over an accumulator, in both
+//               blocks at once. Two accumulators alternate so the epilogue of one tile
+//               overlaps the main loop of the next. Each block holds only half of B, which
+//               cuts the shared-memory operand bytes per FLOP by a third against one block
+//               per tile.
+//   warps 2..9  epilogue (both blocks): warp w reads TMEM lanes 32*(w%4).. (the rows of its
+//               quarter), warps w and w+4 take alternate 32-column chunks of the tile. Per
+//               chunk: tcgen05.ld, the epilogue arithmetic on packed fp32 pairs, the result
+//               into a swizzled shared-memory staging buffer, then one TMA bulk-tensor store
+//               (or, for gradient accumulation, a TMA bulk-tensor reduce-add) of the 32x32
+//               chunk. The epilogue warps of both blocks arrive on the even block's barrier
+//               when an accumulator is free again.
 // Every mbarrier wait is bounded: on timeout the block records DEV_ERR_TIMEOUT, stops
 // issuing work, waits for its own copies and MMAs and frees its tensor memory.
 #include <cuda.h>
