@@ -460,8 +460,7 @@ classifier_kernel(T* __restrict__ logits, float* __restrict__ losses,
   // pass 1 (log2 domain): running max m and sum s of 2^(z*log2e - m)
   float m = -INFINITY, s = 0.f;
   const int nvec = Vp / VE;
-  for (int i = threadIdx.x; i < nvec; i += CLS_THREADS) {
-    Vec16<T> v = ld16(z + (size_t)i * VE);
+  auto consume = [&](const Vec16<T>& v, int i) {
     float a[VE];
     float lm = -INFINITY;
 #pragma unroll
@@ -469,12 +468,20 @@ classifier_kernel(T* __restrict__ logits, float* __restrict__ losses,
       a[e] = (i * VE + e < V) ? to_f32(v.e[e]) * LOG2E : -INFINITY;
       lm = fmaxf(lm, a[e]);
     }
-    if (lm == -INFINITY) continue;
+    if (lm == -INFINITY) return;
     float ls = 0.f;
 #pragma unroll
     for (int e = 0; e < VE; ++e) ls += fast_exp2(a[e] - lm);
     online_merge(m, s, lm, ls);
+  };
+  // two vectors per step, both loads issued first (more bytes in flight per thread)
+  int i = threadIdx.x;
+  for (; i + CLS_THREADS < nvec; i += 2 * CLS_THREADS) {
+    const Vec16<T> v0 = ld16(z + (size_t)i * VE), v1 = ld16(z + (size_t)(i + CLS_THREADS) * VE);
+    consume(v0, i);
+    consume(v1, i + CLS_THREADS);
   }
+  if (i < nvec) consume(ld16(z + (size_t)i * VE), i);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     float m2 = __shfl_xor_sync(0xffffffffu, m, o);

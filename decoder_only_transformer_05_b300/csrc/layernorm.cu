@@ -549,6 +549,15 @@ colsum_kernel(float* __restrict__ partials, const T* __restrict__ dy, int M, int
   for (int e = 0; e < VE; ++e) acc[e] = 0.f;
   if (c < N) {
     int r = r0 + wid;
+    for (; r + 56 < r1; r += 64) {   // eight rows in flight per thread
+      Vec16<T> v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = ld16(dy + (size_t)(r + 8 * k) * N + c);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+#pragma unroll
+        for (int e = 0; e < VE; ++e) acc[e] += to_f32(v[k].e[e]);
+    }
     for (; r + 24 < r1; r += 32) {
       Vec16<T> v0 = ld16(dy + (size_t)r * N + c), v1 = ld16(dy + (size_t)(r + 8) * N + c);
       Vec16<T> v2 = ld16(dy + (size_t)(r + 16) * N + c), v3 = ld16(dy + (size_t)(r + 24) * N + c);
