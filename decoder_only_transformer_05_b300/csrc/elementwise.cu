@@ -380,14 +380,22 @@ __global__ void encoder_wpe_kernel(float* __restrict__ dwpe, const T* __restrict
   dwpe[i] += scale * s;
 }
 
-template <typename T>
-static cudaError_t launch_bigseg(void (*kern)(float*, const T*, int, float, EncScratch), float* dwte,
-                                const void* dx, int C, int M, float scale, EncScratch sc,
-                                cudaStream_t s) {
+// The segment sums and the position-embedding column sums for one element type and row width.
+template <typename T, int MAXV>
+static cudaError_t encoder_sums(float* dwte, float* dwpe, const void* dx, int B, int T_, int C,
+                                float scale, EncScratch sc, cudaStream_t s) {
+  const int M = B * T_;
+  const T* x = (const T*)dx;
+  encoder_segsum_kernel<T, MAXV><<<ceil_div(M, 8), 256, 0, s>>>(dwte, x, C, scale, sc);
+  count_launches(1);
   const size_t smem = (size_t)(ENC_BIG_THREADS / 32) * C * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(encoder_bigseg_kernel<T, MAXV>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<enc_max_big(M), ENC_BIG_THREADS, smem, s>>>(dwte, (const T*)dx, C, scale, sc);
+  encoder_bigseg_kernel<T, MAXV><<<enc_max_big(M), ENC_BIG_THREADS, smem, s>>>(dwte, x, C, scale,
+                                                                               sc);
+  count_launches(1);
+  encoder_wpe_kernel<T><<<ceil_div((long long)T_ * C, 256), 256, 0, s>>>(dwpe, x, B, T_, C, scale);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -395,35 +403,23 @@ static cudaError_t launch_bigseg(void (*kern)(float*, const T*, int, float, EncS
 cudaError_t encoder_backward(DType t, float* dwte, float* dwpe, const void* dx, const int* tokens,
                              int B, int T_, int C, int Vp, float scale, void* scratch,
                              cudaStream_t s) {
-  int M = B * T_;
+  const int M = B * T_;
   EncScratch sc = enc_scratch(scratch, M);
-  encoder_sort_kernel<<<1, SORT_THREADS, 0, s>>>(tokens, M, Vp, sc); count_launches(1);
+  encoder_sort_kernel<<<1, SORT_THREADS, 0, s>>>(tokens, M, Vp, sc);
+  count_launches(1);
+  // MAXV 16-byte vectors per lane cover the row: 8 bf16 or 4 fp32 each, 32 lanes
   if (t == DType::BF16) {
     if (C > 2048 || C % 8) return cudaErrorInvalidValue;
-    if (C <= 256) { encoder_segsum_kernel<bf16, 1><<<ceil_div(M, 8), 256, 0, s>>>(dwte, (const bf16*)dx, C, scale, sc); count_launches(1); }
-    else if (C <= 512) { encoder_segsum_kernel<bf16, 2><<<ceil_div(M, 8), 256, 0, s>>>(dwte, (const bf16*)dx, C, scale, sc); count_launches(1); }
-    else if (C <= 1024) { encoder_segsum_kernel<bf16, 4><<<ceil_div(M, 8), 256, 0, s>>>(dwte, (const bf16*)dx, C, scale, sc); count_launches(1); }
-    else { encoder_segsum_kernel<bf16, 8><<<ceil_div(M, 8), 256, 0, s>>>(dwte, (const bf16*)dx, C, scale, sc); count_launches(1); }
-    cudaError_t e = C <= 256    ? launch_bigseg(encoder_bigseg_kernel<bf16, 1>, dwte, dx, C, M, scale, sc, s)
-                    : C <= 512  ? launch_bigseg(encoder_bigseg_kernel<bf16, 2>, dwte, dx, C, M, scale, sc, s)
-                    : C <= 1024 ? launch_bigseg(encoder_bigseg_kernel<bf16, 4>, dwte, dx, C, M, scale, sc, s)
-                                : launch_bigseg(encoder_bigseg_kernel<bf16, 8>, dwte, dx, C, M, scale, sc, s);
-    if (e != cudaSuccess) return e;
-    encoder_wpe_kernel<bf16><<<ceil_div((long long)T_ * C, 256), 256, 0, s>>>(dwpe, (const bf16*)dx, B, T_, C, scale); count_launches(1);
-  } else {
-    if (C > 1024 || C % 4) return cudaErrorInvalidValue;
-    if (C <= 128) { encoder_segsum_kernel<float, 1><<<ceil_div(M, 8), 256, 0, s>>>(dwte, (const float*)dx, C, scale, sc); count_launches(1); }
-    else if (C <= 256) { encoder_segsum_kernel<float, 2><<<ceil_div(M, 8), 256, 0, s>>>(dwte, (const float*)dx, C, scale, sc); count_launches(1); }
-    else if (C <= 512) { encoder_segsum_kernel<float, 4><<<ceil_div(M, 8), 256, 0, s>>>(dwte, (const float*)dx, C, scale, sc); count_launches(1); }
-    else { encoder_segsum_kernel<float, 8><<<ceil_div(M, 8), 256, 0, s>>>(dwte, (const float*)dx, C, scale, sc); count_launches(1); }
-    cudaError_t e = C <= 128   ? launch_bigseg(encoder_bigseg_kernel<float, 1>, dwte, dx, C, M, scale, sc, s)
-                    : C <= 256 ? launch_bigseg(encoder_bigseg_kernel<float, 2>, dwte, dx, C, M, scale, sc, s)
-                    : C <= 512 ? launch_bigseg(encoder_bigseg_kernel<float, 4>, dwte, dx, C, M, scale, sc, s)
-                               : launch_bigseg(encoder_bigseg_kernel<float, 8>, dwte, dx, C, M, scale, sc, s);
-    if (e != cudaSuccess) return e;
-    encoder_wpe_kernel<float><<<ceil_div((long long)T_ * C, 256), 256, 0, s>>>(dwpe, (const float*)dx, B, T_, C, scale); count_launches(1);
+    if (C <= 256) return encoder_sums<bf16, 1>(dwte, dwpe, dx, B, T_, C, scale, sc, s);
+    if (C <= 512) return encoder_sums<bf16, 2>(dwte, dwpe, dx, B, T_, C, scale, sc, s);
+    if (C <= 1024) return encoder_sums<bf16, 4>(dwte, dwpe, dx, B, T_, C, scale, sc, s);
+    return encoder_sums<bf16, 8>(dwte, dwpe, dx, B, T_, C, scale, sc, s);
   }
-  return last();
+  if (C > 1024 || C % 4) return cudaErrorInvalidValue;
+  if (C <= 128) return encoder_sums<float, 1>(dwte, dwpe, dx, B, T_, C, scale, sc, s);
+  if (C <= 256) return encoder_sums<float, 2>(dwte, dwpe, dx, B, T_, C, scale, sc, s);
+  if (C <= 512) return encoder_sums<float, 4>(dwte, dwpe, dx, B, T_, C, scale, sc, s);
+  return encoder_sums<float, 8>(dwte, dwpe, dx, B, T_, C, scale, sc, s);
 }
 
 // =====================================================================================
