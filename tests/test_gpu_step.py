@@ -340,6 +340,39 @@ def test_forward_backward_graphs_per_shape():
     m.close()
 
 
+def test_checkpoint_resume_is_bit_identical():
+    """Checkpoint = the fp32 parameters, both AdamW moments and the step counter. Restored into
+    a new handle (writing the parameters refreshes its bf16 copy), the next optimiser step
+    gives the same parameters bit for bit as the uninterrupted run."""
+    m, params, cfg, w = make("char-bf16", B=8)
+    batches = [tokens_for(w, 8, index=30 + i) for i in range(3)]
+
+    def train_step(model, i):
+        tok, tgt, dtok, dtgt = batches[i]
+        model.zero_grad()
+        model.forward_backward(dtok, dtgt, 8, w["T"], 1.0)
+        model.adamw_step(1e-3, 0.9, 0.95, 1e-8, 0.1, grad_clip=1.0)
+
+    train_step(m, 0)
+    train_step(m, 1)
+    ckpt = {r: m.read_region(r, np.float32) for r in ("params", "m", "v")}
+    t = m.step
+    assert t == 2
+    train_step(m, 2)
+    want = m.read_region("params", np.float32)
+
+    m2, _, _, _ = make("char-bf16", B=8)
+    for r, a in ckpt.items():
+        m2.write_region(r, a)
+    m2.step = t
+    train_step(m2, 2)
+    got = m2.read_region("params", np.float32)
+    assert not np.array_equal(want, ckpt["params"])   # the step did move the parameters
+    assert np.array_equal(got, want)
+    m.close()
+    m2.close()
+
+
 def test_bf16_zero_logits_give_ln_vocab():
     """lnf gamma = beta = 0 makes every logit exactly 0: the loss is ln V over the real
     vocabulary (the padded columns are masked)."""
