@@ -907,8 +907,8 @@ extern "C" int gpt2_region_ptr(gpt2_handle h, int r, void** d_ptr, size_t* bytes
 extern "C" int gpt2_copy_region(gpt2_handle h, int r, size_t offset, void* h_buf, size_t bytes,
                                 int to_device) {
   if (!h || (!h_buf && bytes)) return fail(GPT2_ERR_ARG, "null argument");
-  void* p;
-  size_t n;
+  void* p = nullptr;
+  size_t n = 0;
   int rc = region(h, r, &p, &n);
   if (rc) return rc;
   if (offset > n || bytes > n - offset) return fail(GPT2_ERR_ARG, "copy out of range");
