@@ -87,53 +87,14 @@ __device__ __forceinline__ float gelu_tanh_grad(float x) {
   return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * k * (1.0f + 3.0f * 0.044715f * x * x);
 }
 
-// The same two functions with tanh from the hardware approximation (PTX tanh.approx.f32,
-// relative error about 2^-11): used where the result is rounded to bf16 (8 significant
-// bits), so the approximation error stays well below the rounding step.
+// tanh from the hardware approximation (PTX tanh.approx.f32, relative error about 2^-11):
+// used where the result is rounded to bf16 (8 significant bits), so the approximation
+// error stays well below the rounding step.
 __device__ __forceinline__ float tanh_approx(float x) {
   float y;
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ float gelu_tanh_fast(float x) {
-  const float k0 = 0.7978845608028654f, k1 = 0.044715f * 0.7978845608028654f;
-  const float t = tanh_approx(x * fmaf(k1, x * x, k0));
-  const float hx = 0.5f * x;
-  return fmaf(hx, t, hx);
-}
-__device__ __forceinline__ float gelu_tanh_grad_fast(float x) {
-  const float k0 = 0.7978845608028654f, k1 = 0.044715f * 0.7978845608028654f;
-  const float x2 = x * x;
-  const float t = tanh_approx(x * fmaf(k1, x2, k0));
-  // 0.5 (1 + t) + 0.5 x (1 - t^2) (k0 + 3 k1 x^2)
-  return fmaf(0.5f * x * fmaf(-t, t, 1.0f), fmaf(3.0f * k1, x2, k0), fmaf(0.5f, t, 0.5f));
-}
-
-// The same on a pair of values with the packed two-lane fp32 instructions.
-__device__ __forceinline__ float2 gelu_tanh_fast2(float2 x) {
-  const float2 k0 = make_float2(0.7978845608028654f, 0.7978845608028654f);
-  const float2 k1 = make_float2(0.044715f * 0.7978845608028654f, 0.044715f * 0.7978845608028654f);
-  const float2 h = make_float2(0.5f, 0.5f);
-  const float2 u = __fmul2_rn(x, __ffma2_rn(k1, __fmul2_rn(x, x), k0));
-  const float2 t = make_float2(tanh_approx(u.x), tanh_approx(u.y));
-  const float2 hx = __fmul2_rn(h, x);
-  return __ffma2_rn(hx, t, hx);
-}
-__device__ __forceinline__ float2 gelu_tanh_grad_fast2(float2 x) {
-  const float2 k0 = make_float2(0.7978845608028654f, 0.7978845608028654f);
-  const float2 k1 = make_float2(0.044715f * 0.7978845608028654f, 0.044715f * 0.7978845608028654f);
-  const float2 k3 = make_float2(3.0f * 0.044715f * 0.7978845608028654f,
-                                3.0f * 0.044715f * 0.7978845608028654f);
-  const float2 h = make_float2(0.5f, 0.5f), one = make_float2(1.0f, 1.0f);
-  const float2 x2 = __fmul2_rn(x, x);
-  const float2 u = __fmul2_rn(x, __ffma2_rn(k1, x2, k0));
-  const float2 t = make_float2(tanh_approx(u.x), tanh_approx(u.y));
-  const float2 nt = make_float2(-t.x, -t.y);
-  // 0.5 (1 + t) + 0.5 x (1 - t^2) (k0 + 3 k1 x^2)
-  const float2 a = __fmul2_rn(__fmul2_rn(h, x), __ffma2_rn(nt, t, one));
-  return __ffma2_rn(a, __ffma2_rn(k3, x2, k0), __ffma2_rn(h, t, h));
-}
-
 // gelu_tanh(x) and, in `grad`, gelu_tanh'(x) from one tanh
 __device__ __forceinline__ float2 gelu_tanh_and_grad_fast2(float2 x, float2& grad) {
   const float2 k0 = make_float2(0.7978845608028654f, 0.7978845608028654f);

@@ -31,6 +31,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -68,6 +69,9 @@ struct Params {
   const bf16* bias; const bf16* resid; const bf16* aux;
   float scale;
   int* err;
+  unsigned long long wait_ns;   // limit of every bounded wait (normally TIMEOUT_NS)
+  int drop_first_signal;        // test hook: the first accumulator of each block pair is
+                                // never signalled ready, so its epilogue wait runs out
 };
 
 // ------------------------------------------------------------------ epilogue
@@ -233,7 +237,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % Cf::STAGES;
           const uint32_t ph = (uint32_t)(it / Cf::STAGES) & 1u;
-          if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, p.err, true, p.wait_ns)) { ok = false; break; }
           const uint32_t a_dst = base + s * Cf::STAGE, b_dst = a_dst + Cf::A_BYTES;
           if (leader) mbar_expect_tx(full(s), 2 * Cf::STAGE);   // both blocks' bytes
           const uint32_t fb = mapa_shared(full(s), 0);
@@ -269,13 +273,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         const int kb0 = sp * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         const int acc = tcount & 1;
         const uint32_t aph = (uint32_t)(tcount >> 1) & 1u;
-        if (!mbar_wait(tempty(acc), aph ^ 1u, abort_flag, p.err)) { ok = false; break; }
+        if (!mbar_wait(tempty(acc), aph ^ 1u, abort_flag, p.err, true, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % Cf::STAGES;
           const uint32_t ph = (uint32_t)(it / Cf::STAGES) & 1u;
-          if (!mbar_wait(full(s), ph, abort_flag, p.err)) { ok = false; break; }
+          if (!mbar_wait(full(s), ph, abort_flag, p.err, true, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_base = base + s * Cf::STAGE, b_base = a_base + Cf::A_BYTES;
 #pragma unroll
@@ -289,7 +293,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           umma_commit_pair_mc(empty(s), PAIR);   // the stage is free in both blocks
         }
         if (!ok) break;
-        umma_commit_pair_mc(tfull(acc), PAIR);   // both blocks' accumulators are ready
+        if (!(p.drop_first_signal && tcount == 0))
+          umma_commit_pair_mc(tfull(acc), PAIR);   // both blocks' accumulators are ready
       }
       // all issued MMAs complete before tensor memory is released
       umma_commit_pair(final_bar);
@@ -337,7 +342,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       decode(unit, mb, nb, sp);
       const int acc = tcount & 1;
       const uint32_t aph = (uint32_t)(tcount >> 1) & 1u;
-      bool ok = mbar_wait(tfull(acc), aph, abort_flag, p.err);
+      bool ok = mbar_wait(tfull(acc), aph, abort_flag, p.err, true, p.wait_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -349,7 +354,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         if (col0 >= p.N) break;
         uint4 inp[4];
         if (has_in) {
-          ok = __all_sync(0xffffffffu, mbar_wait(ibar, (uint32_t)n_in & 1u, abort_flag, p.err));
+          ok = __all_sync(0xffffffffu, mbar_wait(ibar, (uint32_t)n_in & 1u, abort_flag, p.err, true, p.wait_ns));
           if (!ok) break;
           ++n_in;
           in_pending = false;
@@ -396,6 +401,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 }
 
 // ------------------------------------------------------------------ host side
+// Test hook for the bounded waits (gpt2_debug_gemm_waits): a wait limit other than
+// TIMEOUT_NS and a dropped accumulator signal, read at every launch. Off by default.
+static std::atomic<long long> g_gemm_wait_ns{0};
+static std::atomic<int> g_gemm_drop_signal{0};
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -471,6 +481,11 @@ static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
   p.aux = (const bf16*)g.aux;
   p.scale = g.scale;
   p.err = g.err;
+  {
+    const long long w = g_gemm_wait_ns.load(std::memory_order_relaxed);
+    p.wait_ns = w > 0 ? (unsigned long long)w : TIMEOUT_NS;
+    p.drop_first_signal = g_gemm_drop_signal.load(std::memory_order_relaxed);
+  }
   if (p.splits > 1 && !g.workspace) return cudaErrorInvalidValue;
   if ((g.bias && ((uintptr_t)g.bias & 15u)) || (g.resid && ((uintptr_t)g.resid & 15u)) ||
       (g.aux && ((uintptr_t)g.aux & 15u)) || (g.ldo % 8))
@@ -526,6 +541,11 @@ static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
 }
 
 }  // namespace tc
+
+void gemm_tc_debug_waits(long long wait_limit_ns, int drop_first_signal) {
+  tc::g_gemm_wait_ns.store(wait_limit_ns > 0 ? wait_limit_ns : 0);
+  tc::g_gemm_drop_signal.store(drop_first_signal ? 1 : 0);
+}
 
 int gemm_tc_num_sms() {
   static int n = 0;

@@ -80,3 +80,8 @@ extern "C" int gpt2_op_classifier(int precision, void* logits, float* losses,
   return status(classifier(dtype(precision), logits, losses, targets, M, V, Vp, err,
                            (cudaStream_t)stream));
 }
+
+extern "C" int gpt2_debug_gemm_waits(int64_t wait_limit_ns, int drop_first_signal) {
+  gemm_tc_debug_waits((long long)wait_limit_ns, drop_first_signal);
+  return GPT2_OK;
+}

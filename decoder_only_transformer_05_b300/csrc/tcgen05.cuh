@@ -51,9 +51,11 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
       : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
   return ok != 0;
 }
-// Bounded wait. Returns false if the block is aborting or this wait timed out.
+// Bounded wait (limit_ns of %globaltimer). Returns false if the block is aborting or this
+// wait timed out; a timeout sets the block's abort flag and DEV_ERR_TIMEOUT in *err.
 static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       int* err, bool honour_abort = true) {
+                                       int* err, bool honour_abort = true,
+                                       unsigned long long limit_ns = TIMEOUT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
@@ -61,7 +63,7 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (honour_abort && *abort_flag) return false;
-    if (globaltimer() - t0 > TIMEOUT_NS) {
+    if (globaltimer() - t0 > limit_ns) {
       *abort_flag = 1;
       if (err) atomicOr(err, DEV_ERR_TIMEOUT);
       return false;
@@ -74,16 +76,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"((unsigned long long)map), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-// The same load delivered to every CTA of the cluster in cta_mask, at the same shared-memory
-// offset, each completing bytes on its own barrier at the offset of `bar`.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                               int c0, int c1, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"((unsigned long long)map), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask)
       : "memory");
 }
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -175,13 +167,6 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-// ... arriving on the barrier at the offset of `bar` in every CTA of cta_mask
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(cta_mask)
       : "memory");
 }
 // 32 TMEM lanes x 32 consecutive 32-bit columns; thread i of the warp gets lane base+i.

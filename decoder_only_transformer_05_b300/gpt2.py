@@ -87,6 +87,7 @@ SIGNATURES = {
     "gpt2_op_classifier": (_I, [_I, _P, _P, _P, _I, _I, _I, _P, _P]),
     "gpt2_op_layernorm_backward_noalloc": (_I, [_I, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I,
                                                 _I, _F, _P]),
+    "gpt2_debug_gemm_waits": (_I, [_I64, _I]),
 }
 
 _lib = None
@@ -380,3 +381,9 @@ def op_layernorm_backward_noalloc(precision, dres, accumulate, dw, db, dy, x, w,
                                                   ptr(dw), ptr(db), ptr(dy), ptr(x), ptr(w),
                                                   ptr(mean), ptr(rstd), M, C, scale,
                                                   stream_handle(stream)))
+
+
+def debug_gemm_waits(wait_limit_ns=0, drop_first_signal=False):
+    """Test hook of the GEMM's bounded waits (see include/gpt2_ops.h); (0, False) = off."""
+    lib = load_library()
+    _check(lib.gpt2_debug_gemm_waits(int(wait_limit_ns), int(bool(drop_first_signal))))

@@ -74,8 +74,9 @@ int gpt2_op_layernorm_backward(int precision, void* dres, int accumulate, float*
  *     at any M, e.g. C = 768 or 1024); larger shapes return GPT2_ERR_ARG with a message
  *     and launch nothing.
  *   - Set-up: the first call on each device (made with that device current) looks up the
- *     array's device address with cudaGetSymbolAddress; make that first call before any
- *     stream capture on that device.
+ *     array's device address with cudaGetSymbolAddress, and so does the first call after
+ *     that device's CUDA context changed (cudaDeviceReset, a driver-API context); make
+ *     those calls before any stream capture on that device.
  *   - Sharing: every call uses the same array. Calls whose work overlaps on the GPU (two
  *     streams, or two host threads) race on it; serialise them. Nothing in the array needs
  *     to start at zero: each call overwrites the partial sums it reads.
@@ -90,6 +91,20 @@ int gpt2_op_layernorm_backward_noalloc(int precision, void* dres, int accumulate
    err: device int, OR-ed with 4 when a target is out of range. */
 int gpt2_op_classifier(int precision, void* logits, float* losses, const int32_t* targets,
                        int M, int V, int Vp, int* err, void* stream);
+
+/*
+ * Test hook for failure detection; the pages have no counterpart. Every mbarrier wait in the
+ * tensor-core GEMM is bounded: when one runs out, the kernel sets GPT2_ERR_TIMEOUT in the
+ * device error word it was given (a handle's word: reported by its next gpt2_sync /
+ * gpt2_get_loss), stops issuing work, lets its own copies and MMAs finish, frees its tensor
+ * memory and returns, so the context and the handle stay usable. This call changes, for the
+ * GEMM launches that follow it in this process, the limit of those waits (wait_limit_ns;
+ * <= 0 restores the default of 2 s) and, with drop_first_signal = 1, withholds the signal
+ * that the first accumulator of each block pair is ready, so that its epilogue's wait runs
+ * out. Launches already recorded into a CUDA graph keep the settings they were recorded
+ * with. Off by default; (0, 0) turns it off.
+ */
+int gpt2_debug_gemm_waits(int64_t wait_limit_ns, int drop_first_signal);
 
 #ifdef __cplusplus
 }
