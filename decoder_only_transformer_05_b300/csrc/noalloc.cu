@@ -9,6 +9,7 @@
 // the scratch in one fixed array that is part of the library's device image: it is
 // reserved when the library's device code is loaded on a GPU and stays reserved until the
 // process exits, on every GPU that loads it.
+#include <cuda.h>
 #include <cstdio>
 #include <mutex>
 
@@ -29,19 +30,46 @@ static __device__ __align__(256) float g_ln_scratch[kScratchFloats];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-float* g_scratch_ptr[kMaxDevices] = {};
+// Per device: the scratch address and the CUDA context it was looked up in. A device reset
+// (cudaDeviceReset) or a context made through the driver API gives the device another
+// context, in which the old address means nothing; the lookup is then made again.
+struct ScratchEntry { float* ptr; CUcontext ctx; };
+ScratchEntry g_scratch[kMaxDevices] = {};
+
+// cuCtxGetCurrent from the driver, looked up once through the runtime (no -lcuda).
+CUresult (*ctx_get_current())(CUcontext*) {
+  static CUresult (*fn)(CUcontext*) = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CUresult (*)(CUcontext*)>(f);
+  });
+  return fn;
+}
 
 // Device address of g_ln_scratch on the current device. In host code the symbol itself
 // is only a host-side handle, so the address is looked up with cudaGetSymbolAddress,
-// once per device, while that device is current.
+// once per device (and again after that device's context changed), while that device is
+// current.
 int scratch_on_current_device(float** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return gpt2_set_error(GPT2_ERR_CUDA, cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices)
     return gpt2_set_error(GPT2_ERR_ARG, "device index beyond the scratch table");
+  // the current context (null before the runtime has made the device's context; the
+  // lookup below makes it, and the entry records the context it ran in)
+  CUcontext ctx = nullptr;
+  auto get = ctx_get_current();
+  if (!get || get(&ctx) != CUDA_SUCCESS)
+    return gpt2_set_error(GPT2_ERR_CUDA, "cuCtxGetCurrent is not available");
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  ScratchEntry& ent = g_scratch[dev];
+  if (!ent.ptr || ent.ctx != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_ln_scratch);
     if (e != cudaSuccess) {
@@ -50,9 +78,11 @@ int scratch_on_current_device(float** out) {
                cudaGetErrorString(e));
       return gpt2_set_error(GPT2_ERR_CUDA, msg);
     }
-    g_scratch_ptr[dev] = static_cast<float*>(p);
+    if (get(&ctx) != CUDA_SUCCESS) return gpt2_set_error(GPT2_ERR_CUDA, "cuCtxGetCurrent failed");
+    ent.ptr = static_cast<float*>(p);
+    ent.ctx = ctx;
   }
-  *out = g_scratch_ptr[dev];
+  *out = ent.ptr;
   return GPT2_OK;
 }
 

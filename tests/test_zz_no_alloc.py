@@ -57,21 +57,18 @@ def _run(prec, M, C, seed, noalloc, scale=0.5):
     return dres.float().cpu().numpy(), dw.cpu().numpy(), db.cpu().numpy()
 
 
-def _rel_inf(a, r):
-    return float(np.abs(a - r).max() / max(np.abs(r).max(), 1e-30))
-
-
 # the GPT-2 124M rows (B=12, T=1024, C=768), a ragged row count, and the fp32 path
 @pytest.mark.parametrize("prec,M,C", [("bf16", 12288, 768), ("bf16", 4133, 1024),
                                       ("fp32", 1000, 384)])
 def test_noalloc_matches_caller_scratch_on_two_calls(prec, M, C):
-    tol = 1e-2 if prec == "bf16" else 1e-5     # the LayerNorm parity tests' bounds
+    # Both entry points run the same kernels with the same fixed summation order, so the
+    # results must agree bit for bit; a tolerance could hide partial sums left over from
+    # the previous call in the shared array.
     for seed in (1, 2):                          # two calls in a row, different inputs
         want = _run(prec, M, C, seed, noalloc=False)
         got = _run(prec, M, C, seed, noalloc=True)
-        assert _rel_inf(got[0], want[0]) <= tol
-        assert _rel_inf(got[1], want[1]) <= 1e-4
-        assert _rel_inf(got[2], want[2]) <= 1e-4
+        for g, w_ in zip(got, want):
+            assert np.array_equal(g, w_)
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
