@@ -142,35 +142,6 @@ __global__ void attn_bwd_dkv_f32_kernel(float* __restrict__ dqkv, const float* _
   }
 }
 
-// =====================================================================================
-// bf16 path, head size 64: D for the tensor-core backward (attention_tc.cu)
-namespace fa {
-
-constexpr int D = 64;
-
-// D_i = dO_i . O_i, one thread per (b, h, t), t fastest: each thread reads one 128-byte row
-// slice of dO and of O, and the writes to D [B, H, T] are contiguous across the warp
-__global__ void bwd_D_kernel(float* __restrict__ Dbuf, const bf16* __restrict__ dout,
-                             const bf16* __restrict__ out, int B, int T, int C, int H) {
-  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (long long)B * T * H) return;
-  const int t = (int)(i % T);
-  const long long bh = i / T;
-  const int h = (int)(bh % H), b = (int)(bh / H);
-  const size_t bt = (size_t)b * T + t;
-  const bf16* a = dout + bt * C + h * D;
-  const bf16* c = out + bt * C + h * D;
-  float s = 0.f;
-#pragma unroll
-  for (int k = 0; k < D; k += 8) {
-    Vec16<bf16> x = ld16(a + k), y = ld16(c + k);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) s += to_f32(x.e[e]) * to_f32(y.e[e]);
-  }
-  Dbuf[i] = s;
-}
-
-}  // namespace fa
 
 // =====================================================================================
 cudaError_t attention_forward(DType t, void* out, float* lse, const void* qkv, int B, int T, int C,
@@ -186,13 +157,8 @@ cudaError_t attention_backward(DType t, void* dqkv, float* Dbuf, const void* dou
                                const void* out, const void* qkv, const float* lse, int B, int T,
                                int C, int H, int* err, cudaStream_t s) {
   if (t == DType::BF16) {
-    if (C / H != fa::D || C % H || T % 4) return cudaErrorInvalidValue;
-    long long n = (long long)B * T * H;
-    fa::bwd_D_kernel<<<ceil_div(n, 256), 256, 0, s>>>(Dbuf, (const bf16*)dout, (const bf16*)out,
-                                                      B, T, C, H); count_launches(1);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return attention_backward_tc(dqkv, Dbuf, dout, qkv, lse, B, T, C, H, err, s);
+    if (C / H != 64 || C % H || T % 4) return cudaErrorInvalidValue;
+    return attention_backward_tc(dqkv, Dbuf, dout, out, qkv, lse, B, T, C, H, err, s);
   }
   long long warps = (long long)B * H * T;
   int blocks = ceil_div(warps, 4);

@@ -22,10 +22,11 @@
 //   tensor memory when it does. The two tiles' softmax warps run side by side and share
 //   every K, V tile; K and V have rings of their own, P is double-buffered per tile, and the
 //   MMA thread issues whichever S or P V group is ready (non-blocking probes).
-// Backward (D = rowsum(dO * O) from a separate kernel; P = exp2(s sl2 - lse log2 e)):
-//   dK/dV unit = (batch, head, 128 keys): S^T = K Q_i^T, dP^T = V dO_i^T, then
-//   dV += P^T dO_i, dK += dS^T Q_i with dS = P (dP - D); dQ unit = (batch, head, 128
-//   queries): S = Q K_j^T, dP = dO V_j^T, dQ += dS K_j. Each output row belongs to one
+// Backward (P = exp2(s sl2 - lse log2 e), D = rowsum(dO * O)): the dQ kernel runs first;
+//   its unit = (batch, head, 128 queries) loads Q, dO and O, computes D for its rows (and
+//   writes it for the dK/dV kernel), then S = Q K_j^T, dP = dO V_j^T, dQ += dS K_j with
+//   dS = P (dP - D). The dK/dV unit = (batch, head, 128 keys): S^T = K Q_i^T,
+//   dP^T = V dO_i^T, then dV += P^T dO_i, dK += dS^T Q_i. Each output row belongs to one
 //   unit, so the result is deterministic. The eight elementwise warps split the columns
 //   (warps w and w + 4 take 64 each): no row reduction is needed once lse and D are known.
 //   P^T, dS^T (dK/dV) and dS (dQ, double-buffered) go back into tensor memory as bf16 pairs
@@ -81,7 +82,7 @@ __device__ __forceinline__ void stage_row32(uint32_t slice, int r, const float* 
 struct Params {
   int B, T, H, C, nqb, units;
   float* lse;            // forward output, backward input [B, H, T]
-  const float* Dbuf;     // backward: rowsum(dO * O) [B, H, T]
+  float* Dbuf;           // backward: rowsum(dO * O) [B, H, T], written by the dQ kernel
   int* err;
 };
 
@@ -93,30 +94,36 @@ struct Bars {
 
 // =====================================================================================
 // forward
-//   shared memory: Q_A, Q_B | K ring (2) | V ring (2) | P_A[2], P_B[2] (double-buffered,
-//   so block j's P is written while P V of block j - 1 still reads the other buffer)
-constexpr int F_RING = 2;
-constexpr int F_SM_Q = 0;                                  // A, B
-constexpr int F_SM_K = F_SM_Q + 2 * TILE;                  // K ring
+//   unit = (batch, head, query tiles A = 2 pair and B = 2 pair + 1 of 128 queries each);
+//   keys in blocks of 128.
+//   shared memory: Q_A, Q_B of two units (double-buffered: the next unit's queries load while
+//   this one runs) | K ring | V ring | output staging (8 warps x 32 rows x 128 B)
+//   tensor memory: S_A, S_B (fp32, 128 columns each) | P_A, P_B (bf16 pairs, 64 columns
+//   each: the A operand of O += P V, read by the MMA from tensor memory) | O_A, O_B (fp32)
+constexpr int F_RING = 4;
+constexpr int F_SM_Q = 0;                                  // [buf][tile]
+constexpr int F_SM_K = F_SM_Q + 4 * TILE;                  // K ring
 constexpr int F_SM_V = F_SM_K + F_RING * TILE;             // V ring
-constexpr int F_SM_P = F_SM_V + F_RING * TILE;             // [tile][buf]: two 64-key halves
-constexpr int F_SM_BAR = F_SM_P + 4 * 2 * TILE;
-constexpr int F_SMEM = F_SM_BAR + 256 + 1024;
+constexpr int F_SM_STG = F_SM_V + F_RING * TILE;           // 8 warps x 4 KB
+constexpr int F_SM_BAR = F_SM_STG + 8 * 4096;
+constexpr int F_SMEM = F_SM_BAR + 512 + 1024;
+constexpr uint32_t F_COL_S = 0, F_COL_P = 256, F_COL_O = 384;
 enum {
-  FB_QFULL = 0,
-  FB_QEMPTY = 1,
-  FB_KFULL = 2,              // [2]
-  FB_KEMPTY = 4,             // [2]
-  FB_VFULL = 6,              // [2]
-  FB_VEMPTY = 8,             // [2]
-  FB_SFULL = 10,             // [tile]
-  FB_SEMPTY = 12,            // [tile]
-  FB_PFULL = 14,             // [tile][buf]
-  FB_ODONE = 18,             // [tile][buf]
-  FB_OFREE = 22,             // [tile]
-  FB_FINAL = 24,
-  FB_COUNT = 25
+  FB_QFULL = 0,                  // [buf]
+  FB_QEMPTY = 2,                 // [buf]
+  FB_KFULL = 4,                  // [F_RING]
+  FB_KEMPTY = FB_KFULL + F_RING,
+  FB_VFULL = FB_KEMPTY + F_RING,
+  FB_VEMPTY = FB_VFULL + F_RING,
+  FB_SFULL = FB_VEMPTY + F_RING,   // [tile]: S_x computed
+  FB_SEMPTY = FB_SFULL + 2,        // [tile]: S_x read out by the tile's four softmax warps
+  FB_PFULL = FB_SEMPTY + 2,        // [tile]: P_x written
+  FB_ODONE = FB_PFULL + 2,         // [tile]: O_x += P_x V done (P_x free, O_x stable)
+  FB_OFREE = FB_ODONE + 2,         // [tile]: the unit's O_x read out
+  FB_FINAL = FB_OFREE + 2,
+  FB_COUNT
 };
+static_assert(8 * FB_COUNT + 16 <= 512, "forward barrier area");
 
 struct FwdUnit {
   int b, h, qa, nA, nB;      // tile A = query block qa, tile B = qa + 1 (nB = 0: absent)
@@ -133,7 +140,11 @@ __device__ __forceinline__ FwdUnit fwd_unit(const Params& p, int u) {
   return w;
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+// 11 warps: warp 0 TMA producer, warp 1 + x the MMA issuer of query tile x (each tile's
+// chain of S, softmax and P V then never waits on the other tile's), warps 3..10 softmax
+constexpr int F_THREADS = 352;
+
+__global__ void __launch_bounds__(F_THREADS, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_out,
            const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -146,24 +157,25 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(FB_QFULL), 1);
-    mbar_init(bar(FB_QEMPTY), 1);
+    // Q, K and V stages are released by both MMA issuers (one commit each)
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(FB_QFULL + i), 1);
+      mbar_init(bar(FB_QEMPTY + i), 2);
+    }
     for (int s = 0; s < F_RING; ++s) {
       mbar_init(bar(FB_KFULL + s), 1);
-      mbar_init(bar(FB_KEMPTY + s), 1);
+      mbar_init(bar(FB_KEMPTY + s), 2);
       mbar_init(bar(FB_VFULL + s), 1);
-      mbar_init(bar(FB_VEMPTY + s), 1);
+      mbar_init(bar(FB_VEMPTY + s), 2);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(FB_SFULL + x), 1);
       mbar_init(bar(FB_SEMPTY + x), 4);
+      mbar_init(bar(FB_PFULL + x), 4);
+      mbar_init(bar(FB_ODONE + x), 1);
       mbar_init(bar(FB_OFREE + x), 4);
-      for (int bf = 0; bf < 2; ++bf) {
-        mbar_init(bar(FB_PFULL + 2 * x + bf), 4);
-        mbar_init(bar(FB_ODONE + 2 * x + bf), 1);
-      }
     }
-    mbar_init(bar(FB_FINAL), 1);
+    mbar_init(bar(FB_FINAL), 2);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -175,151 +187,144 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot_ptr;
-  // TMEM: S_A [0,128), S_B [128,256), O_A [256,320), O_B [320,384)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer: Q per unit, then K_j, V_j on their own rings
+      // ---------------- TMA producer: Q_A, Q_B per unit (double-buffered), then K_j, V_j on
+      // their rings
       bool ok = true;
       int uc = 0, kv = 0;
+      int nq = 0, nk = 0, nv = 0;   // copies issued per barrier (what an abort waits for)
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
         const FwdUnit w = fwd_unit(p, u);
-        if (uc >= 1 && !mbar_wait(bar(FB_QEMPTY), par(uc - 1), abort_flag, p.err)) {
+        const int qb = uc & 1;
+        if (uc >= 2 && !mbar_wait(bar(FB_QEMPTY + qb), par((uc >> 1) - 1), abort_flag, p.err)) {
           ok = false;
           break;
         }
-        mbar_expect_tx(bar(FB_QFULL), (w.nB ? 2 : 1) * TILE);
-        tma_load_3d(base + F_SM_Q, &tm_qkv, bar(FB_QFULL), w.h * D, w.qa * BQ, w.b);
+        ++nq;
+        const uint32_t qdst = base + F_SM_Q + 2 * qb * TILE;
+        mbar_expect_tx(bar(FB_QFULL + qb), (w.nB ? 2 : 1) * TILE);
+        tma_load_3d(qdst, &tm_qkv, bar(FB_QFULL + qb), w.h * D, w.qa * BQ, w.b);
         if (w.nB)
-          tma_load_3d(base + F_SM_Q + TILE, &tm_qkv, bar(FB_QFULL), w.h * D, (w.qa + 1) * BQ, w.b);
+          tma_load_3d(qdst + TILE, &tm_qkv, bar(FB_QFULL + qb), w.h * D, (w.qa + 1) * BQ, w.b);
         const int nkv = w.nB ? w.nB : w.nA;
         for (int j = 0; j < nkv && ok; ++j, ++kv) {
           const int s = kv % F_RING;
           const uint32_t ph = par(kv / F_RING) ^ 1u;
           if (!mbar_wait(bar(FB_KEMPTY + s), ph, abort_flag, p.err)) { ok = false; break; }
+          ++nk;
           mbar_expect_tx(bar(FB_KFULL + s), TILE);
           tma_load_3d(base + F_SM_K + s * TILE, &tm_qkv, bar(FB_KFULL + s), p.C + w.h * D, j * BKV, w.b);
-          if (!mbar_wait(bar(FB_VEMPTY + s), ph, abort_flag, p.err)) { ok = false; ++kv; break; }
+          if (!mbar_wait(bar(FB_VEMPTY + s), ph, abort_flag, p.err)) { ok = false; break; }
+          ++nv;
           mbar_expect_tx(bar(FB_VFULL + s), TILE);
           tma_load_3d(base + F_SM_V + s * TILE, &tm_qkv, bar(FB_VFULL + s), 2 * p.C + w.h * D, j * BKV, w.b);
         }
       }
       if (!ok) {   // let issued copies land before the block leaves
-        if (uc >= 0) mbar_wait(bar(FB_QFULL), par(uc), abort_flag, nullptr, false);
-        for (int k = max(0, kv - F_RING); k < kv; ++k) {
+        for (int i = max(0, nq - 2); i < nq; ++i)
+          mbar_wait(bar(FB_QFULL + (i & 1)), par(i >> 1), abort_flag, nullptr, false);
+        for (int k = max(0, nk - F_RING); k < nk; ++k)
           mbar_wait(bar(FB_KFULL + k % F_RING), par(k / F_RING), abort_flag, nullptr, false);
+        for (int k = max(0, nv - F_RING); k < nv; ++k)
           mbar_wait(bar(FB_VFULL + k % F_RING), par(k / F_RING), abort_flag, nullptr, false);
-        }
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer: issues whichever of S_A, S_B, P_A V, P_B V is ready
-      // (non-blocking probes), so one tile's slower step never holds up the other's.
-      constexpr uint32_t IDESC_S = make_idesc(BQ, BKV, false, false);
-      constexpr uint32_t IDESC_O = make_idesc(BQ, D, false, true);
-      // descriptors of the tiles' first 16 columns; a k step adds (bytes >> 4)
-      const uint64_t dq0 = sdesc(base + F_SM_Q, 16, 1024);
-      const uint64_t dk0 = sdesc(base + F_SM_K, 16, 1024);
-      const uint64_t dv0 = sdesc(base + F_SM_V, 16384, 1024);
-      const uint64_t dp0 = sdesc(base + F_SM_P, 16, 1024);
-      constexpr uint64_t TILE16 = TILE >> 4;
-      bool ok = true;
-      int uc = 0, kvb = 0;               // units done; K/V blocks consumed so far
-      int gs[2] = {0, 0}, gp[2] = {0, 0}, uo[2] = {0, 0};
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
-        const FwdUnit w = fwd_unit(p, u);
-        const int n[2] = {w.nA, w.nB};
-        const int nkv = w.nB ? w.nB : w.nA;
-        int si[2] = {0, 0}, pi[2] = {0, 0};   // next S / P V block per tile in this unit
-        int kr = 0, vr = 0;                    // K / V blocks released so far
-        bool qready = false, qfreed = false;
-        unsigned long long t_last = globaltimer();
-        while (ok) {
-          bool progress = false;
-          if (!qready) qready = mbar_test(bar(FB_QFULL), par(uc));
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            // S_x(j) = Q_x K_j^T: needs Q, K_j, and the tile's S buffer drained
-            const int j = si[x];
-            if (qready && j < n[x]) {
-              const int kb = kvb + j;
-              if (mbar_test(bar(FB_KFULL + kb % F_RING), par(kb / F_RING)) &&
-                  (gs[x] == 0 || mbar_test(bar(FB_SEMPTY + x), par(gs[x] - 1)))) {
-                tc_fence_after();
-                const uint64_t a = dq0 + x * TILE16, bk = dk0 + (kb % F_RING) * TILE16;
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k)
-                  umma_bf16(tmem + x * BKV, a + 2 * k, bk + 2 * k, IDESC_S, k > 0 ? 1u : 0u);
-                umma_commit(bar(FB_SFULL + x));
-                ++si[x];
-                ++gs[x];
-                progress = true;
-              }
-            }
-            // P_x(j) V_j: needs P_x(j) written, V_j, and (first block) O_x read out
-            const int jp = pi[x];
-            if (jp < si[x]) {
-              const int vb = kvb + jp, bf = gp[x] & 1;
-              if (mbar_test(bar(FB_VFULL + vb % F_RING), par(vb / F_RING)) &&
-                  mbar_test(bar(FB_PFULL + 2 * x + bf), par(gp[x] >> 1)) &&
-                  (jp > 0 || uo[x] == 0 || mbar_test(bar(FB_OFREE + x), par(uo[x] - 1)))) {
-                tc_fence_after();
-                const uint64_t a = dp0 + (2 * x + bf) * 2 * TILE16;
-                const uint64_t bv = dv0 + (vb % F_RING) * TILE16;
-#pragma unroll
-                for (int k = 0; k < BKV / 16; ++k)
-                  umma_bf16(tmem + 256 + x * D, a + (k >> 2) * TILE16 + 2 * (k & 3), bv + 128 * k,
-                            IDESC_O, (jp > 0 || k > 0) ? 1u : 0u);
-                umma_commit(bar(FB_ODONE + 2 * x + bf));
-                ++pi[x];
-                ++gp[x];
-                progress = true;
-              }
-            }
-          }
-          // release K_j once every tile that needs it has issued S(j); V_j likewise for P V
-          while (kr < nkv && (si[0] > kr || kr >= n[0]) && (si[1] > kr || kr >= n[1])) {
-            umma_commit(bar(FB_KEMPTY + (kvb + kr) % F_RING));
-            ++kr;
-          }
-          while (vr < nkv && (pi[0] > vr || vr >= n[0]) && (pi[1] > vr || vr >= n[1])) {
-            umma_commit(bar(FB_VEMPTY + (kvb + vr) % F_RING));
-            ++vr;
-          }
-          if (!qfreed && si[0] == n[0] && si[1] == n[1]) {
-            // the unit's last S MMAs are issued: Q can be refilled once they complete
-            umma_commit(bar(FB_QEMPTY));
-            qfreed = true;
-          }
-          if (pi[0] == n[0] && pi[1] == n[1]) break;
-          if (progress) {
-            t_last = globaltimer();
-          } else if (*abort_flag) {
-            ok = false;
-          } else if (globaltimer() - t_last > TIMEOUT_NS) {
-            *abort_flag = 1;
-            if (p.err) atomicOr(p.err, DEV_ERR_TIMEOUT);
-            ok = false;
-          }
-        }
-        if (!ok) break;
-        kvb += nkv;
-        ++uo[0];
-        if (w.nB) ++uo[1];
+  } else if (warp <= 2) {
+    // ---------------- MMA issuer of tile x (the whole warp runs the loop; one elected lane
+    // issues), per key block j: S_x(j) = Q_x K_j^T, then O_x += P_x(j-1) V_{j-1} (P_x read
+    // from tensor memory). Every K, V and Q stage gets one release commit from each issuer,
+    // also for blocks this tile does not use.
+    const int x = warp - 1;
+    // every lane waits; the result is made warp-uniform so the lanes never diverge
+    auto wait_u = [&](uint32_t b, uint32_t ph) {
+      return __all_sync(0xffffffffu, mbar_wait(b, ph, abort_flag, p.err));
+    };
+    constexpr uint32_t IDESC_S = make_idesc(BQ, BKV, false, false);
+    constexpr uint32_t IDESC_O = make_idesc(BQ, D, false, true);
+    bool ok = true;
+    int uc = 0, kv = 0, gs = 0, gp = 0, uo = 0;
+    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
+      const FwdUnit w = fwd_unit(p, u);
+      const int n = x == 0 ? w.nA : w.nB;
+      const int nkv = w.nB ? w.nB : w.nA;
+      const int qb = uc & 1;
+      if (n > 0 && !wait_u(bar(FB_QFULL + qb), par(uc >> 1))) {
+        ok = false;
+        break;
       }
+      const uint64_t qd = sdesc(base + F_SM_Q + (2 * qb + x) * TILE, 16, 1024);
+      for (int j = 0; j <= nkv && ok; ++j) {
+        if (j < nkv) {
+          const int kb = kv + j, s = kb % F_RING;
+          if (j < n) {
+            // S_x's columns are free once the softmax warps have read the previous S_x
+            if (!wait_u(bar(FB_KFULL + s), par(kb / F_RING)) ||
+                (gs > 0 && !wait_u(bar(FB_SEMPTY + x), par(gs - 1)))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t kd = sdesc(base + F_SM_K + s * TILE, 16, 1024);
+            if (elect_one()) {
+#pragma unroll
+              for (int k = 0; k < D / 16; ++k)   // a k step of 16 columns adds 32 bytes (2 units)
+                umma_bf16(tmem + F_COL_S + x * BKV, qd + 2 * k, kd + 2 * k, IDESC_S, k > 0 ? 1u : 0u);
+              umma_commit(bar(FB_SFULL + x));
+            }
+            __syncwarp();
+            ++gs;
+          }
+          if (elect_one()) {
+            umma_commit(bar(FB_KEMPTY + s));
+            if (j == nkv - 1) umma_commit(bar(FB_QEMPTY + qb));
+          }
+          __syncwarp();
+        }
+        if (j >= 1) {
+          const int jp = j - 1, vb = kv + jp, s = vb % F_RING;
+          if (jp < n) {
+            if (!wait_u(bar(FB_VFULL + s), par(vb / F_RING)) ||
+                !wait_u(bar(FB_PFULL + x), par(gp)) ||
+                (jp == 0 && uo > 0 && !wait_u(bar(FB_OFREE + x), par(uo - 1)))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t vd = sdesc(base + F_SM_V + s * TILE, 16384, 1024);
+            if (elect_one()) {
+#pragma unroll
+              for (int k = 0; k < BKV / 16; ++k)   // a k step of 16 keys adds 2048 bytes
+                umma_bf16_ts(tmem + F_COL_O + x * D, tmem + F_COL_P + x * 64 + k * 8, vd + 128 * k,
+                             IDESC_O, (jp > 0 || k > 0) ? 1u : 0u);
+              umma_commit(bar(FB_ODONE + x));
+            }
+            __syncwarp();
+            ++gp;
+          }
+          if (elect_one()) umma_commit(bar(FB_VEMPTY + s));
+          __syncwarp();
+        }
+      }
+      if (!ok) break;
+      kv += nkv;
+      if (n > 0) ++uo;
+    }
+    if (elect_one()) {
       umma_commit(bar(FB_FINAL));
       mbar_wait(bar(FB_FINAL), 0, abort_flag, nullptr, false);
     }
+    __syncwarp();
   } else {
-    // ---------------- softmax: tile x = 0 (warps 2..5) or 1 (warps 6..9)
-    const int x = (warp - 2) >> 2, q = warp & 3;
+    // ---------------- softmax: tile x = 0 (warps 3..6) or 1 (warps 7..10); thread = query row
+    const int x = (warp - 3) >> 2, q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    const uint32_t s_col = x * BKV, o_col = 256 + x * D;
+    const uint32_t s_col = F_COL_S + x * BKV, p_col = F_COL_P + x * 64, o_col = F_COL_O + x * D;
+    const uint32_t slice = base + F_SM_STG + (warp - 3) * 4096;
     const float sl2 = rsqrtf((float)D) * LOG2E;
     int g = 0;                                          // S / P blocks of this tile so far
-    int last_buf = 0;                                   // P buffer holding the last output staging
     bool ok = true;
     for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
       const FwdUnit w = fwd_unit(p, u);
@@ -332,8 +337,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
         ok = mbar_wait(bar(FB_SFULL + x), par(g), abort_flag, p.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        // the block's score row (one TMEM round trip) and its maximum (causal mask on
-        // the diagonal block only)
+        // the block's score row (one tensor-memory round trip), then its maximum (causal
+        // mask on the diagonal block only) in eight independent chains
         const bool diag = (j == qblk);
         uint32_t sr[4][32];
 #pragma unroll
@@ -342,7 +347,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(FB_SEMPTY + x));
-        // eight independent partial maxima (no 128-long dependency chain)
         float mxp[8];
 #pragma unroll
         for (int t = 0; t < 8; ++t) mxp[t] = -INFINITY;
@@ -366,20 +370,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
           alpha = fast_exp2(m - mx);
           m = mx;
         }
-        // P buffer g & 1 was last read by P V of block g - 2
-        const int bf = g & 1;
-        if (g >= 2) {
-          ok = mbar_wait(bar(FB_ODONE + 2 * x + bf), par((g - 2) >> 1), abort_flag, p.err);
+        // P_x and O_x are free once the previous O_x += P_x V has completed (it was issued
+        // when this tile's previous P was written, so it has had the S wait, the load and the
+        // maximum to run)
+        if (g >= 1) {
+          ok = mbar_wait(bar(FB_ODONE + x), par(g - 1), abort_flag, p.err);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
         }
-        if (lane == 0) bulk_wait_read();   // an output store may still read this warp's slice
-        __syncwarp();
-        const uint32_t p_tile = base + F_SM_P + (2 * x + bf) * 2 * TILE;
-        // P = exp2(s sl2 - m) as bf16, 32 keys at a time straight into the operand tile;
-        // the row sum in eight independent partials
-        float sp[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) sp[t] = 0.f;
+        // P = exp2(s sl2 - m) as bf16 pairs straight into tensor memory, 32 keys at a time;
+        // the row sum in four independent partials
+        float sp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
@@ -391,25 +392,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
               if (c * 32 + 2 * e > r) p0 = 0.f;
               if (c * 32 + 2 * e + 1 > r) p1 = 0.f;
             }
-            sp[(2 * e) & 7] += p0;
-            sp[(2 * e + 1) & 7] += p1;
+            sp[(2 * e) & 3] += p0;
+            sp[(2 * e + 1) & 3] += p1;
             pk[e] = pack2_bf16(p0, p1);
           }
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int unit = (c & 1) * 4 + v;
-            st_shared16(p_tile + (c >> 1) * TILE + r * 128 + ((unit ^ (r & 7)) << 4),
-                        make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]));
-          }
+          tmem_st16(lane_base + p_col + c * 16, pk);
         }
-        const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-        l = l * alpha + sum;
-        // a moved maximum rescales O in tensor memory, after the previous P V and
-        // before this block's
+        l = l * alpha + ((sp[0] + sp[1]) + (sp[2] + sp[3]));
+        // a moved maximum rescales O (which holds the sum up to the previous block)
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-          ok = mbar_wait(bar(FB_ODONE + 2 * x + (bf ^ 1)), par((g - 1) >> 1), abort_flag, p.err);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          tc_fence_after();
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
@@ -419,16 +410,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
             tmem_st32(lane_base + o_col + c * 32, o);
           }
-          tmem_wait_st();
         }
-        fence_proxy_async();
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(FB_PFULL + 2 * x + bf));
+        if (lane == 0) mbar_arrive(bar(FB_PFULL + x));
       }
       if (!ok) break;
-      // the unit's last P V (block g - 1) is done: O is final
-      ok = mbar_wait(bar(FB_ODONE + 2 * x + ((g - 1) & 1)), par((g - 1) >> 1), abort_flag, p.err);
+      // the unit's last O_x += P_x V is done: O is final
+      ok = mbar_wait(bar(FB_ODONE + x), par(g - 1), abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       uint32_t o[2][32];
@@ -438,10 +428,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(FB_OFREE + x));
-      // O / l through this warp's rows of the P buffer the last P V read (free now), one
-      // TMA store
-      last_buf = (g - 1) & 1;
-      const uint32_t slice = base + F_SM_P + (2 * x + last_buf) * 2 * TILE + q * 4096;
+      // O / l through this warp's staging slice (free once its previous store has read it),
+      // one TMA store of the warp's 32 rows
+      if (lane == 0) bulk_wait_read();
+      __syncwarp();
       stage_row64(slice, lane, reinterpret_cast<const float*>(o), 1.0f / l);
       fence_proxy_async();
       __syncwarp();
@@ -451,7 +441,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
       }
       if (query < p.T) p.lse[((size_t)w.b * p.H + w.h) * p.T + query] = (m + __log2f(l)) * LN2;
     }
-    (void)last_buf;
     if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
@@ -544,7 +533,7 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
-      int uc = 0, it = 0;
+      int uc = 0, it = 0, nkv = 0;   // nkv: K / V copies issued (what an abort waits for)
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
         int b, h, kb, n;
         dkv_unit(p, u, b, h, kb, n);
@@ -553,6 +542,7 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
           ok = false;
           break;
         }
+        ++nkv;
         const uint32_t kdst = base + K_SM_KV + kbuf * 2 * TILE;
         mbar_expect_tx(bar(KB_KVFULL + kbuf), 2 * TILE);
         tma_load_3d(kdst, &tm_qkv, bar(KB_KVFULL + kbuf), p.C + h * D, kb * BKV, b);
@@ -578,10 +568,8 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
         }
       }
       if (!ok) {
-        for (int i = 0; i < 2; ++i)
-          if (uc - i >= 0)
-            mbar_wait(bar(KB_KVFULL + ((uc - i) & 1)), par((uc - i) >> 1), abort_flag, nullptr,
-                      false);
+        for (int i = max(0, nkv - 2); i < nkv; ++i)
+          mbar_wait(bar(KB_KVFULL + (i & 1)), par(i >> 1), abort_flag, nullptr, false);
         for (int k = max(0, it - K_QD_STAGES); k < it; ++k)
           mbar_wait(bar(KB_QDFULL + k % K_QD_STAGES), par(k / K_QD_STAGES), abort_flag, nullptr,
                     false);
@@ -772,12 +760,13 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
 }
 
 // =====================================================================================
-// backward: dQ
+// backward: dQ (and D)
 constexpr int Q_KV_STAGES = 4;
 constexpr int Q_SM_QD = 0;                                   // [2 units]: Q, dO
 constexpr int Q_SM_KV = Q_SM_QD + 4 * TILE;                  // stage s: K at 2s, V at 2s+1
 constexpr int Q_SM_STG = Q_SM_KV + 2 * Q_KV_STAGES * TILE;   // 8 warps x 2 KB output staging
-constexpr int Q_SM_BAR = Q_SM_STG + TILE;
+constexpr int Q_SM_O = Q_SM_STG + TILE;                      // the unit's O rows (for D)
+constexpr int Q_SM_BAR = Q_SM_O + TILE;
 constexpr int Q_SMEM = Q_SM_BAR + 256 + 1024;
 enum {
   QB_QFULL = 0,     // [2]
@@ -790,6 +779,8 @@ enum {
   QB_DONE,          // [2]: one per dS buffer
   QB_ACCFREE = QB_DONE + 2,
   QB_FINAL,
+  QB_OFULL,
+  QB_OEMPTY,
   QB_COUNT
 };
 
@@ -805,7 +796,8 @@ __device__ __forceinline__ void dq_unit(const Params& p, int u, int& b, int& h, 
 // 10 warps: one SM sub-partition holds three of them, so at most 168 registers
 __global__ void __launch_bounds__(THREADS, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
-              const __grid_constant__ CUtensorMap tm_dqkv, const Params p) {
+              const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_dqkv,
+              const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -828,6 +820,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
     mbar_init(bar(QB_DONE + 1), 1);
     mbar_init(bar(QB_ACCFREE), 8);
     mbar_init(bar(QB_FINAL), 1);
+    mbar_init(bar(QB_OFULL), 1);
+    mbar_init(bar(QB_OEMPTY), 8);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -846,7 +840,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
-      int uc = 0, kv = 0;
+      int uc = 0, kv = 0, n_q = 0, n_o = 0;   // n_q, n_o: Q / dO and O copies issued
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
         int b, h, qb, n;
         dq_unit(p, u, b, h, qb, n);
@@ -855,10 +849,19 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
           ok = false;
           break;
         }
+        ++n_q;
         const uint32_t qdst = base + Q_SM_QD + qbuf * 2 * TILE;
         mbar_expect_tx(bar(QB_QFULL + qbuf), 2 * TILE);
         tma_load_3d(qdst, &tm_qkv, bar(QB_QFULL + qbuf), h * D, qb * BQ, b);
         tma_load_3d(qdst + TILE, &tm_do, bar(QB_QFULL + qbuf), h * D, qb * BQ, b);
+        // O rows of the unit (D), once the elementwise warps have read the previous unit's
+        if (uc >= 1 && !mbar_wait(bar(QB_OEMPTY), par(uc - 1), abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(bar(QB_OFULL), TILE);
+        tma_load_3d(base + Q_SM_O, &tm_o, bar(QB_OFULL), h * D, qb * BQ, b);
+        ++n_o;
         for (int j = 0; j < n; ++j, ++kv) {
           const int s = kv % Q_KV_STAGES;
           if (!mbar_wait(bar(QB_KVEMPTY + s), par(kv / Q_KV_STAGES) ^ 1u, abort_flag, p.err)) {
@@ -872,10 +875,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
         }
       }
       if (!ok) {
-        for (int i = 0; i < 2; ++i)
-          if (uc - i >= 0)
-            mbar_wait(bar(QB_QFULL + ((uc - i) & 1)), par((uc - i) >> 1), abort_flag, nullptr,
-                      false);
+        for (int i = max(0, n_q - 2); i < n_q; ++i)   // the last two units' Q / dO copies
+          mbar_wait(bar(QB_QFULL + (i & 1)), par(i >> 1), abort_flag, nullptr, false);
+        if (n_o > 0) mbar_wait(bar(QB_OFULL), par(n_o - 1), abort_flag, nullptr, false);
         for (int k = max(0, kv - Q_KV_STAGES); k < kv; ++k)
           mbar_wait(bar(QB_KVFULL + k % Q_KV_STAGES), par(k / Q_KV_STAGES), abort_flag, nullptr,
                     false);
@@ -946,18 +948,40 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     const uint32_t slice = base + Q_SM_STG + (warp - 2) * 2048;   // output staging
     const float sl2 = rsqrtf((float)D) * LOG2E;
-    int g = 0;
+    int g = 0, uc = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
       int b, h, qb, n;
       dq_unit(p, u, b, h, qb, n);
       const int query = qb * BQ + r;
-      float nlse2 = 0.f, Dr = 0.f;
-      if (query < p.T) {
-        const size_t t = ((size_t)b * p.H + h) * p.T + query;
-        nlse2 = -__ldg(p.lse + t) * LOG2E;
-        Dr = __ldg(p.Dbuf + t);
+      const size_t t = ((size_t)b * p.H + h) * p.T + query;
+      const float nlse2 = query < p.T ? -__ldg(p.lse + t) * LOG2E : 0.f;
+      // D = rowsum(dO * O) of this thread's query row, from the unit's dO and O tiles
+      // (rows past T were loaded as zeros); both warps of a row compute the same value
+      const int qbuf = uc & 1;
+      ok = mbar_wait(bar(QB_QFULL + qbuf), par(uc >> 1), abort_flag, p.err) &&
+           mbar_wait(bar(QB_OFULL), par(uc), abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      float Dr = 0.f;
+      {
+        const uint32_t drow = base + Q_SM_QD + (2 * qbuf + 1) * TILE + r * 128;
+        const uint32_t orow = base + Q_SM_O + r * 128;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint32_t off = (uint32_t)((v ^ (r & 7)) << 4);
+          const uint4 x = ld_shared16(drow + off), y = ld_shared16(orow + off);
+          const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 a = bf2_to_f2(xs[e]), c = bf2_to_f2(ys[e]);
+            Dr = fmaf(a.x, c.x, Dr);
+            Dr = fmaf(a.y, c.y, Dr);
+          }
+        }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(QB_OEMPTY));
+      if (half == 0 && query < p.T) p.Dbuf[t] = Dr;
       for (int j = 0; j < n; ++j, ++g) {
         ok = mbar_wait(bar(QB_SFULL), par(g), abort_flag, p.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -1090,12 +1114,12 @@ cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, 
   p.units = B * H * ((p.nqb + 1) / 2);
   p.lse = lse; p.Dbuf = nullptr; p.err = err;
   const int grid = std::min(p.units, num_sms());
-  fwd_kernel<<<grid, THREADS, F_SMEM, s>>>(mq, mo, p);
+  fwd_kernel<<<grid, F_THREADS, F_SMEM, s>>>(mq, mo, p);
   count_launches(1);
   return cudaGetLastError();
 }
 
-cudaError_t attention_backward_tc(void* dqkv, const float* Dbuf, const void* dout,
+cudaError_t attention_backward_tc(void* dqkv, float* Dbuf, const void* dout, const void* out,
                                   const void* qkv, const float* lse, int B, int T, int C, int H,
                                   int* err, cudaStream_t s) {
   using namespace fatc;
@@ -1111,9 +1135,10 @@ cudaError_t attention_backward_tc(void* dqkv, const float* Dbuf, const void* dou
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  CUtensorMap mq, md, mg;
+  CUtensorMap mq, md, mo, mg;
   if (!map_btw(&mq, qkv, B, T, 3 * C, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !map_btw(&md, dout, B, T, C, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !map_btw(&mo, out, B, T, C, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !map_btw(&mg, dqkv, B, T, 3 * C, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   Params p;
@@ -1121,11 +1146,12 @@ cudaError_t attention_backward_tc(void* dqkv, const float* Dbuf, const void* dou
   p.units = B * H * p.nqb;
   p.lse = const_cast<float*>(lse); p.Dbuf = Dbuf; p.err = err;
   const int grid = std::min(p.units, num_sms());
-  bwd_dkv_kernel<<<grid, THREADS, K_SMEM, s>>>(mq, md, mg, p);
+  // dQ first: it computes D = rowsum(dO * O), which the dK/dV kernel reads
+  bwd_dq_kernel<<<grid, THREADS, Q_SMEM, s>>>(mq, md, mo, mg, p);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  bwd_dq_kernel<<<grid, THREADS, Q_SMEM, s>>>(mq, md, mg, p);
+  bwd_dkv_kernel<<<grid, THREADS, K_SMEM, s>>>(mq, md, mg, p);
   count_launches(1);
   return cudaGetLastError();
 }

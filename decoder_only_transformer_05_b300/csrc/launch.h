@@ -60,6 +60,11 @@ cudaError_t splitk_reduce(float* accum, const float* ws, int splits, long long n
 // accum += sum_s ws[s] (fixed order), then ws = 0: folds deferred split-K partials.
 cudaError_t splitk_fold(float* accum, float* ws, int splits, long long n, cudaStream_t s);
 int gemm_tc_num_sms();
+// Test hook of the bounded waits: later GEMM launches use wait_limit_ns (<= 0: the default
+// 2 s) as every wait's limit, and with drop_first_signal the first accumulator of each
+// block pair is never signalled ready (its epilogue wait runs out and reports
+// DEV_ERR_TIMEOUT).
+void gemm_tc_debug_waits(long long wait_limit_ns, int drop_first_signal);
 
 // ---------------------------------------------------------------- elementwise
 cudaError_t encoder_forward(DType t, void* x, const int* tokens, const void* wte, const void* wpe,
@@ -118,12 +123,13 @@ cudaError_t attention_forward(DType t, void* out, float* lse, const void* qkv, i
                               int H, int* err, cudaStream_t s);
 cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, int T, int C,
                                  int H, int* err, cudaStream_t s);
-// dout [B, T, C] -> dqkv [B, T, 3C]; Dbuf [B, H, T] scratch. The bf16 path runs D =
-// rowsum(dout * out) and then the tcgen05 dK/dV and dQ kernels (needs T % 4 == 0).
+// dout [B, T, C] -> dqkv [B, T, 3C]; Dbuf [B, H, T] scratch. The bf16 path runs the tcgen05
+// dQ kernel (which also computes D = rowsum(dout * out) into Dbuf) and then the dK/dV
+// kernel (needs T % 4 == 0).
 cudaError_t attention_backward(DType t, void* dqkv, float* Dbuf, const void* dout,
                                const void* out, const void* qkv, const float* lse, int B, int T,
                                int C, int H, int* err, cudaStream_t s);
-cudaError_t attention_backward_tc(void* dqkv, const float* Dbuf, const void* dout,
+cudaError_t attention_backward_tc(void* dqkv, float* Dbuf, const void* dout, const void* out,
                                   const void* qkv, const float* lse, int B, int T, int C, int H,
                                   int* err, cudaStream_t s);
 

@@ -78,6 +78,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"((unsigned long long)map), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
 }
+// One lane of the (fully active) warp: true in exactly one lane. Lets a whole warp run an MMA
+// issuer loop in lockstep, so operand descriptors stay warp-uniform, while one lane issues.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
