@@ -576,66 +576,80 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t IDESC_S = make_idesc(BKV, BQ, false, false);
-      constexpr uint32_t IDESC_G = make_idesc(BKV, D, false, true);
-      bool ok = true;
-      int uc = 0, it = 0, gs = 0, gp = 0;
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
-        int b, h, kb, n;
-        dkv_unit(p, u, b, h, kb, n);
-        const int kbuf = uc & 1;
-        const uint32_t kt = base + K_SM_KV + kbuf * 2 * TILE, vt = kt + TILE;
-        if (!mbar_wait(bar(KB_KVFULL + kbuf), par(uc >> 1), abort_flag, p.err)) { ok = false; break; }
-        for (int i = 0; i <= n && ok; ++i) {
-          // S^T, dP^T of block i (one block ahead of dV, dK of block i - 1)
-          if (i < n) {
-            const int s = (it + i) % K_QD_STAGES;
-            if (!mbar_wait(bar(KB_QDFULL + s), par((it + i) / K_QD_STAGES), abort_flag, p.err) ||
-                (gs >= 1 && !mbar_wait(bar(KB_SEMPTY), par(gs - 1), abort_flag, p.err))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t qa = base + K_SM_QD + 2 * s * TILE, da = qa + TILE;
+    // ---------------- MMA issuer: the whole warp runs the loop (waits made warp-uniform, so
+    // the operand descriptors stay uniform) and one elected lane issues
+    auto wait_u = [&](uint32_t b, uint32_t ph) {
+      return __all_sync(0xffffffffu, mbar_wait(b, ph, abort_flag, p.err));
+    };
+    constexpr uint32_t IDESC_S = make_idesc(BKV, BQ, false, false);
+    constexpr uint32_t IDESC_G = make_idesc(BKV, D, false, true);
+    bool ok = true;
+    int uc = 0, it = 0, gs = 0, gp = 0;
+    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
+      int b, h, kb, n;
+      dkv_unit(p, u, b, h, kb, n);
+      const int kbuf = uc & 1;
+      const uint64_t kd = sdesc(base + K_SM_KV + kbuf * 2 * TILE, 16, 1024);
+      const uint64_t vd = kd + (TILE >> 4);
+      if (!wait_u(bar(KB_KVFULL + kbuf), par(uc >> 1))) { ok = false; break; }
+      for (int i = 0; i <= n && ok; ++i) {
+        // S^T, dP^T of block i (one block ahead of dV, dK of block i - 1)
+        if (i < n) {
+          const int s = (it + i) % K_QD_STAGES;
+          if (!wait_u(bar(KB_QDFULL + s), par((it + i) / K_QD_STAGES)) ||
+              (gs >= 1 && !wait_u(bar(KB_SEMPTY), par(gs - 1)))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t qd = sdesc(base + K_SM_QD + 2 * s * TILE, 16, 1024);
+          const uint64_t dd = qd + (TILE >> 4);
+          if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-              umma_bf16(tmem + COL_S, sdesc(kt + k * 32, 16, 1024), sdesc(qa + k * 32, 16, 1024),
-                        IDESC_S, k > 0 ? 1u : 0u);
-              umma_bf16(tmem + COL_DP, sdesc(vt + k * 32, 16, 1024), sdesc(da + k * 32, 16, 1024),
-                        IDESC_S, k > 0 ? 1u : 0u);
+            for (int k = 0; k < D / 16; ++k) {   // a k step of 16 columns adds 32 bytes
+              umma_bf16(tmem + COL_S, kd + 2 * k, qd + 2 * k, IDESC_S, k > 0 ? 1u : 0u);
+              umma_bf16(tmem + COL_DP, vd + 2 * k, dd + 2 * k, IDESC_S, k > 0 ? 1u : 0u);
             }
             umma_commit(bar(KB_SFULL));
-            ++gs;
           }
-          if (i >= 1) {
-            const int ib = i - 1, s = (it + ib) % K_QD_STAGES;
-            if (!mbar_wait(bar(KB_PFULL), par(gp), abort_flag, p.err) ||
-                (ib == 0 && uc >= 1 && !mbar_wait(bar(KB_ACCFREE), par(uc - 1), abort_flag, p.err))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t qa = base + K_SM_QD + 2 * s * TILE, da = qa + TILE;
+          __syncwarp();
+          ++gs;
+        }
+        if (i >= 1) {
+          const int ib = i - 1, s = (it + ib) % K_QD_STAGES;
+          if (!wait_u(bar(KB_PFULL), par(gp)) ||
+              (ib == 0 && uc >= 1 && !wait_u(bar(KB_ACCFREE), par(uc - 1)))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t qg = sdesc(base + K_SM_QD + 2 * s * TILE, 16384, 1024);
+          const uint64_t dg = qg + (TILE >> 4);
+          if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < BQ / 16; ++k) {
-              umma_bf16_ts(tmem + COL_DV, tmem + COL_PT + k * 8, sdesc(da + k * 2048, 16384, 1024),
-                           IDESC_G, (ib > 0 || k > 0) ? 1u : 0u);
-              umma_bf16_ts(tmem + COL_DK, tmem + COL_DST + k * 8, sdesc(qa + k * 2048, 16384, 1024),
-                           IDESC_G, (ib > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < BQ / 16; ++k) {   // a k step of 16 queries adds 2048 bytes
+              umma_bf16_ts(tmem + COL_DV, tmem + COL_PT + k * 8, dg + 128 * k, IDESC_G,
+                           (ib > 0 || k > 0) ? 1u : 0u);
+              umma_bf16_ts(tmem + COL_DK, tmem + COL_DST + k * 8, qg + 128 * k, IDESC_G,
+                           (ib > 0 || k > 0) ? 1u : 0u);
             }
             umma_commit(bar(KB_DONE));
             umma_commit(bar(KB_QDEMPTY + s));
-            ++gp;
           }
+          __syncwarp();
+          ++gp;
         }
-        if (!ok) break;
-        it += n;
-        umma_commit(bar(KB_KVEMPTY + kbuf));
       }
+      if (!ok) break;
+      it += n;
+      if (elect_one()) umma_commit(bar(KB_KVEMPTY + kbuf));
+      __syncwarp();
+    }
+    if (elect_one()) {
       umma_commit(bar(KB_FINAL));
       mbar_wait(bar(KB_FINAL), 0, abort_flag, nullptr, false);
     }
+    __syncwarp();
   } else {
     // ---------------- elementwise: key row r, query columns c0 .. c0 + 63
     const int q = warp & 3, half = (warp - 2) >> 2;
@@ -884,63 +898,76 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t IDESC_S = make_idesc(BQ, BKV, false, false);
-      constexpr uint32_t IDESC_G = make_idesc(BQ, D, false, true);
-      bool ok = true;
-      int uc = 0, kv = 0, gs = 0, gp = 0;
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
-        int b, h, qb, n;
-        dq_unit(p, u, b, h, qb, n);
-        const int qbuf = uc & 1;
-        const uint32_t qt = base + Q_SM_QD + qbuf * 2 * TILE, dt = qt + TILE;
-        if (!mbar_wait(bar(QB_QFULL + qbuf), par(uc >> 1), abort_flag, p.err)) { ok = false; break; }
-        for (int j = 0; j <= n && ok; ++j) {
-          if (j < n) {
-            const int s = (kv + j) % Q_KV_STAGES;
-            if (!mbar_wait(bar(QB_KVFULL + s), par((kv + j) / Q_KV_STAGES), abort_flag, p.err) ||
-                (gs >= 1 && !mbar_wait(bar(QB_SEMPTY), par(gs - 1), abort_flag, p.err))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t ka = base + Q_SM_KV + 2 * s * TILE, va = ka + TILE;
+    // ---------------- MMA issuer: the whole warp runs the loop (waits made warp-uniform, so
+    // the operand descriptors stay uniform) and one elected lane issues
+    auto wait_u = [&](uint32_t b, uint32_t ph) {
+      return __all_sync(0xffffffffu, mbar_wait(b, ph, abort_flag, p.err));
+    };
+    constexpr uint32_t IDESC_S = make_idesc(BQ, BKV, false, false);
+    constexpr uint32_t IDESC_G = make_idesc(BQ, D, false, true);
+    bool ok = true;
+    int uc = 0, kv = 0, gs = 0, gp = 0;
+    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uc) {
+      int b, h, qb, n;
+      dq_unit(p, u, b, h, qb, n);
+      const int qbuf = uc & 1;
+      const uint64_t qd = sdesc(base + Q_SM_QD + qbuf * 2 * TILE, 16, 1024);
+      const uint64_t dd = qd + (TILE >> 4);
+      if (!wait_u(bar(QB_QFULL + qbuf), par(uc >> 1))) { ok = false; break; }
+      for (int j = 0; j <= n && ok; ++j) {
+        if (j < n) {
+          const int s = (kv + j) % Q_KV_STAGES;
+          if (!wait_u(bar(QB_KVFULL + s), par((kv + j) / Q_KV_STAGES)) ||
+              (gs >= 1 && !wait_u(bar(QB_SEMPTY), par(gs - 1)))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t kd = sdesc(base + Q_SM_KV + 2 * s * TILE, 16, 1024);
+          const uint64_t vd = kd + (TILE >> 4);
+          if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-              umma_bf16(tmem + COL_S, sdesc(qt + k * 32, 16, 1024), sdesc(ka + k * 32, 16, 1024),
-                        IDESC_S, k > 0 ? 1u : 0u);
-              umma_bf16(tmem + COL_DP, sdesc(dt + k * 32, 16, 1024), sdesc(va + k * 32, 16, 1024),
-                        IDESC_S, k > 0 ? 1u : 0u);
+            for (int k = 0; k < D / 16; ++k) {   // a k step of 16 columns adds 32 bytes
+              umma_bf16(tmem + COL_S, qd + 2 * k, kd + 2 * k, IDESC_S, k > 0 ? 1u : 0u);
+              umma_bf16(tmem + COL_DP, dd + 2 * k, vd + 2 * k, IDESC_S, k > 0 ? 1u : 0u);
             }
             umma_commit(bar(QB_SFULL));
-            ++gs;
           }
-          if (j >= 1) {
-            const int jb = j - 1, s = (kv + jb) % Q_KV_STAGES;
-            if (!mbar_wait(bar(QB_PFULL), par(gp), abort_flag, p.err) ||
-                (jb == 0 && uc >= 1 && !mbar_wait(bar(QB_ACCFREE), par(uc - 1), abort_flag, p.err))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t ka = base + Q_SM_KV + 2 * s * TILE;
-            const uint32_t ds = tmem + COL_DS + (uint32_t)(gp & 1) * 64;
+          __syncwarp();
+          ++gs;
+        }
+        if (j >= 1) {
+          const int jb = j - 1, s = (kv + jb) % Q_KV_STAGES;
+          if (!wait_u(bar(QB_PFULL), par(gp)) ||
+              (jb == 0 && uc >= 1 && !wait_u(bar(QB_ACCFREE), par(uc - 1)))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t kg = sdesc(base + Q_SM_KV + 2 * s * TILE, 16384, 1024);
+          const uint32_t ds = tmem + COL_DS + (uint32_t)(gp & 1) * 64;
+          if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < BKV / 16; ++k)
-              umma_bf16_ts(tmem + COL_DQ, ds + k * 8, sdesc(ka + k * 2048, 16384, 1024), IDESC_G,
+            for (int k = 0; k < BKV / 16; ++k)   // a k step of 16 keys adds 2048 bytes
+              umma_bf16_ts(tmem + COL_DQ, ds + k * 8, kg + 128 * k, IDESC_G,
                            (jb > 0 || k > 0) ? 1u : 0u);
             umma_commit(bar(QB_DONE + (gp & 1)));
             umma_commit(bar(QB_KVEMPTY + s));
-            ++gp;
           }
+          __syncwarp();
+          ++gp;
         }
-        if (!ok) break;
-        kv += n;
-        umma_commit(bar(QB_QEMPTY + qbuf));
       }
+      if (!ok) break;
+      kv += n;
+      if (elect_one()) umma_commit(bar(QB_QEMPTY + qbuf));
+      __syncwarp();
+    }
+    if (elect_one()) {
       umma_commit(bar(QB_FINAL));
       mbar_wait(bar(QB_FINAL), 0, abort_flag, nullptr, false);
     }
+    __syncwarp();
   } else {
     // ---------------- elementwise: query row r, key columns c0 .. c0 + 63
     const int q = warp & 3, half = (warp - 2) >> 2;
