@@ -223,24 +223,29 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
   };
 
+  // Producer and MMA issuer loops run on whole warps: waits are made warp-uniform (so the
+  // coordinates and operand descriptors stay uniform) and one elected lane issues.
+  auto wait_u = [&](uint32_t b, uint32_t ph) {
+    return __all_sync(0xffffffffu, mbar_wait(b, ph, abort_flag, p.err, true, p.wait_ns));
+  };
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer (both blocks): this block's rows of A and its half
-      // of the B columns, completing on the even block's full barrier
-      int it = 0;
-      bool ok = true;
-      for (int unit = first; unit < units && ok; unit += stride) {
-        int mb, nb, sp;
-        decode(unit, mb, nb, sp);
-        const int m0 = mb * BM, n0 = nb * BN + (int)rank * (BN / 2);
-        const int kb0 = sp * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int s = it % Cf::STAGES;
-          const uint32_t ph = (uint32_t)(it / Cf::STAGES) & 1u;
-          if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, p.err, true, p.wait_ns)) { ok = false; break; }
-          const uint32_t a_dst = base + s * Cf::STAGE, b_dst = a_dst + Cf::A_BYTES;
+    // ---------------- TMA producer (both blocks): this block's rows of A and its half
+    // of the B columns, completing on the even block's full barrier
+    int it = 0;
+    bool ok = true;
+    for (int unit = first; unit < units && ok; unit += stride) {
+      int mb, nb, sp;
+      decode(unit, mb, nb, sp);
+      const int m0 = mb * BM, n0 = nb * BN + (int)rank * (BN / 2);
+      const int kb0 = sp * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        const int s = it % Cf::STAGES;
+        const uint32_t ph = (uint32_t)(it / Cf::STAGES) & 1u;
+        if (!wait_u(empty(s), ph ^ 1u)) { ok = false; break; }
+        const uint32_t a_dst = base + s * Cf::STAGE, b_dst = a_dst + Cf::A_BYTES;
+        const uint32_t fb = mapa_shared(full(s), 0);
+        if (elect_one()) {
           if (leader) mbar_expect_tx(full(s), 2 * Cf::STAGE);   // both blocks' bytes
-          const uint32_t fb = mapa_shared(full(s), 0);
           if (AMN) {
             tma_load_2d_pair(a_dst, &tmA, fb, m0, kb * BK);
             tma_load_2d_pair(a_dst + 8192, &tmA, fb, m0 + 64, kb * BK);
@@ -255,15 +260,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             tma_load_2d_pair(b_dst, &tmB, fb, kb * BK, n0);
           }
         }
-      }
-      if (!ok && leader) {
-        // let the copies already issued land before the block exits
-        for (int j = max(0, it - Cf::STAGES); j < it; ++j)
-          mbar_wait(full(j % Cf::STAGES), (uint32_t)(j / Cf::STAGES) & 1u, abort_flag, nullptr, false);
+        __syncwarp();
       }
     }
+    if (!ok && leader && lane == 0) {
+      // let the copies already issued land before the block exits
+      for (int j = max(0, it - Cf::STAGES); j < it; ++j)
+        mbar_wait(full(j % Cf::STAGES), (uint32_t)(j / Cf::STAGES) & 1u, abort_flag, nullptr, false);
+    }
+    __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0 && leader) {
+    if (leader) {
       // ---------------- MMA issuer (even block): M = 256 MMAs over both blocks' stages
       int it = 0, tcount = 0;
       bool ok = true;
@@ -273,32 +280,39 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         const int kb0 = sp * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         const int acc = tcount & 1;
         const uint32_t aph = (uint32_t)(tcount >> 1) & 1u;
-        if (!mbar_wait(tempty(acc), aph ^ 1u, abort_flag, p.err, true, p.wait_ns)) { ok = false; break; }
+        if (!wait_u(tempty(acc), aph ^ 1u)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % Cf::STAGES;
           const uint32_t ph = (uint32_t)(it / Cf::STAGES) & 1u;
-          if (!mbar_wait(full(s), ph, abort_flag, p.err, true, p.wait_ns)) { ok = false; break; }
+          if (!wait_u(full(s), ph)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_base = base + s * Cf::STAGE, b_base = a_base + Cf::A_BYTES;
+          // a k step of 16 adds 32 bytes along K (K-major) or 2048 bytes (MN-major)
+          const uint64_t ad0 = AMN ? sdesc(a_base, 8192, 1024) : sdesc(a_base, 16, 1024);
+          const uint64_t bd0 = BMN ? sdesc(b_base, 8192, 1024) : sdesc(b_base, 16, 1024);
+          constexpr uint64_t ASTEP = AMN ? 128 : 2, BSTEP = BMN ? 128 : 2;
+          if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = AMN ? sdesc(a_base + k * 2048, 8192, 1024)
-                                    : sdesc(a_base + k * 32, 16, 1024);
-            const uint64_t bd = BMN ? sdesc(b_base + k * 2048, 8192, 1024)
-                                    : sdesc(b_base + k * 32, 16, 1024);
-            umma_bf16_pair(d, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < BK / 16; ++k)
+              umma_bf16_pair(d, ad0 + ASTEP * k, bd0 + BSTEP * k, IDESC,
+                             (kb > kb0 || k > 0) ? 1u : 0u);
+            umma_commit_pair_mc(empty(s), PAIR);   // the stage is free in both blocks
           }
-          umma_commit_pair_mc(empty(s), PAIR);   // the stage is free in both blocks
+          __syncwarp();
         }
         if (!ok) break;
-        if (!(p.drop_first_signal && tcount == 0))
+        if (elect_one() && !(p.drop_first_signal && tcount == 0))
           umma_commit_pair_mc(tfull(acc), PAIR);   // both blocks' accumulators are ready
+        __syncwarp();
       }
       // all issued MMAs complete before tensor memory is released
-      umma_commit_pair(final_bar);
-      mbar_wait(final_bar, 0, abort_flag, nullptr, false);
+      if (elect_one()) {
+        umma_commit_pair(final_bar);
+        mbar_wait(final_bar, 0, abort_flag, nullptr, false);
+      }
+      __syncwarp();
     }
   } else {
     // ---------------- epilogue warps 2..9 of both blocks; warp % 4 selects the TMEM lane
