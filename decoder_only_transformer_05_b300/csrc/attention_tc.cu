@@ -82,7 +82,8 @@ __device__ __forceinline__ void stage_row32(uint32_t slice, int r, const float* 
 struct Params {
   int B, T, H, C, nqb, units;
   float* lse;            // forward output, backward input [B, H, T]
-  float* Dbuf;           // backward: rowsum(dO * O) [B, H, T], written by the dQ kernel
+  float* Dbuf;           // backward scratch [2][B, H, T], written by the dQ kernel for the
+                         // dK/dV kernel: -D = -rowsum(dO * O), then -lse * log2(e)
   int* err;
 };
 
@@ -562,7 +563,9 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
           mbar_expect_tx(bar(KB_QDFULL + s), 2 * TILE + 2 * nb);
           tma_load_3d(dst, &tm_qkv, bar(KB_QDFULL + s), h * D, qbi * BQ, b);
           tma_load_3d(dst + TILE, &tm_do, bar(KB_QDFULL + s), h * D, qbi * BQ, b);
-          bulk_load(base + K_SM_LD + s * 1024, p.lse + bh_t + (size_t)qbi * BQ, nb, bar(KB_QDFULL + s));
+          const size_t bht = (size_t)p.B * p.H * p.T;
+          bulk_load(base + K_SM_LD + s * 1024, p.Dbuf + bht + bh_t + (size_t)qbi * BQ, nb,
+                    bar(KB_QDFULL + s));
           bulk_load(base + K_SM_LD + s * 1024 + 512, p.Dbuf + bh_t + (size_t)qbi * BQ, nb,
                     bar(KB_QDFULL + s));
         }
@@ -685,31 +688,36 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(KB_SEMPTY));
+        // per query column: -lse log2(e) and -D (stored pre-negated by the dQ kernel), so
+        // P = exp2(s sl2 - lse log2 e) is one fma and dS = P (dP - D) an add and a multiply,
+        // each on packed fp32 pairs
         auto chunk = [&](int c, auto masked_tag) -> bool {
           constexpr bool MASKED = decltype(masked_tag)::value;
           uint32_t pk[16], dk[16];
+          const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
             const float4 L = lse4[c * 8 + e4], Dd = D4[c * 8 + e4];
-            const float lv[4] = {L.x, L.y, L.z, L.w}, dd[4] = {Dd.x, Dd.y, Dd.z, Dd.w};
-            float pp[4], ds[4];
+            const float2 lv[2] = {make_float2(L.x, L.y), make_float2(L.z, L.w)};
+            const float2 dd[2] = {make_float2(Dd.x, Dd.y), make_float2(Dd.z, Dd.w)};
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int e = e4 * 4 + t;
-              float pv = fast_exp2(fmaf(__uint_as_float(sv[c][e]), sl2, -lv[t] * LOG2E));
-              float dsv = pv * (__uint_as_float(dv[c][e]) - dd[t]);
+            for (int t = 0; t < 2; ++t) {
+              const int e = e4 * 4 + 2 * t;
+              const float2 a = __ffma2_rn(
+                  make_float2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), sl2x2, lv[t]);
+              float2 pv = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+              float2 dsv = __fmul2_rn(
+                  pv, __fadd2_rn(make_float2(__uint_as_float(dv[c][e]), __uint_as_float(dv[c][e + 1])),
+                                 dd[t]));
               if (MASKED) {
                 // past T the lse / D entries were never loaded: zero both results outright
                 const int query = q0 + c * 32 + e;
-                if (query < key || query >= p.T) { pv = 0.f; dsv = 0.f; }
+                if (query < key || query >= p.T) { pv.x = 0.f; dsv.x = 0.f; }
+                if (query + 1 < key || query + 1 >= p.T) { pv.y = 0.f; dsv.y = 0.f; }
               }
-              pp[t] = pv;
-              ds[t] = dsv;
+              pk[e4 * 2 + t] = pack2_bf16(pv.x, pv.y);
+              dk[e4 * 2 + t] = pack2_bf16(dsv.x, dsv.y);
             }
-            pk[e4 * 2] = pack2_bf16(pp[0], pp[1]);
-            pk[e4 * 2 + 1] = pack2_bf16(pp[2], pp[3]);
-            dk[e4 * 2] = pack2_bf16(ds[0], ds[1]);
-            dk[e4 * 2 + 1] = pack2_bf16(ds[2], ds[3]);
           }
           if (c == 0) {
             // the previous block's dV, dK MMAs have read P^T, dS^T from tensor memory (for
@@ -1008,7 +1016,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(QB_OEMPTY));
-      if (half == 0 && query < p.T) p.Dbuf[t] = Dr;
+      if (half == 0 && query < p.T) {   // for the dK/dV kernel, pre-negated
+        p.Dbuf[t] = -Dr;
+        p.Dbuf[(size_t)p.B * p.H * p.T + t] = nlse2;
+      }
       for (int j = 0; j < n; ++j, ++g) {
         ok = mbar_wait(bar(QB_SFULL), par(g), abort_flag, p.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -1024,20 +1035,27 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
         if (lane == 0) mbar_arrive(bar(QB_SEMPTY));
         const int k0 = j * BKV + c0;
         uint32_t dk[32];
-        auto compute = [&](auto masked_tag) {   // causal mask on the diagonal block only
+        // dS = exp2(s sl2 - lse log2 e) (dP - D) on packed fp32 pairs; the causal mask on
+        // the diagonal block only
+        const float2 sl2x2 = make_float2(sl2, sl2), nl2 = make_float2(nlse2, nlse2);
+        const float2 nD2 = make_float2(-Dr, -Dr);
+        auto compute = [&](auto masked_tag) {
           constexpr bool MASKED = decltype(masked_tag)::value;
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
-              float ds[2];
-#pragma unroll
-              for (int t = 0; t < 2; ++t) {
-                float pv = fast_exp2(fmaf(__uint_as_float(sv[c][e + t]), sl2, nlse2));
-                if (MASKED && k0 + c * 32 + e + t > query) pv = 0.f;
-                ds[t] = pv * (__uint_as_float(dv[c][e + t]) - Dr);
+              const float2 a = __ffma2_rn(
+                  make_float2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), sl2x2, nl2);
+              float2 pv = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+              if (MASKED) {
+                if (k0 + c * 32 + e > query) pv.x = 0.f;
+                if (k0 + c * 32 + e + 1 > query) pv.y = 0.f;
               }
-              dk[c * 16 + e / 2] = pack2_bf16(ds[0], ds[1]);
+              const float2 ds = __fmul2_rn(
+                  pv, __fadd2_rn(make_float2(__uint_as_float(dv[c][e]), __uint_as_float(dv[c][e + 1])),
+                                 nD2));
+              dk[c * 16 + e / 2] = pack2_bf16(ds.x, ds.y);
             }
           }
         };

@@ -348,7 +348,7 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   size_t o_lnf = plan(M * C * es), o_lnfm = plan(M * 4), o_lnfr = plan(M * 4);
   size_t o_logits = plan(M * (size_t)h->Vp * es), o_losses = plan(M * 4), o_argmax = plan(M * 4);
   size_t o_dres = plan(M * C * es), o_dln = plan(M * C * es), o_datt = plan(M * C * es);
-  size_t o_dqkv = plan(M * 3 * C * es), o_dfch = plan(M * 4 * C * es), o_D = plan(BHT * 4);
+  size_t o_dqkv = plan(M * 3 * C * es), o_dfch = plan(M * 4 * C * es), o_D = plan(2 * BHT * 4);
   // split-K workspace for a tied lm_head gradient that needed one (it does not at these
   // shapes; the per-layer weight gradients use the deferred buffers below)
   size_t ws = 0;

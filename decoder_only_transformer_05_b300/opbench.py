@@ -79,7 +79,7 @@ def run_attention(iters):
     lse = torch.empty(B, H, T, device="cuda")
     dout = _bf16(B, T, C)
     dqkv = torch.empty_like(qkv)
-    Dbuf = torch.empty(B, H, T, device="cuda")
+    Dbuf = torch.empty(2, B, H, T, device="cuda")
     flops = 2 * 2 * B * H * (T * (T + 1) / 2) * (C // H)   # causal QK^T and PV
     ms_f = _time(lambda: G.op_attention_forward("bf16", out, lse, qkv, B, T, C, H), iters)
     ms_b = _time(lambda: G.op_attention_backward("bf16", dqkv, Dbuf, dout, out, qkv, lse, B, T,

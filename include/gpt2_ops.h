@@ -45,7 +45,8 @@ int gpt2_op_gemm(int precision, int M, int N, int K, const void* A, int64_t lda,
    GPT2_BF16 needs head size 64. */
 int gpt2_op_attention_forward(int precision, void* out, float* lse, const void* qkv, int B,
                               int T, int C, int H, void* stream);
-/* dout [B, T, C] -> dqkv [B, T, 3C]; Dbuf is [B, H, T] fp32 scratch. */
+/* dout [B, T, C] -> dqkv [B, T, 3C]; Dbuf is fp32 scratch of 2 * B * H * T floats (its
+   contents on return are unspecified). */
 int gpt2_op_attention_backward(int precision, void* dqkv, float* Dbuf, const void* dout,
                                const void* out, const void* qkv, const float* lse, int B,
                                int T, int C, int H, void* stream);

@@ -188,7 +188,7 @@ def test_attention_bf16(B, T, H, hs):
     G.op_attention_forward("bf16", out, lse, qkv, B, T, C, H)
     dout = dev(rnd((B, T, C), 21), torch.bfloat16)
     dqkv = torch.zeros(B, T, 3 * C, dtype=torch.bfloat16, device="cuda")
-    Dbuf = torch.empty(B, H, T, dtype=torch.float32, device="cuda")
+    Dbuf = torch.empty(2, B, H, T, dtype=torch.float32, device="cuda")
     G.op_attention_backward("bf16", dqkv, Dbuf, dout, out, qkv, lse, B, T, C, H)
     torch.cuda.synchronize()
     q = host(qkv)
@@ -214,7 +214,7 @@ def test_attention_bf16_backward_rejects_t_not_multiple_of_4():
     out = torch.zeros(B, T, C, dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros(B, H, T, dtype=torch.float32, device="cuda")
     dqkv = torch.zeros_like(qkv)
-    Dbuf = torch.zeros_like(lse)
+    Dbuf = torch.zeros(2, B, H, T, dtype=torch.float32, device="cuda")
     with pytest.raises(G.GPT2Error) as e:
         G.op_attention_backward("bf16", dqkv, Dbuf, out, out, qkv, lse, B, T, C, H)
     assert e.value.name == "ARG"
@@ -228,7 +228,7 @@ def test_attention_fp32():
     G.op_attention_forward("fp32", out, lse, qkv, B, T, C, H)
     dout = dev(rnd((B, T, C), 23), torch.float32)
     dqkv = torch.zeros(B, T, 3 * C, device="cuda")
-    Dbuf = torch.empty(B, H, T, device="cuda")
+    Dbuf = torch.empty(2, B, H, T, device="cuda")
     G.op_attention_backward("fp32", dqkv, Dbuf, dout, out, qkv, lse, B, T, C, H)
     torch.cuda.synchronize()
     ref_out, P = O.attention_forward(host(qkv), H)
