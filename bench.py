@@ -3,10 +3,13 @@
 (forward, backward, global-norm clip, AdamW) through the libgpt2 C ABI.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload gpt2-124m-step|gpt2-350m-shape]
 
 One step = the GPT-2 124M optimiser step: 40 micro-batches of 12 x 1024 tokens
 (forward + backward each, gradients accumulated with scale 1/40), global-norm clip 1.0 and
-AdamW (lr from the 6e-4 warmup-cosine schedule, betas 0.9/0.95, wd 0.1). Each micro-batch
+AdamW (lr from the 6e-4 warmup-cosine schedule, betas 0.9/0.95, wd 0.1). With
+--workload gpt2-350m-shape: the 350M-shape model (L=24, H=16, C=1024), 8 micro-batches of
+8 x 1024 tokens, the same optimiser settings. Each micro-batch
 is one gpt2_forward_backward call (replayed as a CUDA graph after its first call). Tokens are
 seeded synthetic Zipf(1.0) ids over the GPT-2 vocabulary (no dataset is available) and
 weights are the N(0, 0.02) initialisation. Under torchrun each rank runs an independent
@@ -31,6 +34,12 @@ from decoder_only_transformer_05_b300 import synthetic as S  # noqa: E402
 
 METRIC = "GPT-2 124M training tokens/sec on 1 B300; MFU vs dense BF16 tensor peak"
 WORKLOAD = "gpt2-124m-step"
+WORKLOAD_TEXT = {
+    "gpt2-124m-step": "GPT-2 124M (L=12, H=12, C=768, T=1024, V=50257 padded to 50304), "
+                      "40 micro-batches of 12 x 1024 tokens, clip 1.0, AdamW",
+    "gpt2-350m-shape": "GPT-2 350M shape (L=24, H=16, C=1024, T=1024, V=50257 padded to "
+                       "50304), 8 micro-batches of 8 x 1024 tokens, clip 1.0, AdamW",
+}
 
 
 # DRAM bytes read + written per GEMM launch (the micro-batch's GEMM launches averaged) from
@@ -175,8 +184,9 @@ def blas_threads():
     return os.cpu_count()
 
 
-SAMPLE_DESC = ("one 1024-token sequence of the GPT-2 124M step (forward, backward, "
-               "global-norm clip and AdamW over all 124M parameters) in float64 numpy")
+def sample_desc(w):
+    return (f"one 1024-token sequence of the {w['name']} step (forward, backward, global-norm "
+            "clip and AdamW over all parameters) in float64 numpy")
 
 
 def run_reference(args, w):
@@ -192,7 +202,7 @@ def run_reference(args, w):
         secs += s
     value = toks / secs
     cores = blas_threads()
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+    line = {"impl": "reference", "metric": w["metric"], "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * secs / args.steps, "higher_is_better": True,
             # each timed step of this arm is one sample, not the config's 491,520 tokens
@@ -201,10 +211,10 @@ def run_reference(args, w):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_block(w),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
-                             "kind": "oracle", "sample": SAMPLE_DESC + " per step; the AdamW "
-                             "pass over all 124M parameters is paid once per 1024 tokens "
-                             "here (once per 491,520 in the config), which understates the "
-                             "oracle's per-token rate"},
+                             "kind": "oracle", "sample": sample_desc(w) + " per step; the "
+                             "AdamW pass over all parameters is paid once per 1024 tokens "
+                             "here (once per optimiser step in the config), which "
+                             "understates the oracle's per-token rate"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -212,9 +222,7 @@ def run_reference(args, w):
 
 
 def config_block(w):
-    return {"workload": f"{WORKLOAD}: GPT-2 124M (L=12, H=12, C=768, T=1024, V=50257 "
-                        "padded to 50304), 40 micro-batches of 12 x 1024 tokens, clip 1.0, "
-                        "AdamW",
+    return {"workload": f"{w['name']}: {WORKLOAD_TEXT[w['name']]}",
             "batch": w["B"], "seq_len": w["T"], "grad_accum": w["accum"],
             "tokens_per_step": w["B"] * w["T"] * w["accum"],
             "l2": "working set (weights, activations, 1.2 GB logits) far larger than L2"}
@@ -328,11 +336,11 @@ def run_ours(args, w):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         toks, secs = oracle_sample(w, w["w_seed"], 0, "baseline")
         cpu = {"value": toks / secs, "unit": "tokens/s", "cores": blas_threads(),
-               "kind": "oracle", "sample": SAMPLE_DESC}
+               "kind": "oracle", "sample": sample_desc(w)}
     m.close()
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "metric": w["metric"], "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_block(w),
@@ -369,8 +377,12 @@ def main():
     ap.add_argument("--accum", type=int, default=None, help="override micro-batches per step")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default=WORKLOAD)
     args = ap.parse_args()
-    w = dict(S.WORKLOADS[WORKLOAD])
+    w = dict(S.WORKLOADS[args.workload])
+    w["name"] = args.workload
+    w["metric"] = METRIC if args.workload == WORKLOAD else (
+        "GPT-2 350M-shape training tokens/sec on 1 B300; MFU vs dense BF16 tensor peak")
     if args.accum:
         w["accum"] = args.accum
     if args.impl == "reference":
