@@ -71,6 +71,17 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(GemmArgs g) {
         case EPI_GELU_BWD:
           ((float*)g.out)[o] = v * ((const float*)g.aux)[o];
           break;
+        case EPI_GELU_FWD_U:
+          if (g.bias) v += ((const float*)g.bias)[n];
+          ((float*)g.pre)[o] = v;
+          ((float*)g.out)[o] = gelu_tanh(v);
+          break;
+        case EPI_GELU_BWD_U: {
+          const float u = ((const float*)g.aux)[o];
+          ((float*)g.out)[o] = v * gelu_tanh_grad(u);
+          ((float*)g.pre)[o] = gelu_tanh(u);
+          break;
+        }
         case EPI_ACCUM:
           g.accum[o] += g.scale * v;
           break;

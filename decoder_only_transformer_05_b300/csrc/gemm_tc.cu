@@ -80,7 +80,7 @@ struct Params {
 // pre-activation); lane 0 then stores the chunk with TMA.
 struct EpiMaps {
   CUtensorMap out;   // bf16 [M, N] (64-byte swizzle) or fp32 [M, N] / [splits, M, N] (128-byte)
-  CUtensorMap pre;   // bf16 [M, N], EPI_GELU_FWD only
+  CUtensorMap pre;   // bf16 [M, N]: the second output of EPI_GELU_FWD / _FWD_U / _BWD_U
   CUtensorMap in;    // bf16 [M, N] pre-activation, EPI_GELU_BWD only
 };
 
@@ -95,7 +95,7 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const EpiMaps& m
 #pragma unroll
     for (int i = 0; i < 4; ++i) bia[i] = __ldg(reinterpret_cast<const uint4*>(p.bias + col0) + i);
   }
-  const bool src = p.epi == EPI_GELU_BWD || (p.epi == EPI_STORE && p.resid);
+  const bool src = p.epi == EPI_GELU_BWD || p.epi == EPI_GELU_BWD_U || (p.epi == EPI_STORE && p.resid);
   // the accumulator as 16 column pairs (packed two-lane fp32 arithmetic below)
   float2 v[16];
   tmem_ld32(taddr, reinterpret_cast<float (&)[32]>(v));
@@ -129,6 +129,27 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const EpiMaps& m
         w[e] = pack2_bf16(g.x, g.y);
       }
       stage_row_bf16(stg + 2048, lane, u);
+    } else if (p.epi == EPI_GELU_FWD_U) {   // keep u itself for the recomputing backward
+      uint32_t u[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        float2 d;
+        const float2 g = gelu_tanh_and_grad_fast2(v[e], d);
+        u[e] = pack2_bf16(v[e].x, v[e].y);
+        w[e] = pack2_bf16(g.x, g.y);
+      }
+      stage_row_bf16(stg + 2048, lane, u);
+    } else if (p.epi == EPI_GELU_BWD_U) {   // gelu'(u) and gelu(u) recomputed from u
+      uint32_t gu[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        float2 d;
+        const float2 g = gelu_tanh_and_grad_fast2(bf2_to_f2(in[e]), d);
+        const float2 o = __fmul2_rn(v[e], d);
+        w[e] = pack2_bf16(o.x, o.y);
+        gu[e] = pack2_bf16(g.x, g.y);
+      }
+      stage_row_bf16(stg + 2048, lane, gu);
     } else {   // EPI_GELU_BWD
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
@@ -147,7 +168,8 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const EpiMaps& m
       else tma_store_3d(&maps.out, stg, col0, row0, split);
     } else {
       tma_store_2d(&maps.out, stg, col0, row0);
-      if (p.epi == EPI_GELU_FWD) tma_store_2d(&maps.pre, stg + 2048, col0, row0);
+      if (p.epi == EPI_GELU_FWD || p.epi == EPI_GELU_FWD_U || p.epi == EPI_GELU_BWD_U)
+        tma_store_2d(&maps.pre, stg + 2048, col0, row0);
     }
     bulk_commit();
   }
@@ -319,7 +341,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     // quarter, and warps w, w + 4 split the tile's 32-column chunks between them
     const int q = warp & 3, ew = warp - 2, half = ew >> 2;
     const uint32_t stg = staging + ew * STG_BYTES;
-    if (p.epi == EPI_GELU_FWD && lane == 0) {
+    if ((p.epi == EPI_GELU_FWD || p.epi == EPI_GELU_FWD_U || p.epi == EPI_GELU_BWD_U) &&
+        lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"((unsigned long long)&maps.pre) : "memory");
     }
     // The GELU pre-activation rows of a chunk come by TMA into the second half of the warp's
@@ -383,11 +406,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         } else {
 #pragma unroll
           for (int j = 0; j < 4; ++j) inp[j] = make_uint4(0u, 0u, 0u, 0u);
-          // residual rows (rows past M are computed but never stored: TMA clips them)
-          if (p.epi == EPI_STORE && p.resid && row0 + lane < p.M) {
+          // residual rows, or the pre-activation of EPI_GELU_BWD_U (whose second output
+          // needs the staging half that the TMA-prefetched input would use); rows past M are
+          // computed but never stored: TMA clips them
+          const bf16* rsrc = p.epi == EPI_GELU_BWD_U ? p.aux : (p.epi == EPI_STORE ? p.resid : nullptr);
+          if (rsrc && row0 + lane < p.M) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              inp[j] = __ldg(reinterpret_cast<const uint4*>(p.resid + (size_t)(row0 + lane) * p.ldo +
+              inp[j] = __ldg(reinterpret_cast<const uint4*>(rsrc + (size_t)(row0 + lane) * p.ldo +
                                                              col0) + j);
           }
         }
@@ -515,12 +541,12 @@ static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
                     32, 32, CU_TENSOR_MAP_SWIZZLE_128B, (uint64_t)p.splits,
                     (uint64_t)g.M * g.N);
   } else {
-    if (g.epi == EPI_GELU_BWD && !g.aux) return cudaErrorInvalidValue;
+    if ((g.epi == EPI_GELU_BWD || g.epi == EPI_GELU_BWD_U) && !g.aux) return cudaErrorInvalidValue;
     ok = make_map_bf16(&maps.out, g.out, g.N, g.M, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     const void* in = g.epi == EPI_GELU_BWD ? g.aux : nullptr;
     if (ok && in)
       ok = make_map_bf16(&maps.in, in, g.N, g.M, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-    if (ok && g.epi == EPI_GELU_FWD)
+    if (ok && (g.epi == EPI_GELU_FWD || g.epi == EPI_GELU_FWD_U || g.epi == EPI_GELU_BWD_U))
       ok = g.pre && make_map_bf16(&maps.pre, g.pre, g.N, g.M, g.ldo, 32, 32,
                                   CU_TENSOR_MAP_SWIZZLE_64B);
   }

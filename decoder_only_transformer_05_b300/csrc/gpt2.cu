@@ -94,7 +94,7 @@ struct ProfPair { cudaEvent_t a, b; int cls; double work; };
 struct gpt2 {
   gpt2_config cfg{};
   int V = 0, Vp = 0, T = 0, L = 0, H = 0, C = 0, Bmax = 0;
-  bool is_bf16 = false, bias = false;
+  bool is_bf16 = false, bias = false, recompute = false;
   DType dt = DType::F32;
   size_t es = 4;   // activation element size
   cudaStream_t stream = nullptr;
@@ -104,12 +104,15 @@ struct gpt2 {
   size_t P = 0, n_model = 0;
 
   char* pmem = nullptr;   // params block
+  size_t pmem_bytes = 0;
   float *params = nullptr, *grads = nullptr, *m = nullptr, *v = nullptr;
   bf16* params_bf16 = nullptr;
   char* amem = nullptr;   // activations + scratch
   size_t amem_bytes = 0;
 
-  // activations (element type per path)
+  // activations (element type per path). With recompute, ln1[l] and ln2[l] all point at one
+  // shared LayerNorm-output buffer and fcg[l] at one shared GELU-output buffer, and fch[l]
+  // holds the pre-activation u (otherwise gelu'(u)).
   std::vector<void*> x;   // L+1 residual streams
   std::vector<void*> ln1, qkv, att, xmid, ln2, fch, fcg;
   std::vector<float*> ln1_mean, ln1_rstd, ln2_mean, ln2_rstd, lse;
@@ -273,6 +276,7 @@ static void setup_shape(gpt2* h, const gpt2_config& cfg) {
   h->L = cfg.n_layer; h->H = cfg.n_head; h->C = cfg.n_embd; h->Bmax = cfg.batch_size;
   h->is_bf16 = cfg.precision == GPT2_BF16;
   h->bias = cfg.bias != 0;
+  h->recompute = cfg.recompute != 0;
   h->dt = h->is_bf16 ? DType::BF16 : DType::F32;
   h->es = h->is_bf16 ? 2 : 4;
   build_layout(h);
@@ -317,6 +321,7 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   // ---- parameter block
   const size_t P = h->P;
   size_t pbytes = 4 * align256(P * 4) + (h->is_bf16 ? align256(P * 2) : 0);
+  h->pmem_bytes = pbytes;
   if (cudaError_t e = cudaMalloc(&h->pmem, pbytes); e != cudaSuccess) {
     cudaGetLastError();
     delete h;
@@ -338,10 +343,15 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   std::vector<size_t> o_x(L + 1), o_ln1(L), o_qkv(L), o_att(L), o_xmid(L), o_ln2(L), o_fch(L),
       o_fcg(L), o_m1(L), o_r1(L), o_m2(L), o_r2(L), o_lse(L);
   for (size_t l = 0; l <= L; ++l) o_x[l] = plan(M * C * es);
+  const size_t o_ln_shared = h->recompute ? plan(M * C * es) : 0;
+  const size_t o_g_shared = h->recompute ? plan(M * 4 * C * es) : 0;
   for (size_t l = 0; l < L; ++l) {
-    o_ln1[l] = plan(M * C * es); o_qkv[l] = plan(M * 3 * C * es); o_att[l] = plan(M * C * es);
-    o_xmid[l] = plan(M * C * es); o_ln2[l] = plan(M * C * es); o_fch[l] = plan(M * 4 * C * es);
-    o_fcg[l] = plan(M * 4 * C * es);
+    o_ln1[l] = h->recompute ? o_ln_shared : plan(M * C * es);
+    o_qkv[l] = plan(M * 3 * C * es); o_att[l] = plan(M * C * es);
+    o_xmid[l] = plan(M * C * es);
+    o_ln2[l] = h->recompute ? o_ln_shared : plan(M * C * es);
+    o_fch[l] = plan(M * 4 * C * es);
+    o_fcg[l] = h->recompute ? o_g_shared : plan(M * 4 * C * es);
     o_m1[l] = plan(M * 4); o_r1[l] = plan(M * 4); o_m2[l] = plan(M * 4); o_r2[l] = plan(M * 4);
     o_lse[l] = plan(BHT * 4);
   }
@@ -617,7 +627,7 @@ extern "C" int gpt2_forward(gpt2_handle h, const int32_t* tokens, const int32_t*
     prof_end(h, pi, (double)M * C * es * 2);
     g = linear_fwd(M, 4 * C, C, h->ln2[l], h->pw(T_FCW, l), h->fcg[l]);
     if (h->bias) g.bias = h->pw(T_FCB, l);
-    g.epi = EPI_GELU_FWD;
+    g.epi = h->recompute ? EPI_GELU_FWD_U : EPI_GELU_FWD;   // keeps u or gelu'(u)
     g.pre = h->fch[l];
     CKL(run_gemm(h, g));
     g = linear_fwd(M, C, 4 * C, h->fcg[l], h->pw(T_FCPROJW, l), h->x[l + 1]);
@@ -686,9 +696,19 @@ extern "C" int gpt2_backward(gpt2_handle h, float loss_scale) {
     GemmArgs g = linear_dgrad(M, C, 4 * C, h->dres, h->pw(T_FCPROJW, l), h->dfch);
     g.epi = EPI_GELU_BWD;
     g.aux = h->fch[l];
+    if (h->recompute) {   // gelu'(u) from u, and gelu(u) into the shared buffer for the wgrad
+      g.epi = EPI_GELU_BWD_U;
+      g.pre = h->fcg[l];
+    }
     CKL(run_gemm(h, g));
     CKL(run_gemm(h, linear_wgrad(M, C, 4 * C, h->dres, h->fcg[l], h->gw(T_FCPROJW, l), sc), wg(l, 3)));
     // fch = ln2 Wfc^T + bfc
+    if (h->recompute) {   // LN2's output, recomputed from the kept residual stream
+      pi = prof_begin(h, PC_LN);
+      CKL(layernorm_forward(dt, h->ln2[l], h->ln2_mean[l], h->ln2_rstd[l], h->xmid[l],
+                            h->pw(T_LN2W, l), h->pw(T_LN2B, l), M, C, s));
+      prof_end(h, pi, (double)M * C * es * 2);
+    }
     CKL(run_gemm(h, linear_dgrad(M, 4 * C, C, h->dfch, h->pw(T_FCW, l), h->dln)));
     CKL(run_gemm(h, linear_wgrad(M, 4 * C, C, h->dfch, h->ln2[l], h->gw(T_FCW, l), sc), wg(l, 2)));
     if (h->bias) {
@@ -707,6 +727,12 @@ extern "C" int gpt2_backward(gpt2_handle h, float loss_scale) {
                            C, H, h->d_err, s));
     prof_end(h, pi, 2.5 * 2.0 * 2.0 * B * H * (double)T * (T + 1) / 2 * (C / H));
     // qkv = ln1 Wqkv^T + bqkv
+    if (h->recompute) {   // LN1's output, recomputed from the kept residual stream
+      pi = prof_begin(h, PC_LN);
+      CKL(layernorm_forward(dt, h->ln1[l], h->ln1_mean[l], h->ln1_rstd[l], h->x[l],
+                            h->pw(T_LN1W, l), h->pw(T_LN1B, l), M, C, s));
+      prof_end(h, pi, (double)M * C * es * 2);
+    }
     CKL(run_gemm(h, linear_dgrad(M, 3 * C, C, h->dqkv, h->pw(T_QKVW, l), h->dln)));
     CKL(run_gemm(h, linear_wgrad(M, 3 * C, C, h->dqkv, h->ln1[l], h->gw(T_QKVW, l), sc), wg(l, 0)));
     if (h->bias) {
@@ -973,6 +999,13 @@ extern "C" int gpt2_profile_read(gpt2_handle h, int cls, int64_t* launches, doub
       h->prof_launches[c] = 0; h->prof_ms[c] = 0; h->prof_work[c] = 0;
     }
   }
+  return GPT2_OK;
+}
+
+extern "C" int gpt2_memory_bytes(gpt2_handle h, size_t* param_bytes, size_t* other_bytes) {
+  if (!h) return fail(GPT2_ERR_ARG, "null handle");
+  if (param_bytes) *param_bytes = h->pmem_bytes;
+  if (other_bytes) *other_bytes = h->amem_bytes + h->dmem_bytes;
   return GPT2_OK;
 }
 

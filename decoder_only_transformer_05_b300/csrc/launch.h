@@ -23,6 +23,10 @@ enum GemmEpi : int {
   EPI_GELU_FWD = 1,  // u = v + bias[n]; out = gelu_tanh(u); pre = gelu_tanh'(u)
   EPI_GELU_BWD = 2,  // out = v * aux[m, n]  (aux: the pre of EPI_GELU_FWD)
   EPI_ACCUM = 3,     // accum[m, n] += scale * v   (fp32; wgrad into the grad buffer)
+  // activation recomputation: the forward keeps the pre-activation u instead of gelu'(u),
+  // the backward recomputes gelu'(u) and gelu(u) from it
+  EPI_GELU_FWD_U = 4,  // u = v + bias[n]; out = gelu_tanh(u); pre = u
+  EPI_GELU_BWD_U = 5,  // u = aux[m, n]; out = v * gelu_tanh'(u); pre = gelu_tanh(u)
 };
 
 struct GemmArgs {

@@ -20,7 +20,7 @@ extern "C" int gpt2_op_gemm(int precision, int M, int N, int K, const void* A, i
                             int64_t ldo, const void* bias, const void* resid, void* pre,
                             const void* aux, float* accum, float scale, int splits,
                             float* workspace, size_t workspace_bytes, void* stream) {
-  if (epi < 0 || epi > 3) return gpt2_set_error(GPT2_ERR_ARG, "bad epilogue");
+  if (epi < 0 || epi > 5) return gpt2_set_error(GPT2_ERR_ARG, "bad epilogue");
   GemmArgs g;
   g.M = M; g.N = N; g.K = K;
   g.A = A; g.lda = lda; g.a_mn = a_mn != 0;

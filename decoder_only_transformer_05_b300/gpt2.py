@@ -21,7 +21,7 @@ ERRORS = {-1: "INVALID_CONFIG", -2: "OOM", -3: "CUDA", -4: "BAD_TOKEN", -5: "SEQ
 FP32, BF16 = 0, 1
 REGION = dict(params=0, grads=1, m=2, v=3, params_bf16=4, logits=5, losses=6, encoded=7,
               argmax=8)
-EPI = dict(store=0, gelu_fwd=1, gelu_bwd=2, accum=3)
+EPI = dict(store=0, gelu_fwd=1, gelu_bwd=2, accum=3, gelu_fwd_u=4, gelu_bwd_u=5)
 PROF = dict(gemm=0, attention=1, layernorm=2, classifier=3, encoder=4, optimizer=5, other=6)
 
 
@@ -38,7 +38,7 @@ class _Config(ctypes.Structure):
                 ("n_head", ctypes.c_int32), ("n_embd", ctypes.c_int32),
                 ("bias", ctypes.c_int32), ("precision", ctypes.c_int32),
                 ("batch_size", ctypes.c_int32), ("init", ctypes.c_int32),
-                ("seed", ctypes.c_uint64)]
+                ("seed", ctypes.c_uint64), ("recompute", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -73,6 +73,7 @@ SIGNATURES = {
     "gpt2_profile_enable": (_I, [_P, _I, _I]),
     "gpt2_profile_read": (_I, [_P, _I, ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_double),
                                ctypes.POINTER(ctypes.c_double), _I]),
+    "gpt2_memory_bytes": (_I, [_P, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
     "gpt2_last_error": (ctypes.c_char_p, []),
     "gpt2_kernel_launches": (_I64, []),
     "gpt2_destroy": (None, [_P]),
@@ -139,10 +140,11 @@ def stream_handle(s):
 
 
 def make_config(vocab_size, block_size, n_layer, n_head, n_embd, batch_size,
-                padded_vocab_size=0, bias=True, precision="bf16", init=True, seed=0):
+                padded_vocab_size=0, bias=True, precision="bf16", init=True, seed=0,
+                recompute=False):
     return _Config(vocab_size, padded_vocab_size, block_size, n_layer, n_head, n_embd,
                    int(bool(bias)), BF16 if precision == "bf16" else FP32, batch_size,
-                   int(bool(init)), seed & 0xFFFFFFFFFFFFFFFF)
+                   int(bool(init)), seed & 0xFFFFFFFFFFFFFFFF, int(bool(recompute)))
 
 
 def host_num_params(**cfg):
@@ -168,10 +170,11 @@ class GPT2:
     """One model instance on the current CUDA device (see include/gpt2.h)."""
 
     def __init__(self, vocab_size, block_size, n_layer, n_head, n_embd, batch_size,
-                 padded_vocab_size=0, bias=True, precision="bf16", init=True, seed=0):
+                 padded_vocab_size=0, bias=True, precision="bf16", init=True, seed=0,
+                 recompute=False):
         lib = load_library()
         cfg = make_config(vocab_size, block_size, n_layer, n_head, n_embd, batch_size,
-                          padded_vocab_size, bias, precision, init, seed)
+                          padded_vocab_size, bias, precision, init, seed, recompute)
         h = _P()
         _check(lib.gpt2_create(ctypes.byref(cfg), ctypes.byref(h)))
         self._h = h
@@ -198,6 +201,12 @@ class GPT2:
     @property
     def handle(self):
         return self._h
+
+    def memory_bytes(self):
+        """(parameter block bytes, all other device bytes) the handle holds."""
+        a, b = _SZ(), _SZ()
+        _check(self.lib.gpt2_memory_bytes(self._h, ctypes.byref(a), ctypes.byref(b)))
+        return a.value, b.value
 
     def set_stream(self, stream):
         _check(self.lib.gpt2_set_stream(self._h, stream_handle(stream)))

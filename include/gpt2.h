@@ -84,11 +84,19 @@ typedef struct {
   int32_t batch_size;        /* maximum B; sizes the activation memory */
   int32_t init;              /* 1: initialise weights from seed (see below); 0: all zero */
   uint64_t seed;
+  int32_t recompute;         /* 1: activation recomputation (see below); 0: keep them all */
 } gpt2_config;
 
 /*
  * Create a handle: one device allocation for [params | grads | m | v | bf16 params], one
- * for activations and scratch. With init = 1 weights are N(0, 0.02) (residual
+ * for activations and scratch.
+ * With recompute = 1 the activation memory holds, per layer, the MLP pre-activation u
+ * instead of gelu(u) and gelu'(u), and no LayerNorm outputs: the backward recomputes both
+ * LayerNorm outputs of a layer (from the kept residual streams, means and inverse standard
+ * deviations) and gelu(u), gelu'(u) (from u, in the fc-proj input-gradient GEMM) where it
+ * needs them. Per layer that is 2 [B*T, C] + [B*T, 4C] activation elements fewer, for a
+ * few more kernels (memory relief, not speed). The forward's results are unchanged; the
+ * gradients differ from recompute = 0 only by the rounding of u to the activation type. With init = 1 weights are N(0, 0.02) (residual
  * projections attnproj and fcproj N(0, 0.02/sqrt(2L))), Linear biases 0, LayerNorm
  * gamma 1 and beta 0, padded vocabulary rows 0, drawn with SplitMix64 in counter mode
  * (tensor i of the full table draws from stream draw(seed, i); normals by Box-Muller).
@@ -225,6 +233,10 @@ int gpt2_profile_read(gpt2_handle h, int cls, int64_t* launches, double* total_m
 
 /* Number of CUDA kernels this library has launched in this process so far. */
 int64_t gpt2_kernel_launches(void);
+
+/* Device memory the handle holds, in bytes: the flat parameter block (params, grads, m, v,
+   bf16 copy) and everything else (activations, scratch, deferred gradient partials). */
+int gpt2_memory_bytes(gpt2_handle h, size_t* param_bytes, size_t* other_bytes);
 
 /* Message of the last failed call on this thread ("" if none). */
 const char* gpt2_last_error(void);

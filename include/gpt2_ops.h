@@ -20,7 +20,10 @@ enum {
   GPT2_EPI_STORE = 0,    /* out = v (+ bias[n]) (+ resid[m, n]) */
   GPT2_EPI_GELU_FWD = 1, /* u = v + bias[n]; out = gelu_tanh(u); pre = gelu_tanh'(u) */
   GPT2_EPI_GELU_BWD = 2, /* out = v * aux[m, n] (aux: the pre of GPT2_EPI_GELU_FWD) */
-  GPT2_EPI_ACCUM = 3     /* accum[m, n] += scale * v (fp32) */
+  GPT2_EPI_ACCUM = 3,    /* accum[m, n] += scale * v (fp32) */
+  /* for activation recomputation (gpt2_config.recompute): */
+  GPT2_EPI_GELU_FWD_U = 4, /* u = v + bias[n]; out = gelu_tanh(u); pre = u */
+  GPT2_EPI_GELU_BWD_U = 5  /* u = aux[m, n]; out = v * gelu_tanh'(u); pre = gelu_tanh(u) */
 };
 
 /*

@@ -110,6 +110,34 @@ def test_gemm_gelu_fwd_and_bwd(prec):
     assert rel_inf(host(d), ref) < (1.5e-2 if prec == "bf16" else 1e-5)
 
 
+@pytest.mark.parametrize("prec", ["bf16", "fp32"])
+def test_gemm_gelu_epilogues_for_recomputation(prec):
+    """The recomputation pair: the forward keeps u = X W^T + b (and writes gelu(u)); the
+    backward's dgrad multiplies by gelu'(u) recomputed from u and writes gelu(u) again (for
+    the weight gradient). Ragged M and 3 column tiles."""
+    M, N, K = 300, 384, 128
+    dt = torch.bfloat16 if prec == "bf16" else torch.float32
+    X, W, b = dev(rnd((M, K), 15), dt), dev(rnd((N, K), 16, 0.1), dt), dev(rnd((N,), 17), dt)
+    out = torch.empty(M, N, dtype=dt, device="cuda")
+    u = torch.empty(M, N, dtype=dt, device="cuda")
+    G.op_gemm(prec, M, N, K, X, K, False, W, K, False, "gelu_fwd_u", out=out, ldo=N, bias=b,
+              pre=u)
+    torch.cuda.synchronize()
+    ref_u = host(X) @ host(W).T + host(b)[None, :]
+    tol = 8e-3 if prec == "bf16" else 1e-5
+    assert rel_inf(host(u), ref_u) < tol
+    assert rel_inf(host(out), O.gelu(ref_u)) < tol
+    dY = dev(rnd((M, K), 18), dt)
+    W2 = dev(rnd((K, N), 19, 0.1), dt)
+    d = torch.empty(M, N, dtype=dt, device="cuda")
+    g = torch.empty(M, N, dtype=dt, device="cuda")
+    G.op_gemm(prec, M, N, K, dY, K, False, W2, N, True, "gelu_bwd_u", out=d, ldo=N, aux=u, pre=g)
+    torch.cuda.synchronize()
+    uu = host(u)   # the kept (rounded) pre-activation is what the backward sees
+    assert rel_inf(host(d), (host(dY) @ host(W2)) * O.gelu_grad(uu)) < (1.5e-2 if prec == "bf16" else 1e-5)
+    assert rel_inf(host(g), O.gelu(uu)) < tol
+
+
 @pytest.mark.parametrize("splits", [1, 3, 0])
 @pytest.mark.parametrize("shape", [(384, 256, 1024), (768, 768, 4096), (384, 256, 300)])
 def test_gemm_wgrad_accumulate_bf16(splits, shape):
