@@ -23,7 +23,7 @@ long long& launch_counter() {
 template <typename T>
 __global__ void encoder_fwd_kernel(T* __restrict__ x, const int* __restrict__ tokens,
                                    const T* __restrict__ wte, const T* __restrict__ wpe,
-                                   int M, int T_, int C, int V, int* err) {
+                                   int M, int T_, int C, int V, int* err, int pos0) {
   constexpr int VE = 16 / sizeof(T);
   const int vpr = C / VE;
   long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -35,7 +35,7 @@ __global__ void encoder_fwd_kernel(T* __restrict__ x, const int* __restrict__ to
     atomicOr(err, DEV_ERR_BAD_TOKEN);
     tok = tok < 0 ? 0 : V - 1;
   }
-  int t = p % T_;
+  int t = pos0 + p % T_;
   Vec16<T> a = ld16(wte + (size_t)tok * C + c);
   Vec16<T> b = ld16(wpe + (size_t)t * C + c);
   Vec16<T> o;
@@ -45,16 +45,16 @@ __global__ void encoder_fwd_kernel(T* __restrict__ x, const int* __restrict__ to
 }
 
 cudaError_t encoder_forward(DType t, void* x, const int* tokens, const void* wte, const void* wpe,
-                            int B, int T_, int C, int V, int* err, cudaStream_t s) {
+                            int B, int T_, int C, int V, int* err, cudaStream_t s, int pos0) {
   int M = B * T_;
   if (t == DType::BF16) {
     long long n = (long long)M * (C / 8);
     encoder_fwd_kernel<bf16><<<ceil_div(n, 256), 256, 0, s>>>(
-        (bf16*)x, tokens, (const bf16*)wte, (const bf16*)wpe, M, T_, C, V, err); count_launches(1);
+        (bf16*)x, tokens, (const bf16*)wte, (const bf16*)wpe, M, T_, C, V, err, pos0); count_launches(1);
   } else {
     long long n = (long long)M * (C / 4);
     encoder_fwd_kernel<float><<<ceil_div(n, 256), 256, 0, s>>>(
-        (float*)x, tokens, (const float*)wte, (const float*)wpe, M, T_, C, V, err); count_launches(1);
+        (float*)x, tokens, (const float*)wte, (const float*)wpe, M, T_, C, V, err, pos0); count_launches(1);
   }
   return last();
 }

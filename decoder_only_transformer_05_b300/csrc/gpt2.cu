@@ -119,6 +119,10 @@ struct gpt2 {
   void *lnf = nullptr, *logits = nullptr;
   float *lnf_mean = nullptr, *lnf_rstd = nullptr, *losses = nullptr;
   int* argmax = nullptr;
+  // inference: per layer the keys and values of every position so far, [Bmax][T][2C]
+  void* kvcache = nullptr;
+  int dec_B = 0, dec_len = 0;   // batch and length of the cached sequences (0: none)
+  void* kv(int layer) { return (char*)kvcache + (size_t)layer * Bmax * T * 2 * C * es; }
   // backward scratch
   void *dres = nullptr, *dln = nullptr, *datt = nullptr, *dqkv = nullptr, *dfch = nullptr;
   float* Dbuf = nullptr;
@@ -371,6 +375,7 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   size_t o_enc = plan(encoder_backward_scratch_bytes((int)M, h->Vp));
   size_t o_err = plan(64), o_loss = plan(64), o_norm = plan(64);
   size_t o_mbtok = plan(M * 4), o_mbtgt = plan(M * 4);
+  size_t o_kv = plan(L * M * 2 * C * es);
   h->amem_bytes = need;
   if (cudaError_t e = cudaMalloc(&h->amem, need); e != cudaSuccess) {
     cudaGetLastError();
@@ -398,6 +403,7 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   h->enc_scratch = a + o_enc;
   h->d_err = (int*)(a + o_err); h->d_loss = (float*)(a + o_loss); h->d_norm = (float*)(a + o_norm);
   h->mb_tok = (int32_t*)(a + o_mbtok); h->mb_tgt = (int32_t*)(a + o_mbtgt);
+  h->kvcache = a + o_kv;
 
   // ---- deferred gradient partials (zeroed; see the handle)
   {
@@ -601,6 +607,7 @@ extern "C" int gpt2_forward(gpt2_handle h, const int32_t* tokens, const int32_t*
   cudaStream_t s = h->stream;
   h->have_targets = false;
   h->last_B = B; h->last_T = T; h->last_tokens = tokens;
+  h->dec_len = 0;   // the activations no longer match a decode cache
   const double es = (double)h->es;
 
   size_t pi = prof_begin(h, PC_ENC);
@@ -813,6 +820,7 @@ extern "C" int gpt2_forward_backward(gpt2_handle h, const int32_t* tokens,
     CK(cudaGraphLaunch(g.exec, h->stream));
     count_launches((int)g.launches);
     // host-side state the recorded forward and backward leave behind
+    h->dec_len = 0;
     h->have_targets = true;
     h->last_B = B; h->last_T = T; h->last_tokens = h->mb_tok;
     h->grads_pending = true;
@@ -821,6 +829,73 @@ extern "C" int gpt2_forward_backward(gpt2_handle h, const int32_t* tokens,
   // first call with this shape: run it, then record it for the next calls
   int rc = microbatch_eager(h, B, T, loss_scale);
   return rc ? rc : microbatch_capture(h, B, T, loss_scale);
+}
+
+// ------------------------------------------------------------------ inference (KV cache)
+extern "C" int gpt2_prefill(gpt2_handle h, const int32_t* tokens, int32_t B, int32_t T0,
+                            int32_t* next) {
+  if (!h || !tokens || !next) return fail(GPT2_ERR_ARG, "null argument");
+  int rc = gpt2_forward(h, tokens, nullptr, B, T0, nullptr);
+  if (rc) return rc;
+  cudaStream_t s = h->stream;
+  for (int l = 0; l < h->L; ++l)
+    CKL(kv_cache_store(h->dt, h->kv(l), h->qkv[l], B, T0, 0, T0, h->T, h->C, s));
+  CKL(gather_last(next, h->argmax, B, T0, s));
+  h->dec_B = B;
+  h->dec_len = T0;
+  return GPT2_OK;
+}
+
+extern "C" int gpt2_decode_step(gpt2_handle h, const int32_t* tokens, int32_t B, int32_t* next) {
+  if (!h || !tokens || !next) return fail(GPT2_ERR_ARG, "null argument");
+  if (h->dec_len <= 0) return fail(GPT2_ERR_STATE, "decode_step needs a prefill first");
+  if (B != h->dec_B) return fail(GPT2_ERR_ARG, "B=%d differs from the prefill's B=%d", B, h->dec_B);
+  const int t = h->dec_len;
+  if (t >= h->T) return fail(GPT2_ERR_SEQ_TOO_LONG, "position %d >= block_size %d", t, h->T);
+  const int C = h->C, L = h->L, Vp = h->Vp;
+  const DType dt = h->dt;
+  cudaStream_t s = h->stream;
+  h->have_targets = false;
+  h->last_B = B; h->last_T = 1; h->last_tokens = tokens;
+  // the new position's activations use rows 0..B-1 of the forward's buffers
+  CKL(encoder_forward(dt, h->x[0], tokens, h->pw(T_WTE), h->pw(T_WPE), B, 1, C, h->V, h->d_err, s, t));
+  for (int l = 0; l < L; ++l) {
+    CKL(layernorm_forward(dt, h->ln1[l], h->ln1_mean[l], h->ln1_rstd[l], h->x[l],
+                          h->pw(T_LN1W, l), h->pw(T_LN1B, l), B, C, s));
+    GemmArgs g = linear_fwd(B, 3 * C, C, h->ln1[l], h->pw(T_QKVW, l), h->qkv[l]);
+    if (h->bias) g.bias = h->pw(T_QKVB, l);
+    CKL(run_gemm(h, g));
+    CKL(kv_cache_store(dt, h->kv(l), h->qkv[l], B, 1, t, 1, h->T, C, s));
+    CKL(attention_decode(dt, h->att[l], h->qkv[l], h->kv(l), B, t, h->T, C, h->H, s));
+    g = linear_fwd(B, C, C, h->att[l], h->pw(T_ATTPROJW, l), h->xmid[l]);
+    if (h->bias) g.bias = h->pw(T_ATTPROJB, l);
+    g.resid = h->x[l];
+    CKL(run_gemm(h, g));
+    CKL(layernorm_forward(dt, h->ln2[l], h->ln2_mean[l], h->ln2_rstd[l], h->xmid[l],
+                          h->pw(T_LN2W, l), h->pw(T_LN2B, l), B, C, s));
+    g = linear_fwd(B, 4 * C, C, h->ln2[l], h->pw(T_FCW, l), h->fcg[l]);
+    if (h->bias) g.bias = h->pw(T_FCB, l);
+    g.epi = h->recompute ? EPI_GELU_FWD_U : EPI_GELU_FWD;
+    g.pre = h->fch[l];
+    CKL(run_gemm(h, g));
+    g = linear_fwd(B, C, 4 * C, h->fcg[l], h->pw(T_FCPROJW, l), h->x[l + 1]);
+    if (h->bias) g.bias = h->pw(T_FCPROJB, l);
+    g.resid = h->xmid[l];
+    CKL(run_gemm(h, g));
+  }
+  CKL(layernorm_forward(dt, h->lnf, h->lnf_mean, h->lnf_rstd, h->x[L], h->pw(T_LNFW),
+                        h->pw(T_LNFB), B, C, s));
+  CKL(run_gemm(h, linear_fwd(B, Vp, C, h->lnf, h->pw(T_WTE), h->logits)));
+  CKL(argmax_rows(dt, h->argmax, h->logits, B, h->V, Vp, s));
+  CK(cudaMemcpyAsync(next, h->argmax, (size_t)B * sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+  h->dec_len = t + 1;
+  return GPT2_OK;
+}
+
+extern "C" int gpt2_decode_length(gpt2_handle h, int32_t* length) {
+  if (!h || !length) return fail(GPT2_ERR_ARG, "null argument");
+  *length = h->dec_len;
+  return GPT2_OK;
 }
 
 extern "C" int gpt2_set_graph_mode(gpt2_handle h, int enabled) {

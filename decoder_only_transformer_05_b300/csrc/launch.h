@@ -71,8 +71,9 @@ int gemm_tc_num_sms();
 void gemm_tc_debug_waits(long long wait_limit_ns, int drop_first_signal);
 
 // ---------------------------------------------------------------- elementwise
+// x[b, t] = wte[tokens[b, t]] + wpe[pos0 + t]
 cudaError_t encoder_forward(DType t, void* x, const int* tokens, const void* wte, const void* wpe,
-                            int B, int T, int C, int V, int* err, cudaStream_t s);
+                            int B, int T, int C, int V, int* err, cudaStream_t s, int pos0 = 0);
 // Deterministic embedding backward: counting sort of positions by token id, then a
 // per-id segmented sum in position order. scratch: encoder_backward_scratch_bytes(M, Vp).
 size_t encoder_backward_scratch_bytes(int M, int Vp);
@@ -136,6 +137,18 @@ cudaError_t attention_backward(DType t, void* dqkv, float* Dbuf, const void* dou
 cudaError_t attention_backward_tc(void* dqkv, float* Dbuf, const void* dout, const void* out,
                                   const void* qkv, const float* lse, int B, int T, int C, int H,
                                   int* err, cudaStream_t s);
+
+// ---------------------------------------------------------------- inference (KV cache)
+// cache [Bmax][Tmax][2C] (K then V of each position): rows i < n of batch b of qkv
+// ([B * Trows, 3C]) go to positions pos0 + i of the cache
+cudaError_t kv_cache_store(DType t, void* cache, const void* qkv, int B, int Trows, int pos0,
+                           int n, int Tmax, int C, cudaStream_t s);
+// One query per (batch, head) at position t: q from qkv row b ([B, 3C], Q third), keys and
+// values of positions 0..t from the cache; out [B, C] (heads concatenated); head size <= 128.
+cudaError_t attention_decode(DType t, void* out, const void* qkv, const void* cache, int B,
+                             int t_pos, int Tmax, int C, int H, cudaStream_t s);
+// out[b] = in[b * T + T - 1]
+cudaError_t gather_last(int* out, const int* in, int B, int T, cudaStream_t s);
 
 // ---------------------------------------------------------------- optimiser
 // partials: norm_partials_count() floats; out[0] = ||g||, out[1] = clip coefficient

@@ -59,6 +59,9 @@ SIGNATURES = {
     "gpt2_zero_grad": (_I, [_P]),
     "gpt2_forward_backward": (_I, [_P, _P, _P, ctypes.c_int32, ctypes.c_int32, _F]),
     "gpt2_set_graph_mode": (_I, [_P, _I]),
+    "gpt2_prefill": (_I, [_P, _P, ctypes.c_int32, ctypes.c_int32, _P]),
+    "gpt2_decode_step": (_I, [_P, _P, ctypes.c_int32, _P]),
+    "gpt2_decode_length": (_I, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "gpt2_adamw_step": (_I, [_P, _F, _F, _F, _F, _F, _F, ctypes.POINTER(_F)]),
     "gpt2_get_loss": (_I, [_P, ctypes.POINTER(_F)]),
     "gpt2_sync": (_I, [_P]),
@@ -231,6 +234,41 @@ class GPT2:
             B, T = tokens.shape
         _check(self.lib.gpt2_forward_backward(self._h, ptr(tokens), ptr(targets), B, T,
                                               loss_scale))
+
+    # ------------------------------------------------------------------ inference
+    def prefill(self, tokens, next_tokens, B=None, T0=None):
+        """Forward over the prompt [B, T0] with the key/value cache filled; the argmax token of
+        each row's last position goes to next_tokens [B] (device int32)."""
+        if B is None:
+            B, T0 = tokens.shape
+        _check(self.lib.gpt2_prefill(self._h, ptr(tokens), B, T0, ptr(next_tokens)))
+
+    def decode_step(self, tokens, next_tokens, B=None):
+        """One new token per row (tokens [B] device int32) through the cached model; its
+        logits' argmax goes to next_tokens [B]."""
+        if B is None:
+            B = tokens.shape[0]
+        _check(self.lib.gpt2_decode_step(self._h, ptr(tokens), B, ptr(next_tokens)))
+
+    @property
+    def decode_length(self):
+        n = ctypes.c_int32()
+        _check(self.lib.gpt2_decode_length(self._h, ctypes.byref(n)))
+        return n.value
+
+    def generate(self, prompt, n_new):
+        """Greedy decoding: prompt [B, T0] (device int32) -> the n_new tokens [B, n_new] chosen
+        by argmax, each fed back as the next input."""
+        import torch
+        B = prompt.shape[0]
+        out = torch.empty(B, n_new, dtype=torch.int32, device=prompt.device)
+        nxt = torch.empty(B, dtype=torch.int32, device=prompt.device)
+        self.prefill(prompt, nxt)
+        for i in range(n_new):
+            out[:, i] = nxt
+            if i + 1 < n_new:
+                self.decode_step(out[:, i].contiguous(), nxt)
+        return out
 
     def set_graph_mode(self, enabled):
         _check(self.lib.gpt2_set_graph_mode(self._h, int(bool(enabled))))

@@ -159,6 +159,29 @@ int gpt2_backward(gpt2_handle h, float loss_scale);
  */
 int gpt2_forward_backward(gpt2_handle h, const int32_t* tokens, const int32_t* targets,
                           int32_t B, int32_t T, float loss_scale);
+/*
+ * Forward-only inference with a key/value cache and greedy (argmax) decoding: the
+ * generation loop of 「从零实现一个最小GPT」 三.8, where each new token's logits come from
+ * the last position, with the keys and values of earlier positions kept per layer instead
+ * of recomputed. Tokens are device int32; sampling is not provided.
+ * gpt2_prefill: runs the forward over the prompt d_tokens [B, T0] (B <= batch_size,
+ *   T0 <= block_size), stores every layer's keys and values of the T0 positions in the
+ *   handle's cache (sized at create for batch_size x block_size) and writes to d_next[B]
+ *   the argmax over the first V logits of each row's last position (lowest index on ties).
+ *   The logits region then holds all B*T0 rows' logits.
+ * gpt2_decode_step: appends d_tokens[B] (one token per row, at position t = the current
+ *   length) to the cached sequences: computes that position through every layer (its
+ *   attention reads the cached keys and values of positions 0..t), stores its keys and
+ *   values, and writes the argmax of its logits to d_next[B]; the logits region holds the
+ *   B rows of logits. GPT2_ERR_STATE without a prefill, GPT2_ERR_ARG if B differs from the
+ *   prefill's, GPT2_ERR_SEQ_TOO_LONG once t = block_size.
+ * Any gpt2_forward / gpt2_forward_backward discards the cache (length 0).
+ */
+int gpt2_prefill(gpt2_handle h, const int32_t* d_tokens, int32_t B, int32_t T0, int32_t* d_next);
+int gpt2_decode_step(gpt2_handle h, const int32_t* d_tokens, int32_t B, int32_t* d_next);
+/* Current length of the cached sequences (0: no cache). */
+int gpt2_decode_length(gpt2_handle h, int32_t* length);
+
 /* Turn graph recording and replay in gpt2_forward_backward on (1) or off (0: every call
  * runs eagerly; the recorded graphs are destroyed). */
 int gpt2_set_graph_mode(gpt2_handle h, int enabled);
