@@ -524,6 +524,76 @@ cudaError_t classifier(DType t, void* logits, float* losses, const int* targets,
   return last();
 }
 
+// ------------------------------------------------------------------ cross-entropy from the
+// lm_head's softmax statistics (EPI_LOGITS_CE): one thread per row merges the row's partials
+// (float2 (m, s) at ce_part[part * M + row], log2 domain) in part order into lse2 = m +
+// log2(s); then one block per row writes the loss and the dlogits in a single streaming pass.
+__global__ void ce_combine_kernel(float* __restrict__ lse2_out, const float2* __restrict__ part,
+                                  int nparts, int M) {
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= M) return;
+  float m = -INFINITY, s = 0.f;
+  for (int k = 0; k < nparts; ++k) {
+    const float2 v = part[(size_t)k * M + row];
+    if (v.x == -INFINITY) continue;   // a part with no column < V
+    online_merge(m, s, v.x, v.y);
+  }
+  lse2_out[row] = m + __log2f(s);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(CLS_THREADS)
+ce_finish_kernel(T* __restrict__ logits, float* __restrict__ losses, const float* __restrict__ lse2s,
+                 const int* __restrict__ targets, int V, int Vp, float inv_M, int* err) {
+  constexpr int VE = 16 / sizeof(T);
+  const int row = blockIdx.x;
+  T* z = logits + (size_t)row * Vp;
+  int y = targets[row];
+  if (y < 0 || y >= V) {
+    if (threadIdx.x == 0) atomicOr(err, DEV_ERR_BAD_TARGET);
+    y = y < 0 ? 0 : V - 1;
+  }
+  const float lse2 = lse2s[row];
+  if (threadIdx.x == 0) losses[row] = lse2 * LN2 - to_f32(z[y]);
+  __syncthreads();   // z[y] is read before any thread overwrites it
+  const int nvec = Vp / VE;
+  auto emit = [&](const Vec16<T>& v, int i) {
+    Vec16<T> o;
+#pragma unroll
+    for (int e = 0; e < VE; ++e) {
+      const int col = i * VE + e;
+      float d = 0.f;
+      if (col < V) {
+        d = fast_exp2(to_f32(v.e[e]) * LOG2E - lse2);
+        if (col == y) d -= 1.0f;
+        d *= inv_M;
+      }
+      o.e[e] = from_f32<T>(d);
+    }
+    st16_cs(z + (size_t)i * VE, o);
+  };
+  // two vectors per step, both loads issued first
+  int i = threadIdx.x;
+  for (; i + CLS_THREADS < nvec; i += 2 * CLS_THREADS) {
+    const Vec16<T> v0 = ld16_cs(z + (size_t)i * VE), v1 = ld16_cs(z + (size_t)(i + CLS_THREADS) * VE);
+    emit(v0, i);
+    emit(v1, i + CLS_THREADS);
+  }
+  if (i < nvec) emit(ld16_cs(z + (size_t)i * VE), i);
+}
+
+cudaError_t ce_from_partials(DType t, void* logits, float* losses, const float* ce_part,
+                             int nparts, const int* targets, int M, int V, int Vp, float* lse_tmp,
+                             int* err, cudaStream_t s) {
+  if (t != DType::BF16 || M <= 0 || nparts <= 0) return cudaErrorInvalidValue;
+  ce_combine_kernel<<<ceil_div(M, 256), 256, 0, s>>>(lse_tmp, (const float2*)ce_part, nparts, M);
+  count_launches(1);
+  ce_finish_kernel<bf16><<<M, CLS_THREADS, 0, s>>>((bf16*)logits, losses, lse_tmp, targets, V, Vp,
+                                                  1.0f / (float)M, err);
+  count_launches(1);
+  return last();
+}
+
 __global__ void mean_loss_kernel(float* out, const float* __restrict__ losses, int M) {
   __shared__ double sh[1024];
   double a = 0.0;

@@ -69,6 +69,7 @@ struct Params {
   const bf16* bias; const bf16* resid; const bf16* aux;
   float scale;
   int* err;
+  int vocab; float* ce_part;    // EPI_LOGITS_CE
   unsigned long long wait_ns;   // limit of every bounded wait (normally TIMEOUT_NS)
   int drop_first_signal;        // test hook: the first accumulator of each block pair is
                                 // never signalled ready, so its epilogue wait runs out
@@ -87,7 +88,8 @@ struct EpiMaps {
 // `inp`: this thread's row of the chunk's input (residual or pre-activation), if any.
 __device__ __forceinline__ void epilogue_chunk(const Params& p, const EpiMaps& maps, int row0,
                                                int col0, int split, uint32_t stg,
-                                               uint32_t taddr, const uint4 (&inp)[4]) {
+                                               uint32_t taddr, const uint4 (&inp)[4],
+                                               float& ce_m, float& ce_s) {
   const int lane = threadIdx.x & 31;
   // bias first, so that its latency overlaps the tensor-memory load
   uint4 bia[4];
@@ -112,13 +114,35 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const EpiMaps& m
   } else {
     uint32_t w[16];
     const uint32_t* in = reinterpret_cast<const uint32_t*>(inp);
-    if (p.epi == EPI_STORE) {
+    if (p.epi == EPI_STORE || p.epi == EPI_LOGITS_CE) {
       if (src) {
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = __fadd2_rn(v[e], bf2_to_f2(in[e]));
       }
 #pragma unroll
       for (int e = 0; e < 16; ++e) w[e] = pack2_bf16(v[e].x, v[e].y);
+      if (p.epi == EPI_LOGITS_CE) {
+        // softmax statistics of the rounded logits of this chunk's columns < vocab, merged
+        // into the running (ce_m, ce_s) of the thread's row (log2 domain)
+        constexpr float L2E = 1.4426950408889634f;
+        float a[32], cm = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float2 z = bf2_to_f2(w[e]);
+          a[2 * e] = col0 + 2 * e < p.vocab ? z.x * L2E : -INFINITY;
+          a[2 * e + 1] = col0 + 2 * e + 1 < p.vocab ? z.y * L2E : -INFINITY;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) cm = fmaxf(cm, a[e]);
+        if (cm != -INFINITY) {
+          float cs = 0.f;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) cs += fast_exp2(a[e] - cm);
+          const float mn = fmaxf(ce_m, cm);
+          ce_s = ce_s * fast_exp2(ce_m - mn) + cs * fast_exp2(cm - mn);
+          ce_m = mn;
+        }
+      }
     } else if (p.epi == EPI_GELU_FWD) {
       uint32_t u[16];
 #pragma unroll
@@ -385,6 +409,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       tc_fence_after();
       const int row0 = mb * BM + q * 32;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      float ce_m = -INFINITY, ce_s = 0.f;   // EPI_LOGITS_CE: this row's stats over the tile half
 #pragma unroll 1
       for (int c = half; c < BN / 32; c += 2) {
         const int col0 = nb * BN + c * 32;
@@ -417,9 +442,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                                                              col0) + j);
           }
         }
-        epilogue_chunk(p, maps, row0, col0, sp, stg, taddr + c * 32, inp);
+        epilogue_chunk(p, maps, row0, col0, sp, stg, taddr + c * 32, inp, ce_m, ce_s);
       }
       if (!ok) break;
+      if (p.epi == EPI_LOGITS_CE && row0 + lane < p.M)   // rows past M are never stored
+        reinterpret_cast<float2*>(p.ce_part)[(size_t)(2 * nb + half) * p.M + row0 + lane] =
+            make_float2(ce_m, ce_s);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty(acc), 0));
@@ -521,6 +549,8 @@ static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
   p.aux = (const bf16*)g.aux;
   p.scale = g.scale;
   p.err = g.err;
+  p.vocab = g.vocab;
+  p.ce_part = g.ce_part;
   {
     const long long w = g_gemm_wait_ns.load(std::memory_order_relaxed);
     p.wait_ns = w > 0 ? (unsigned long long)w : TIMEOUT_NS;
@@ -532,6 +562,9 @@ static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
     return cudaErrorInvalidValue;
   EpiMaps maps;
   memset(&maps, 0, sizeof(maps));
+  if (g.epi == EPI_LOGITS_CE &&
+      (BN != 256 || !g.ce_part || ((uintptr_t)g.ce_part & 7u) || g.bias || g.resid))
+    return cudaErrorInvalidValue;
   if (g.epi == EPI_ACCUM) {
     if (p.splits == 1)
       ok = make_map(&maps.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.accum, g.N, g.M, g.ldo, 32,
@@ -605,6 +638,8 @@ static int pick_bn(int N) {
   return waste * 16 <= N ? 256 : 128;
 }
 
+int gemm_ce_parts(int N) { return 2 * ceil_div(N, 256); }
+
 int gemm_tc_pick_splits(int M, int N, int K, int num_sms) {
   const int bn = pick_bn(N);
   const int tiles = ceil_div(M, tc::BM) * ceil_div(N, bn);
@@ -622,7 +657,7 @@ cudaError_t gemm_bf16_tc(const GemmArgs& g, cudaStream_t s) {
   const int sms = gemm_tc_num_sms();
   GemmArgs a = g;
   if (a.epi == EPI_ACCUM && a.splits <= 0) a.splits = gemm_tc_pick_splits(a.M, a.N, a.K, sms);
-  const int bn = pick_bn(a.N);
+  const int bn = a.epi == EPI_LOGITS_CE ? 256 : pick_bn(a.N);
 #define GEMM_TC_DISPATCH(BN_)                                                  \
   if (!a.a_mn && !a.b_mn) return tc::launch<BN_, false, false>(a, sms, s);     \
   if (!a.a_mn && a.b_mn) return tc::launch<BN_, false, true>(a, sms, s);       \

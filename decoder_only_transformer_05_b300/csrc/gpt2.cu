@@ -128,6 +128,8 @@ struct gpt2 {
   float* Dbuf = nullptr;
   float* splitk_ws = nullptr;
   float* norm_partials = nullptr;
+  float* ce_part = nullptr;   // bf16 lm_head cross-entropy: softmax-statistics partials
+  float* ce_lse = nullptr;    // and the per-row log2-domain lse
   void* enc_scratch = nullptr;
   int* d_err = nullptr;
   float* d_loss = nullptr;
@@ -376,6 +378,8 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   size_t o_err = plan(64), o_loss = plan(64), o_norm = plan(64);
   size_t o_mbtok = plan(M * 4), o_mbtgt = plan(M * 4);
   size_t o_kv = plan(L * M * 2 * C * es);
+  const size_t ce_parts = h->is_bf16 ? (size_t)gemm_ce_parts(h->Vp) : 0;
+  size_t o_cep = plan(ce_parts * M * 8 + 16), o_cel = plan(M * 4);
   h->amem_bytes = need;
   if (cudaError_t e = cudaMalloc(&h->amem, need); e != cudaSuccess) {
     cudaGetLastError();
@@ -404,6 +408,7 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   h->d_err = (int*)(a + o_err); h->d_loss = (float*)(a + o_loss); h->d_norm = (float*)(a + o_norm);
   h->mb_tok = (int32_t*)(a + o_mbtok); h->mb_tgt = (int32_t*)(a + o_mbtgt);
   h->kvcache = a + o_kv;
+  h->ce_part = (float*)(a + o_cep); h->ce_lse = (float*)(a + o_cel);
 
   // ---- deferred gradient partials (zeroed; see the handle)
   {
@@ -646,11 +651,27 @@ extern "C" int gpt2_forward(gpt2_handle h, const int32_t* tokens, const int32_t*
   CKL(layernorm_forward(dt, h->lnf, h->lnf_mean, h->lnf_rstd, h->x[L], h->pw(T_LNFW),
                         h->pw(T_LNFB), M, C, s));
   prof_end(h, pi, (double)M * C * es * 2);
-  CKL(run_gemm(h, linear_fwd(M, Vp, C, h->lnf, h->pw(T_WTE), h->logits)));
-  if (targets) {
+  if (targets && h->is_bf16) {
+    // the lm_head GEMM also writes each row's softmax statistics; one streaming pass then
+    // writes the losses and the dlogits in place
+    GemmArgs g = linear_fwd(M, Vp, C, h->lnf, h->pw(T_WTE), h->logits);
+    g.epi = EPI_LOGITS_CE;
+    g.vocab = h->V;
+    g.ce_part = h->ce_part;
+    CKL(run_gemm(h, g));
     pi = prof_begin(h, PC_CLS);
-    CKL(classifier(dt, h->logits, h->losses, targets, M, h->V, Vp, h->d_err, s));
+    CKL(ce_from_partials(dt, h->logits, h->losses, h->ce_part, gemm_ce_parts(Vp), targets, M,
+                         h->V, Vp, h->ce_lse, h->d_err, s));
     prof_end(h, pi, (double)M * Vp * es * 2);
+  } else {
+    CKL(run_gemm(h, linear_fwd(M, Vp, C, h->lnf, h->pw(T_WTE), h->logits)));
+  }
+  if (targets) {
+    if (!h->is_bf16) {
+      pi = prof_begin(h, PC_CLS);
+      CKL(classifier(dt, h->logits, h->losses, targets, M, h->V, Vp, h->d_err, s));
+      prof_end(h, pi, (double)M * Vp * es * 2);
+    }
     CKL(mean_loss(h->d_loss, h->losses, M, s));
     h->have_targets = true;
   } else {

@@ -27,6 +27,11 @@ enum GemmEpi : int {
   // the backward recomputes gelu'(u) and gelu(u) from it
   EPI_GELU_FWD_U = 4,  // u = v + bias[n]; out = gelu_tanh(u); pre = u
   EPI_GELU_BWD_U = 5,  // u = aux[m, n]; out = v * gelu_tanh'(u); pre = gelu_tanh(u)
+  // lm_head with the cross-entropy's softmax statistics: out = v (the logits, rounded to the
+  // activation type); per row and per 128 columns (a tile half) of the first `vocab`
+  // columns, the log2-domain maximum m and sum of 2^(z log2 e - m) of the rounded logits,
+  // written as float2 to ce_part[part * M + row], part = 2 * column tile + half
+  EPI_LOGITS_CE = 6,
 };
 
 struct GemmArgs {
@@ -48,6 +53,8 @@ struct GemmArgs {
   // sums until the caller folds them in with splitk_fold (which also clears them)
   int defer_partials = 0;
   int* err = nullptr;                       // device error word
+  int vocab = 0;                            // EPI_LOGITS_CE: columns that enter the softmax
+  float* ce_part = nullptr;                 // EPI_LOGITS_CE: [ce_parts(N)][M] float2
 };
 
 // fp32 SIMT GEMM (all operands float).
@@ -64,6 +71,8 @@ cudaError_t splitk_reduce(float* accum, const float* ws, int splits, long long n
 // accum += sum_s ws[s] (fixed order), then ws = 0: folds deferred split-K partials.
 cudaError_t splitk_fold(float* accum, float* ws, int splits, long long n, cudaStream_t s);
 int gemm_tc_num_sms();
+// Number of softmax-statistics partials per row that EPI_LOGITS_CE writes for N columns.
+int gemm_ce_parts(int N);
 // Test hook of the bounded waits: later GEMM launches use wait_limit_ns (<= 0: the default
 // 2 s) as every wait's limit, and with drop_first_signal the first accumulator of each
 // block pair is never signalled ready (its epilogue wait runs out and reports
@@ -105,6 +114,12 @@ cudaError_t layernorm_fold(float* dw, float* db, float* dproj, float* partials, 
 // columns; in place, logits become dlogits = (softmax - onehot) / M (0 in pad columns).
 cudaError_t classifier(DType t, void* logits, float* losses, const int* targets, int M, int V,
                        int Vp, int* err, cudaStream_t s);
+// The cross-entropy after an EPI_LOGITS_CE lm_head: per row, the partials combined in part
+// order into lse; losses[row] = lse - z[y]; then, in place over the logits,
+// dlogits = (softmax - onehot) / M over the first V columns and 0 in [V, Vp).
+cudaError_t ce_from_partials(DType t, void* logits, float* losses, const float* ce_part,
+                             int nparts, const int* targets, int M, int V, int Vp, float* lse_tmp,
+                             int* err, cudaStream_t s);
 // loss_out[0] = mean(losses[0..M))  (one block, fixed order)
 cudaError_t mean_loss(float* loss_out, const float* losses, int M, cudaStream_t s);
 // argmax over the first V columns of each row (lowest index on ties)

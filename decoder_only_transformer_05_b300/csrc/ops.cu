@@ -20,7 +20,7 @@ extern "C" int gpt2_op_gemm(int precision, int M, int N, int K, const void* A, i
                             int64_t ldo, const void* bias, const void* resid, void* pre,
                             const void* aux, float* accum, float scale, int splits,
                             float* workspace, size_t workspace_bytes, void* stream) {
-  if (epi < 0 || epi > 5) return gpt2_set_error(GPT2_ERR_ARG, "bad epilogue");
+  if (epi < 0 || epi > 5) return gpt2_set_error(GPT2_ERR_ARG, "bad epilogue (the lm_head cross-entropy has its own entry point)");
   GemmArgs g;
   g.M = M; g.N = N; g.K = K;
   g.A = A; g.lda = lda; g.a_mn = a_mn != 0;
@@ -84,4 +84,33 @@ extern "C" int gpt2_op_classifier(int precision, void* logits, float* losses,
 extern "C" int gpt2_debug_gemm_waits(int64_t wait_limit_ns, int drop_first_signal) {
   gemm_tc_debug_waits((long long)wait_limit_ns, drop_first_signal);
   return GPT2_OK;
+}
+
+extern "C" size_t gpt2_op_lmhead_ce_scratch_bytes(int M, int Vp) {
+  if (M <= 0 || Vp <= 0) return 0;
+  return (size_t)gemm_ce_parts(Vp) * M * 8 + (size_t)M * 4 + 256;
+}
+
+extern "C" int gpt2_op_lmhead_cross_entropy(int M, int C, int V, int Vp, const void* x,
+                                            const void* wte, const int32_t* targets,
+                                            void* logits, float* losses, void* scratch,
+                                            size_t scratch_bytes, int* err, void* stream) {
+  if (M <= 0 || C <= 0 || V <= 0 || Vp < V || !scratch || ((uintptr_t)scratch & 15u))
+    return gpt2_set_error(GPT2_ERR_ARG, "bad size or scratch");
+  if (scratch_bytes < gpt2_op_lmhead_ce_scratch_bytes(M, Vp))
+    return gpt2_set_error(GPT2_ERR_ARG, "scratch too small");
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t part_bytes = (size_t)gemm_ce_parts(Vp) * M * 8;
+  float* part = (float*)scratch;
+  float* lse = (float*)((char*)scratch + (part_bytes + 255) / 256 * 256);
+  GemmArgs g;
+  g.M = M; g.N = Vp; g.K = C;
+  g.A = x; g.lda = C; g.a_mn = false;
+  g.B = wte; g.ldb = C; g.b_mn = false;
+  g.epi = EPI_LOGITS_CE; g.out = logits; g.ldo = Vp;
+  g.vocab = V; g.ce_part = part; g.err = err;
+  int rc = status(gemm_bf16_tc(g, s));
+  if (rc) return rc;
+  return status(ce_from_partials(DType::BF16, logits, losses, part, gemm_ce_parts(Vp), targets, M,
+                                 V, Vp, lse, err, s));
 }

@@ -21,7 +21,7 @@ ERRORS = {-1: "INVALID_CONFIG", -2: "OOM", -3: "CUDA", -4: "BAD_TOKEN", -5: "SEQ
 FP32, BF16 = 0, 1
 REGION = dict(params=0, grads=1, m=2, v=3, params_bf16=4, logits=5, losses=6, encoded=7,
               argmax=8)
-EPI = dict(store=0, gelu_fwd=1, gelu_bwd=2, accum=3, gelu_fwd_u=4, gelu_bwd_u=5)
+EPI = dict(store=0, gelu_fwd=1, gelu_bwd=2, accum=3, gelu_fwd_u=4, gelu_bwd_u=5, logits_ce=6)
 PROF = dict(gemm=0, attention=1, layernorm=2, classifier=3, encoder=4, optimizer=5, other=6)
 
 
@@ -92,6 +92,8 @@ SIGNATURES = {
     "gpt2_op_layernorm_backward_noalloc": (_I, [_I, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I,
                                                 _I, _F, _P]),
     "gpt2_debug_gemm_waits": (_I, [_I64, _I]),
+    "gpt2_op_lmhead_ce_scratch_bytes": (_SZ, [_I, _I]),
+    "gpt2_op_lmhead_cross_entropy": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
 }
 
 _lib = None
@@ -434,3 +436,18 @@ def debug_gemm_waits(wait_limit_ns=0, drop_first_signal=False):
     """Test hook of the GEMM's bounded waits (see include/gpt2_ops.h); (0, False) = off."""
     lib = load_library()
     _check(lib.gpt2_debug_gemm_waits(int(wait_limit_ns), int(bool(drop_first_signal))))
+
+
+def op_lmhead_ce_scratch_bytes(M, Vp):
+    return load_library().gpt2_op_lmhead_ce_scratch_bytes(M, Vp)
+
+
+def op_lmhead_cross_entropy(M, C, V, Vp, x, wte, targets, logits, losses, scratch, err,
+                            stream=None):
+    """bf16 lm_head GEMM with the cross-entropy's softmax statistics in its epilogue, then
+    the losses and the dlogits (in place over the logits) in one pass."""
+    lib = load_library()
+    _check(lib.gpt2_op_lmhead_cross_entropy(M, C, V, Vp, ptr(x), ptr(wte), ptr(targets),
+                                            ptr(logits), ptr(losses), ptr(scratch),
+                                            scratch.numel() * scratch.element_size(), ptr(err),
+                                            stream_handle(stream)))

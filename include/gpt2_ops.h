@@ -97,6 +97,21 @@ int gpt2_op_classifier(int precision, void* logits, float* losses, const int32_t
                        int M, int V, int Vp, int* err, void* stream);
 
 /*
+ * The tied lm_head with the cross-entropy fused into it (bf16 only): logits = x wte^T
+ * ([M, C] x [Vp, C]^T, rounded to bf16), whose GEMM epilogue also produces every row's
+ * softmax statistics (maximum and sum of exponentials per 128 columns of the first V), then
+ * one streaming pass: losses[row] = logsumexp(z[:V]) - z[target] and, in place over the
+ * logits, dlogits = (softmax - onehot) / M in [0, V) and 0 in [V, Vp) (the loss and its
+ * gradient of 「从零实现一个最小GPT」 三.7, F.cross_entropy with the mean over rows).
+ * scratch: gpt2_op_lmhead_ce_scratch_bytes(M, Vp) bytes, 16-byte aligned. Vp % 64 == 0.
+ * err: device int, OR-ed with 4 when a target is outside [0, V).
+ */
+size_t gpt2_op_lmhead_ce_scratch_bytes(int M, int Vp);
+int gpt2_op_lmhead_cross_entropy(int M, int C, int V, int Vp, const void* x, const void* wte,
+                                 const int32_t* targets, void* logits, float* losses,
+                                 void* scratch, size_t scratch_bytes, int* err, void* stream);
+
+/*
  * Test hook for failure detection; the pages have no counterpart. Every mbarrier wait in the
  * tensor-core GEMM is bounded: when one runs out, the kernel sets GPT2_ERR_TIMEOUT in the
  * device error word it was given (a handle's word: reported by its next gpt2_sync /

@@ -321,3 +321,36 @@ def test_classifier(prec, M, V, Vp):
     assert rel_inf(got[:, :V], d) < tol
     assert np.all(got[:, V:] == 0.0)
     assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("M,C,V,Vp", [(300, 128, 1000, 1088), (1024, 768, 50257, 50304)])
+def test_lmhead_cross_entropy_fused(M, C, V, Vp):
+    """The lm_head GEMM with the softmax statistics in its epilogue, then one pass for the
+    losses and dlogits, against the oracle's cross-entropy of the same bf16 logits; the pad
+    rows of wte are set large so the pad logits are large, and must still be ignored."""
+    x = dev(rnd((M, C), 50, 1.0), torch.bfloat16)
+    w = rnd((Vp, C), 51, 0.1)
+    w[V:] = 0.5                       # pad logits ~ 0.5 * sum(x): large
+    wte = dev(w, torch.bfloat16)
+    tgt = np.random.default_rng(52).integers(0, V, size=M).astype(np.int32)
+    logits = torch.empty(M, Vp, dtype=torch.bfloat16, device="cuda")
+    losses = torch.empty(M, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scratch = torch.empty(G.op_lmhead_ce_scratch_bytes(M, Vp) // 4 + 4, device="cuda")
+    G.op_lmhead_cross_entropy(M, C, V, Vp, x, wte, torch.tensor(tgt).cuda(), logits, losses,
+                              scratch, err)
+    # the same logits through the plain GEMM, rounded to bf16 as the fused one rounds them
+    z = torch.empty(M, Vp, dtype=torch.bfloat16, device="cuda")
+    G.op_gemm("bf16", M, Vp, C, x, C, False, wte, C, False, "store", out=z, ldo=Vp)
+    torch.cuda.synchronize()
+    zb = host(z)
+    assert np.abs(zb[:, V:]).max() > 10.0          # the pad logits are large
+    rl, probs = O.cross_entropy_forward(zb[:, :V], tgt.astype(np.int64))
+    np.testing.assert_allclose(losses.cpu().numpy(), rl, rtol=0, atol=1e-4)
+    d = probs.copy()
+    d[np.arange(M), tgt] -= 1.0
+    d /= M
+    got = host(logits)
+    assert rel_inf(got[:, :V], d) < 1e-2
+    assert np.all(got[:, V:] == 0.0)
+    assert int(err.item()) == 0
