@@ -699,6 +699,46 @@ cudaError_t splitk_fold(float* accum, float* ws, int splits, long long n, cudaSt
   return last();
 }
 
+// The same fold, run by a fixed grid of FOLD_BLOCKS blocks (grid-stride), each block also
+// writing the sum of squares of the final values it wrote to nparts[blockIdx.x]: the
+// gradient norm's share of this tensor, produced while the final values pass by.
+constexpr int FOLD_BLOCKS = 148;
+int fold_norm_blocks() { return FOLD_BLOCKS; }
+
+__global__ void __launch_bounds__(256)
+splitk_fold_norm_kernel(float* __restrict__ accum, float* __restrict__ ws, int splits,
+                        long long n4, long long n, float* __restrict__ nparts) {
+  __shared__ float sh[8];
+  float q = 0.f;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    float4 a = reinterpret_cast<float4*>(accum)[i];
+    for (int k = 0; k < splits; ++k) {
+      const float4 w = __ldcs(reinterpret_cast<const float4*>(ws + (size_t)k * n) + i);
+      a.x += w.x; a.y += w.y; a.z += w.z; a.w += w.w;
+      __stcs(reinterpret_cast<float4*>(ws + (size_t)k * n) + i, make_float4(0.f, 0.f, 0.f, 0.f));
+    }
+    reinterpret_cast<float4*>(accum)[i] = a;
+    q += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
+  }
+  q = warp_sum(q);
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = q;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int k = 0; k < 8; ++k) t += sh[k];
+    nparts[blockIdx.x] = t;
+  }
+}
+
+cudaError_t splitk_fold_norm(float* accum, float* ws, int splits, long long n, float* nparts,
+                             cudaStream_t s) {
+  if (n % 4) return cudaErrorInvalidValue;
+  splitk_fold_norm_kernel<<<FOLD_BLOCKS, 256, 0, s>>>(accum, ws, splits, n / 4, n, nparts);
+  count_launches(1);
+  return last();
+}
+
 // =====================================================================================
 // Global gradient norm and clip coefficient, on device (no host sync):
 // out[0] = ||g||_2, out[1] = max_norm > 0 ? min(1, max_norm / (||g|| + 1e-6)) : 1.
@@ -736,6 +776,60 @@ __global__ void norm_finish_kernel(float* out, const float* __restrict__ partial
   float nrm = (float)sqrt(s);
   out[0] = nrm;
   out[1] = max_norm > 0.f ? fminf(1.0f, max_norm / (nrm + 1e-6f)) : 1.0f;
+}
+
+// The same over many partials: thread i adds partials i, i + 1024, ... in order (double),
+// then a fixed tree; deterministic.
+__global__ void __launch_bounds__(1024)
+norm_finish_many_kernel(float* out, const float* __restrict__ partials, int np, float max_norm) {
+  __shared__ double sh[1024];
+  double a = 0.0;
+  for (int k = threadIdx.x; k < np; k += 1024) a += (double)partials[k];
+  sh[threadIdx.x] = a;
+  __syncthreads();
+  for (int o = 512; o > 0; o >>= 1) {
+    if ((int)threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const float nrm = (float)sqrt(sh[0]);
+    out[0] = nrm;
+    out[1] = max_norm > 0.f ? fminf(1.0f, max_norm / (nrm + 1e-6f)) : 1.0f;
+  }
+}
+
+// Sums of squares over a list of [offset, offset + count) ranges of g, one block per range
+// (ranges of at most a few hundred thousand elements), into partials[block].
+__global__ void __launch_bounds__(256)
+sumsq_ranges_kernel(float* __restrict__ partials, const float* __restrict__ g,
+                    const long long* __restrict__ ranges) {
+  __shared__ float sh[8];
+  const long long off = ranges[2 * blockIdx.x], cnt = ranges[2 * blockIdx.x + 1];
+  float a = 0.f;
+  for (long long i = threadIdx.x; i < cnt; i += blockDim.x) {
+    const float v = __ldcs(g + off + i);
+    a += v * v;
+  }
+  a = warp_sum(a);
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int k = 0; k < 8; ++k) t += sh[k];
+    partials[blockIdx.x] = t;
+  }
+}
+
+cudaError_t grad_norm_finish(float* out, const float* partials, int np, const float* g,
+                             const long long* d_ranges, int nranges, float* range_parts,
+                             float max_norm, cudaStream_t s) {
+  if (nranges > 0) {
+    sumsq_ranges_kernel<<<nranges, 256, 0, s>>>(range_parts, g, d_ranges);
+    count_launches(1);
+  }
+  norm_finish_many_kernel<<<1, 1024, 0, s>>>(out, partials, np, max_norm);
+  count_launches(1);
+  return last();
 }
 
 cudaError_t grad_norm(float* out, float* partials, const float* g, long long n, float max_norm,

@@ -148,6 +148,13 @@ struct gpt2 {
   char* dmem = nullptr;
   size_t dmem_bytes = 0;
   bool grads_pending = false;
+  // Gradient norm from the folds: when gpt2_adamw_step itself folds the pending partials,
+  // each fold also writes sums of squares of the final values it writes (norm_slots, in
+  // fold order), and only the gradient ranges no fold finalises (wte, wpe, weights without
+  // split partials) are read again for the norm, as items of at most 256K elements.
+  float* norm_slots = nullptr;
+  int norm_fold_slots = 0, norm_items = 0;
+  long long* norm_ranges = nullptr;   // device: [norm_items][offset, count]
 
   // gpt2_forward_backward: token/target copies and one CUDA graph of the micro-batch per
   // (B, T, loss scale)
@@ -314,6 +321,8 @@ extern "C" int gpt2_host_init(const gpt2_config* cfg_in, float* h_out, size_t n)
   return GPT2_OK;
 }
 
+static int plan_norm(gpt2* h, std::vector<long long>& items);
+
 // ------------------------------------------------------------------ create / destroy
 extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   if (!cfg_in || !out) return fail(GPT2_ERR_ARG, "null argument");
@@ -411,6 +420,7 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   h->ce_part = (float*)(a + o_cep); h->ce_lse = (float*)(a + o_cel);
 
   // ---- deferred gradient partials (zeroed; see the handle)
+  std::vector<long long> norm_items;
   {
     size_t dneed = 0;
     auto dplan = [&](size_t floats) { size_t o = dneed; dneed += align256(floats * 4); return o; };
@@ -431,6 +441,14 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
         o_col[l] = dplan(colsum_deferred_partials_floats((int)M, 4 * (int)C));
         o_col[L + l] = dplan(colsum_deferred_partials_floats((int)M, 3 * (int)C));
       }
+    // gradient-norm slots and range list (upper bounds; plan_norm fills them once the
+    // deferred buffers below exist)
+    const size_t max_slots = (size_t)4 * L * fold_norm_blocks() +
+                             (2 * L + 1) * (size_t)layernorm_fold_norm_parts((int)C, true) +
+                             2 * L * (size_t)bias_grad_fold_norm_parts(4 * (int)C);
+    const size_t max_items = P / 262144 + 4 * L + 8;
+    const size_t o_nslots = dplan(max_slots + max_items + 64);
+    const size_t o_nranges = dplan(max_items * 4 + 64);   // long long pairs
     h->dmem_bytes = dneed + 256;
     if (cudaError_t e = cudaMalloc(&h->dmem, h->dmem_bytes); e != cudaSuccess) {
       cudaGetLastError();
@@ -442,6 +460,8 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
                   cudaGetErrorString(e));
     }
     char* d = h->dmem;
+    h->norm_slots = (float*)(d + o_nslots);
+    h->norm_ranges = (long long*)(d + o_nranges);
     for (size_t l = 0; l < L; ++l)
       for (int k = 0; k < 4; ++k) {
         const int i = (int)(l * 4 + k);
@@ -465,6 +485,10 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
       for (size_t l = 0; l < L; ++l)
         h->def_col.push_back({h->gw(T_QKVB, (int)l), (float*)(d + o_col[L + l]), 3 * (int)C});
     }
+    h->norm_fold_slots = plan_norm(h, norm_items);
+    h->norm_items = (int)(norm_items.size() / 2);
+    if ((size_t)h->norm_fold_slots > max_slots || (size_t)h->norm_items > max_items)
+      h->norm_items = -1;   // the fold norm is then not used (never expected)
   }
 
   // ---- initial values
@@ -472,6 +496,10 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   if (cudaMemset(h->pmem, 0, pbytes) != cudaSuccess || cudaMemset(h->amem, 0, need) != cudaSuccess ||
       cudaMemset(h->dmem, 0, h->dmem_bytes) != cudaSuccess)
     rc = fail(GPT2_ERR_CUDA, "cudaMemset failed");
+  if (rc == GPT2_OK && h->norm_items > 0 &&
+      cudaMemcpy(h->norm_ranges, norm_items.data(), norm_items.size() * sizeof(long long),
+                 cudaMemcpyHostToDevice) != cudaSuccess)
+    rc = fail(GPT2_ERR_CUDA, "norm range upload failed");
   if (rc == GPT2_OK && cfg.init) {
     std::vector<float> host(P, 0.0f);
     fill_init(h, host.data());
@@ -578,19 +606,69 @@ static GemmArgs linear_wgrad(int M, int N, int K, const void* dY, const void* X,
   return g;
 }
 
-// Fold the deferred partial sums into the gradient buffer (and clear them).
-static cudaError_t flush_grads(gpt2* h) {
+// Fold the deferred partial sums into the gradient buffer (and clear them). With norm, each
+// fold also writes its sums of squares into the next norm_slots (the order and counts of
+// plan_norm).
+static cudaError_t flush_grads(gpt2* h, bool norm = false) {
   if (!h->grads_pending) return cudaSuccess;
   cudaStream_t s = h->stream;
   cudaError_t e = cudaSuccess;
+  float* slot = h->norm_slots;
   for (auto& d : h->def_wg)
-    if (e == cudaSuccess && d.splits > 1) e = splitk_fold(d.grad, d.ws, d.splits, (long long)d.n, s);
+    if (e == cudaSuccess && d.splits > 1) {
+      if (norm) {
+        e = splitk_fold_norm(d.grad, d.ws, d.splits, (long long)d.n, slot, s);
+        slot += fold_norm_blocks();
+      } else {
+        e = splitk_fold(d.grad, d.ws, d.splits, (long long)d.n, s);
+      }
+    }
   for (auto& d : h->def_ln)
-    if (e == cudaSuccess) e = layernorm_fold(d.dw, d.db, d.dproj, d.part, h->C, s);
+    if (e == cudaSuccess) {
+      e = layernorm_fold(d.dw, d.db, d.dproj, d.part, h->C, s, norm ? slot : nullptr);
+      if (norm) slot += layernorm_fold_norm_parts(h->C, d.dproj != nullptr);
+    }
   for (auto& d : h->def_col)
-    if (e == cudaSuccess) e = bias_grad_fold(d.db, d.part, h->Bmax * h->T, d.N, s);
+    if (e == cudaSuccess) {
+      e = bias_grad_fold(d.db, d.part, h->Bmax * h->T, d.N, s, norm ? slot : nullptr);
+      if (norm) slot += bias_grad_fold_norm_parts(d.N);
+    }
   if (e == cudaSuccess) h->grads_pending = false;
   return e;
+}
+
+// The slots the folds write and the gradient ranges they leave to a separate read, as host
+// data; returns the number of fold slots, the range items in `items`.
+static int plan_norm(gpt2* h, std::vector<long long>& items) {
+  int slots = 0;
+  for (auto& d : h->def_wg) if (d.splits > 1) slots += fold_norm_blocks();
+  for (auto& d : h->def_ln) slots += layernorm_fold_norm_parts(h->C, d.dproj != nullptr);
+  for (auto& d : h->def_col) slots += bias_grad_fold_norm_parts(d.N);
+  // elements no fold finalises: wte, wpe, and the layer weights whose gradient has no
+  // split partials (written whole by their weight-gradient GEMM)
+  std::vector<std::pair<size_t, size_t>> ranges;
+  auto add = [&](size_t off, size_t n) {
+    if (!ranges.empty() && ranges.back().first + ranges.back().second == off) ranges.back().second += n;
+    else ranges.push_back({off, n});
+  };
+  const TensorInfo& te = h->tensors[h->index[T_WTE]];
+  add(te.offset, te.numel);
+  const TensorInfo& tp = h->tensors[h->index[T_WPE]];
+  add(tp.offset, tp.numel);
+  const int kinds[4] = {T_QKVW, T_ATTPROJW, T_FCW, T_FCPROJW};
+  for (int l = 0; l < h->L; ++l)
+    for (int k = 0; k < 4; ++k) {
+      const gpt2::DefWgrad& d = h->def_wg[l * 4 + k];
+      if (d.splits > 1) continue;
+      add((size_t)(h->gw(kinds[k], l) - h->grads), d.n);
+    }
+  constexpr size_t ITEM = 262144;
+  for (auto& r : ranges)
+    for (size_t o = 0; o < r.second; o += ITEM) {
+      items.push_back((long long)(r.first + o));
+      items.push_back((long long)std::min(ITEM, r.second - o));
+    }
+  return slots;
 }
 
 #define CKL(x)                                                                              \
@@ -941,12 +1019,21 @@ extern "C" int gpt2_zero_grad(gpt2_handle h) {
 extern "C" int gpt2_adamw_step(gpt2_handle h, float lr, float beta1, float beta2, float eps,
                                float weight_decay, float grad_clip, float* h_grad_norm) {
   if (!h) return fail(GPT2_ERR_ARG, "null handle");
-  CKL(flush_grads(h));
+  const bool norm = grad_clip > 0.f || h_grad_norm;
+  // when this call folds the pending partials, the folds also produce the norm's sums of
+  // squares of what they finalise, and only the rest of the gradients is read again
+  const bool fold_norm = norm && h->grads_pending && h->norm_items >= 0;
+  CKL(flush_grads(h, fold_norm));
   h->step += 1;
   cudaStream_t s = h->stream;
-  const bool norm = grad_clip > 0.f || h_grad_norm;
   size_t pi = prof_begin(h, PC_OPT);
-  if (norm) CKL(grad_norm(h->d_norm, h->norm_partials, h->grads, (long long)h->P, grad_clip, s));
+  if (fold_norm) {
+    CKL(grad_norm_finish(h->d_norm, h->norm_slots, h->norm_fold_slots + h->norm_items, h->grads,
+                         h->norm_ranges, h->norm_items, h->norm_slots + h->norm_fold_slots,
+                         grad_clip, s));
+  } else if (norm) {
+    CKL(grad_norm(h->d_norm, h->norm_partials, h->grads, (long long)h->P, grad_clip, s));
+  }
   prof_end(h, pi, (double)h->P * 4);
   pi = prof_begin(h, PC_OPT);
   CKL(adamw(h->params, h->grads, h->m, h->v, h->is_bf16 ? (void*)h->params_bf16 : nullptr,

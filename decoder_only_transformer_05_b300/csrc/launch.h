@@ -70,6 +70,10 @@ cudaError_t splitk_reduce(float* accum, const float* ws, int splits, long long n
                           float scale, cudaStream_t s);
 // accum += sum_s ws[s] (fixed order), then ws = 0: folds deferred split-K partials.
 cudaError_t splitk_fold(float* accum, float* ws, int splits, long long n, cudaStream_t s);
+// The same, also writing fold_norm_blocks() sums of squares of the final values to nparts.
+cudaError_t splitk_fold_norm(float* accum, float* ws, int splits, long long n, float* nparts,
+                             cudaStream_t s);
+int fold_norm_blocks();
 int gemm_tc_num_sms();
 // Number of softmax-statistics partials per row that EPI_LOGITS_CE writes for N columns.
 int gemm_ce_parts(int N);
@@ -107,8 +111,11 @@ cudaError_t layernorm_backward(DType t, void* dres, int accumulate, float* dw, f
                                float* partials, int defer, cudaStream_t s);
 // dw += sum of the deferred partials' first C columns, db the next C, dproj (if non-null)
 // the last C; the partials are cleared.
+// With nparts, also writes layernorm_fold_norm_parts(C, dproj) sums of squares of the
+// final values (for the gradient norm), one per block.
 cudaError_t layernorm_fold(float* dw, float* db, float* dproj, float* partials, int C,
-                           cudaStream_t s);
+                           cudaStream_t s, float* nparts = nullptr);
+int layernorm_fold_norm_parts(int C, bool dproj);
 
 // Fused classifier over the logits rows: per row loss = lse - z[y] over the first V
 // columns; in place, logits become dlogits = (softmax - onehot) / M (0 in pad columns).
@@ -134,7 +141,9 @@ size_t colsum_partials_floats(int M, int N);
 size_t colsum_deferred_partials_floats(int M_max, int N);
 cudaError_t bias_grad(DType t, float* db, const void* dy, int M, int N, float scale,
                       float* partials, int defer, cudaStream_t s);
-cudaError_t bias_grad_fold(float* db, float* partials, int M_max, int N, cudaStream_t s);
+cudaError_t bias_grad_fold(float* db, float* partials, int M_max, int N, cudaStream_t s,
+                           float* nparts = nullptr);
+int bias_grad_fold_norm_parts(int N);
 
 // ---------------------------------------------------------------- attention
 // qkv [B, T, 3C] -> out [B, T, C], lse [B, H, T] (natural log). The bf16 path runs the
@@ -168,6 +177,12 @@ cudaError_t gather_last(int* out, const int* in, int B, int T, cudaStream_t s);
 // ---------------------------------------------------------------- optimiser
 // partials: norm_partials_count() floats; out[0] = ||g||, out[1] = clip coefficient
 int norm_partials_count();
+// ||g|| from partial sums of squares already written (partials[0, np)) plus those of the
+// ranges d_ranges[2i], d_ranges[2i + 1] (offset, count) of g, which go to range_parts
+// (inside partials[0, np)); out as grad_norm's.
+cudaError_t grad_norm_finish(float* out, const float* partials, int np, const float* g,
+                             const long long* d_ranges, int nranges, float* range_parts,
+                             float max_norm, cudaStream_t s);
 cudaError_t grad_norm(float* out, float* partials, const float* g, long long n, float max_norm,
                       cudaStream_t s);
 // One AdamW step over n elements (t counts from 1). The gradient is multiplied by

@@ -403,7 +403,7 @@ ln_bwd_kernel(T* __restrict__ dres, int accumulate, float* __restrict__ partials
 __global__ void __launch_bounds__(256)
 column_reduce_kernel(float* __restrict__ out0, float* __restrict__ out1, float* __restrict__ out2,
                      float* __restrict__ partials, int nparts, int N, int nk, int stride,
-                     float scale, int clear) {
+                     float scale, int clear, float* __restrict__ nparts_out) {
   __shared__ float sh[8][33];
   const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
   const int col = blockIdx.x * 32 + lane;   // over nk * N
@@ -422,21 +422,30 @@ column_reduce_kernel(float* __restrict__ out0, float* __restrict__ out1, float* 
   }
   sh[g][lane] = s;
   __syncthreads();
+  float q = 0.f;   // the final values' squares (for the gradient norm)
   if (g == 0 && col < nk * N) {
     float t = 0.f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) t += sh[k][lane];
     const int k = col / N, c = col - k * N;
     float* out = k == 0 ? out0 : (k == 1 ? out1 : out2);
-    if (out) out[c] += scale * t;
+    if (out) {
+      const float f = out[c] + scale * t;
+      out[c] = f;
+      q = f * f;
+    }
+  }
+  if (nparts_out && g == 0) {
+    q = warp_sum(q);
+    if (lane == 0) nparts_out[blockIdx.x] = q;
   }
 }
 
 static cudaError_t column_reduce(float* o0, float* o1, float* o2, float* partials,
                                  int nparts, int N, int nk, int stride, float scale,
-                                 cudaStream_t s, int clear = 0) {
-  column_reduce_kernel<<<ceil_div((long long)nk * N, 32), 256, 0, s>>>(o0, o1, o2, partials, nparts,
-                                                                       N, nk, stride, scale, clear);
+                                 cudaStream_t s, int clear = 0, float* nparts_out = nullptr) {
+  column_reduce_kernel<<<ceil_div((long long)nk * N, 32), 256, 0, s>>>(
+      o0, o1, o2, partials, nparts, N, nk, stride, scale, clear, nparts_out);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -487,10 +496,11 @@ static cudaError_t ln_bwd_dispatch(T* dres, int acc, float* dw, float* db, float
 }
 
 cudaError_t layernorm_fold(float* dw, float* db, float* dproj, float* partials, int C,
-                           cudaStream_t s) {
+                           cudaStream_t s, float* nparts) {
   const int nk = dproj ? 3 : 2;
-  return column_reduce(dw, db, dproj, partials, LNB_MAX_BLOCKS, C, nk, nk * C, 1.0f, s, 1);
+  return column_reduce(dw, db, dproj, partials, LNB_MAX_BLOCKS, C, nk, nk * C, 1.0f, s, 1, nparts);
 }
+int layernorm_fold_norm_parts(int C, bool dproj) { return ceil_div((dproj ? 3 : 2) * C, 32); }
 
 cudaError_t layernorm_backward(DType t, void* dres, int accumulate, float* dw, float* db,
                                float* dproj, const void* dy, const void* x, const void* w,
@@ -607,9 +617,11 @@ cudaError_t bias_grad(DType t, float* db, const void* dy, int M, int N, float sc
   return column_reduce(db, nullptr, nullptr, partials, chunks, N, 1, N, scale, s);
 }
 
-cudaError_t bias_grad_fold(float* db, float* partials, int M_max, int N, cudaStream_t s) {
+cudaError_t bias_grad_fold(float* db, float* partials, int M_max, int N, cudaStream_t s,
+                           float* nparts) {
   return column_reduce(db, nullptr, nullptr, partials, colsum_max_chunks(M_max, N), N, 1, N, 1.0f,
-                       s, 1);
+                       s, 1, nparts);
 }
+int bias_grad_fold_norm_parts(int N) { return ceil_div(N, 32); }
 
 }  // namespace gpt2k
