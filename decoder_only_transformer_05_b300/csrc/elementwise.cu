@@ -699,27 +699,34 @@ cudaError_t splitk_fold(float* accum, float* ws, int splits, long long n, cudaSt
   return last();
 }
 
-// The same fold, run by a fixed grid of FOLD_BLOCKS blocks (grid-stride), each block also
-// writing the sum of squares of the final values it wrote to nparts[blockIdx.x]: the
-// gradient norm's share of this tensor, produced while the final values pass by.
-constexpr int FOLD_BLOCKS = 148;
-int fold_norm_blocks() { return FOLD_BLOCKS; }
+// The same fold, each block also writing the sum of squares of the final values it wrote to
+// nparts[blockIdx.x] (fold_norm_parts(n) blocks): the gradient norm's share of this tensor,
+// produced while the final values pass by.
+int fold_norm_parts(long long n) { return ceil_div(n / 4, 256); }
 
+template <int S>
 __global__ void __launch_bounds__(256)
 splitk_fold_norm_kernel(float* __restrict__ accum, float* __restrict__ ws, int splits,
                         long long n4, long long n, float* __restrict__ nparts) {
   __shared__ float sh[8];
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   float q = 0.f;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
-       i += (long long)gridDim.x * blockDim.x) {
+  if (i < n4) {
     float4 a = reinterpret_cast<float4*>(accum)[i];
-    for (int k = 0; k < splits; ++k) {
-      const float4 w = __ldcs(reinterpret_cast<const float4*>(ws + (size_t)k * n) + i);
-      a.x += w.x; a.y += w.y; a.z += w.z; a.w += w.w;
-      __stcs(reinterpret_cast<float4*>(ws + (size_t)k * n) + i, make_float4(0.f, 0.f, 0.f, 0.f));
+    for (int k0 = 0; k0 < splits; k0 += S) {
+      float4 w[S];
+#pragma unroll
+      for (int k = 0; k < S; ++k)
+        if (k0 + k < splits) w[k] = __ldcs(reinterpret_cast<const float4*>(ws + (size_t)(k0 + k) * n) + i);
+#pragma unroll
+      for (int k = 0; k < S; ++k)
+        if (k0 + k < splits) {
+          a.x += w[k].x; a.y += w[k].y; a.z += w[k].z; a.w += w[k].w;
+          __stcs(reinterpret_cast<float4*>(ws + (size_t)(k0 + k) * n) + i, make_float4(0.f, 0.f, 0.f, 0.f));
+        }
     }
     reinterpret_cast<float4*>(accum)[i] = a;
-    q += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
+    q = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
   }
   q = warp_sum(q);
   if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = q;
@@ -734,7 +741,8 @@ splitk_fold_norm_kernel(float* __restrict__ accum, float* __restrict__ ws, int s
 cudaError_t splitk_fold_norm(float* accum, float* ws, int splits, long long n, float* nparts,
                              cudaStream_t s) {
   if (n % 4) return cudaErrorInvalidValue;
-  splitk_fold_norm_kernel<<<FOLD_BLOCKS, 256, 0, s>>>(accum, ws, splits, n / 4, n, nparts);
+  splitk_fold_norm_kernel<8><<<fold_norm_parts(n), 256, 0, s>>>(accum, ws, splits, n / 4, n,
+                                                                 nparts);
   count_launches(1);
   return last();
 }

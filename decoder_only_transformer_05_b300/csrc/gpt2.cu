@@ -443,7 +443,8 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
       }
     // gradient-norm slots and range list (upper bounds; plan_norm fills them once the
     // deferred buffers below exist)
-    const size_t max_slots = (size_t)4 * L * fold_norm_blocks() +
+    const size_t max_slots = (size_t)L * (fold_norm_parts(3 * C * C) + fold_norm_parts(C * C) +
+                                          2 * fold_norm_parts(4 * C * C)) +
                              (2 * L + 1) * (size_t)layernorm_fold_norm_parts((int)C, true) +
                              2 * L * (size_t)bias_grad_fold_norm_parts(4 * (int)C);
     const size_t max_items = P / 262144 + 4 * L + 8;
@@ -618,7 +619,7 @@ static cudaError_t flush_grads(gpt2* h, bool norm = false) {
     if (e == cudaSuccess && d.splits > 1) {
       if (norm) {
         e = splitk_fold_norm(d.grad, d.ws, d.splits, (long long)d.n, slot, s);
-        slot += fold_norm_blocks();
+        slot += fold_norm_parts((long long)d.n);
       } else {
         e = splitk_fold(d.grad, d.ws, d.splits, (long long)d.n, s);
       }
@@ -641,7 +642,7 @@ static cudaError_t flush_grads(gpt2* h, bool norm = false) {
 // data; returns the number of fold slots, the range items in `items`.
 static int plan_norm(gpt2* h, std::vector<long long>& items) {
   int slots = 0;
-  for (auto& d : h->def_wg) if (d.splits > 1) slots += fold_norm_blocks();
+  for (auto& d : h->def_wg) if (d.splits > 1) slots += fold_norm_parts((long long)d.n);
   for (auto& d : h->def_ln) slots += layernorm_fold_norm_parts(h->C, d.dproj != nullptr);
   for (auto& d : h->def_col) slots += bias_grad_fold_norm_parts(d.N);
   // elements no fold finalises: wte, wpe, and the layer weights whose gradient has no

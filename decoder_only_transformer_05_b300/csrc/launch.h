@@ -70,10 +70,10 @@ cudaError_t splitk_reduce(float* accum, const float* ws, int splits, long long n
                           float scale, cudaStream_t s);
 // accum += sum_s ws[s] (fixed order), then ws = 0: folds deferred split-K partials.
 cudaError_t splitk_fold(float* accum, float* ws, int splits, long long n, cudaStream_t s);
-// The same, also writing fold_norm_blocks() sums of squares of the final values to nparts.
+// The same, also writing fold_norm_parts(n) sums of squares of the final values to nparts.
 cudaError_t splitk_fold_norm(float* accum, float* ws, int splits, long long n, float* nparts,
                              cudaStream_t s);
-int fold_norm_blocks();
+int fold_norm_parts(long long n);
 int gemm_tc_num_sms();
 // Number of softmax-statistics partials per row that EPI_LOGITS_CE writes for N columns.
 int gemm_ce_parts(int N);
