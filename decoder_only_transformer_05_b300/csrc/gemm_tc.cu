@@ -123,21 +123,36 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const EpiMaps& m
       for (int e = 0; e < 16; ++e) w[e] = pack2_bf16(v[e].x, v[e].y);
       if (p.epi == EPI_LOGITS_CE) {
         // softmax statistics of the rounded logits of this chunk's columns < vocab, merged
-        // into the running (ce_m, ce_s) of the thread's row (log2 domain)
+        // into the running (ce_m, ce_s) of the thread's row (log2 domain); the column mask
+        // only in a chunk that reaches past vocab
         constexpr float L2E = 1.4426950408889634f;
-        float a[32], cm = -INFINITY;
+        float2 z[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float2 z = bf2_to_f2(w[e]);
-          a[2 * e] = col0 + 2 * e < p.vocab ? z.x * L2E : -INFINITY;
-          a[2 * e + 1] = col0 + 2 * e + 1 < p.vocab ? z.y * L2E : -INFINITY;
+        for (int e = 0; e < 16; ++e) z[e] = bf2_to_f2(w[e]);
+        if (col0 + 32 > p.vocab) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            if (col0 + 2 * e >= p.vocab) z[e].x = -INFINITY;
+            if (col0 + 2 * e + 1 >= p.vocab) z[e].y = -INFINITY;
+          }
         }
+        float zm0 = fmaxf(z[0].x, z[0].y), zm1 = fmaxf(z[1].x, z[1].y);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) cm = fmaxf(cm, a[e]);
-        if (cm != -INFINITY) {
-          float cs = 0.f;
+        for (int e = 2; e < 16; e += 2) {
+          zm0 = fmaxf(zm0, fmaxf(z[e].x, z[e].y));
+          zm1 = fmaxf(zm1, fmaxf(z[e + 1].x, z[e + 1].y));
+        }
+        const float zm = fmaxf(zm0, zm1);
+        if (zm != -INFINITY) {
+          const float cm = zm * L2E;
+          const float2 l2e2 = make_float2(L2E, L2E), ncm = make_float2(-cm, -cm);
+          float2 cs2 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) cs += fast_exp2(a[e] - cm);
+          for (int e = 0; e < 16; ++e) {
+            const float2 a = __ffma2_rn(z[e], l2e2, ncm);
+            cs2 = __fadd2_rn(cs2, make_float2(fast_exp2(a.x), fast_exp2(a.y)));
+          }
+          const float cs = cs2.x + cs2.y;
           const float mn = fmaxf(ce_m, cm);
           ce_s = ce_s * fast_exp2(ce_m - mn) + cs * fast_exp2(cm - mn);
           ce_m = mn;

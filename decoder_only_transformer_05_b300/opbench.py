@@ -1,7 +1,7 @@
 """Time single kernels of the training step at the GPT-2 124M shapes (B=12, T=1024,
 C=768, H=12, V=50257 padded to 50304) through the op-level C ABI, with CUDA events.
 
-    python -m decoder_only_transformer_05_b300.opbench [--ops gemm,attn,ln,cls] [--iters N]
+    python -m decoder_only_transformer_05_b300.opbench [--ops gemm,attn,ln,cls,ce,decode] [--iters N]
 
 Each line reports the kernel's average duration and its throughput against the
 algorithmic work (2*M*N*K flops for GEMMs, causal attention flops, bytes moved once for
@@ -111,6 +111,58 @@ def run_classifier(iters):
     return [dict(op="classifier", ms=ms, gbs=2 * M * Vp * 2 / (ms * 1e-3) / 1e9)]
 
 
+def run_ce(iters):
+    """The lm_head with the cross-entropy statistics in its epilogue plus the combine and the
+    streaming dlogits pass, against the plain lm_head GEMM plus the two-pass classifier."""
+    x, wte = _bf16(M, C), _bf16(Vp, C)
+    tgt = torch.randint(0, V, (M,), dtype=torch.int32, device="cuda")
+    logits = torch.empty(M, Vp, dtype=torch.bfloat16, device="cuda")
+    losses = torch.empty(M, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scratch = torch.empty(G.op_lmhead_ce_scratch_bytes(M, Vp) // 4 + 4, device="cuda")
+    ms_fused = _time(lambda: G.op_lmhead_cross_entropy(M, C, V, Vp, x, wte, tgt, logits, losses,
+                                                       scratch, err), iters)
+
+    def unfused():
+        G.op_gemm("bf16", M, Vp, C, x, C, False, wte, C, False, "store", out=logits, ldo=Vp)
+        G.op_classifier("bf16", logits, losses, tgt, M, V, Vp, err)
+    ms_unfused = _time(unfused, iters)
+    return [dict(op="lmhead_cross_entropy_fused", ms=ms_fused),
+            dict(op="lmhead_then_classifier", ms=ms_unfused)]
+
+
+def run_decode(iters):
+    """Greedy decoding with the key/value cache on the 124M shape: a 512-token prompt per row
+    (prefill), then `iters` decode steps of one token per row, for 1 and 12 rows."""
+    out = []
+    for rows in (1, 12):
+        m = G.GPT2(vocab_size=V, padded_vocab_size=Vp, block_size=T, n_layer=12, n_head=H,
+                   n_embd=C, batch_size=rows, bias=True, precision="bf16", init=True, seed=5)
+        prompt = torch.randint(0, V, (rows, 512), dtype=torch.int32, device="cuda")
+        nxt = torch.empty(rows, dtype=torch.int32, device="cuda")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        m.prefill(prompt, nxt)
+        torch.cuda.synchronize()
+        e0.record()
+        m.prefill(prompt, nxt)
+        e1.record()
+        torch.cuda.synchronize()
+        ms_pre = e0.elapsed_time(e1)
+        steps = min(iters, T - 512 - 1)
+        e0.record()
+        for _ in range(steps):
+            m.decode_step(nxt, nxt)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        out.append(dict(op=f"decode_step_rows{rows}", ms=ms, tokens_per_s=rows / (ms * 1e-3),
+                        prefill_ms=ms_pre,
+                        # every step reads all bf16 weights once (the lm_head's 77 MB included)
+                        weight_gbs=2 * m.num_params / (ms * 1e-3) / 1e9))
+        m.close()
+    return out
+
+
 def _time(fn, iters):
     for _ in range(2):
         fn()
@@ -147,6 +199,10 @@ def main():
         rows += run_layernorm(a.iters)
     if "cls" in ops:
         rows += run_classifier(a.iters)
+    if "ce" in ops:
+        rows += run_ce(a.iters)
+    if "decode" in ops:
+        rows += run_decode(max(a.iters, 64))
     for r in rows:
         print(json.dumps(r))
 
