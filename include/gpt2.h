@@ -88,8 +88,10 @@ typedef struct {
 } gpt2_config;
 
 /*
- * Create a handle: one device allocation for [params | grads | m | v | bf16 params], one
- * for activations and scratch.
+ * Create a handle: one device allocation for [params | grads | m | v | bf16 params] (the
+ * flat array of 「手写训练脚本」 section 二, which every weight tensor indexes into), one
+ * for activations and scratch. The initialisation with init = 1 follows the _init_weights
+ * of 「从零实现一个最小GPT」 section 三.7 (normal(0, 0.02) weights, zero biases).
  * With recompute = 1 the activation memory holds, per layer, the MLP pre-activation u
  * instead of gelu(u) and gelu'(u), and no LayerNorm outputs: the backward recomputes both
  * LayerNorm outputs of a layer (from the kept residual streams, means and inverse standard
@@ -118,8 +120,10 @@ int gpt2_host_num_params(const gpt2_config* cfg, size_t* n_model, size_t* n_buff
 int gpt2_set_stream(gpt2_handle h, void* cuda_stream);
 
 /*
- * Forward pass on d_tokens [B, T] (int32, row-major, device). T <= block_size,
- * B <= batch_size (GPT2_ERR_SEQ_TOO_LONG otherwise).
+ * Forward pass on d_tokens [B, T] (int32, row-major, device): the model's forward(idx,
+ * targets) of 「从零实现一个最小GPT」 sections 二.7 and 三.7 (embeddings, L blocks, final
+ * LayerNorm, lm_head, mean cross-entropy). T <= block_size, B <= batch_size
+ * (GPT2_ERR_SEQ_TOO_LONG otherwise).
  * With d_targets [B, T] (the next tokens): computes the mean cross-entropy over all B*T
  * positions and overwrites the logits with dlogits = (softmax - onehot)/(B*T), ready
  * for gpt2_backward. If h_loss is non-NULL the call waits and writes the loss there;
@@ -130,7 +134,9 @@ int gpt2_forward(gpt2_handle h, const int32_t* d_tokens, const int32_t* d_target
                  int32_t T, float* h_loss);
 
 /*
- * Backward pass of the last forward (which must have had targets). Adds
+ * Backward pass of the last forward (which must have had targets): the loss.backward() of
+ * the training loop in 「从零实现一个最小GPT」 section 三.9, every layer's gradient written out
+ * by hand (the chain rule through the same steps as the forward, in reverse). Adds
  * loss_scale * d(mean loss)/d(param) to the gradients (gradients accumulate, as in
  * PyTorch; use loss_scale = 1/accum for gradient accumulation). The bf16 path needs
  * T % 4 == 0 (GPT2_ERR_ARG otherwise).
@@ -143,7 +149,9 @@ int gpt2_forward(gpt2_handle h, const int32_t* d_tokens, const int32_t* d_target
 int gpt2_backward(gpt2_handle h, float loss_scale);
 
 /*
- * One micro-batch: gpt2_forward with targets, then gpt2_backward(loss_scale), with the same
+ * One micro-batch of the gradient-accumulation loop of 「4.1 GPT-2 (124M) 复现」 section 2.3
+ * (the caller sums accum of these with loss_scale = 1/accum before gpt2_adamw_step):
+ * gpt2_forward with targets, then gpt2_backward(loss_scale), with the same
  * results and the same state afterwards (the loss stays on the device for gpt2_get_loss).
  * tokens and targets [B, T] int32 may be device or host pointers: they are copied with
  * cudaMemcpyAsync into library-owned buffers on the handle's stream (pinned host memory
@@ -186,12 +194,17 @@ int gpt2_decode_length(gpt2_handle h, int32_t* length);
  * runs eagerly; the recorded graphs are destroyed). */
 int gpt2_set_graph_mode(gpt2_handle h, int enabled);
 
-/* Set every gradient (and every pending partial sum) to zero. */
+/* Set every gradient (and every pending partial sum) to zero: the zero_grad of the training
+   loop in 「从零实现一个最小GPT」 section 三.9. */
 int gpt2_zero_grad(gpt2_handle h);
 
 /*
- * One optimiser step over the whole flat buffer: if grad_clip > 0 the gradients are
- * scaled by min(1, grad_clip / (||g||_2 + 1e-6)), computed on the device; then AdamW
+ * One optimiser step over the whole flat buffer: the optimizer.step() of the training loop
+ * in 「从零实现一个最小GPT」 section 三.9 (AdamW; the learning rate is the caller's, e.g. the
+ * warm-up + cosine schedule whose numbers 「4.1 GPT-2 (124M) 复现」 section 2.3 lists). That
+ * loop has no clipping step; the one here is the usual global-norm clip: if grad_clip > 0
+ * the gradients are scaled by min(1, grad_clip / (||g||_2 + 1e-6)), computed on the
+ * device; then AdamW
  * (decoupled weight decay applied to every parameter, bias-corrected moments, step
  * counter t incremented first, t = 1 on the first call). Gradients are left as they are.
  * If h_grad_norm is non-NULL the call waits and writes ||g||_2 (before clipping).
