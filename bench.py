@@ -42,9 +42,11 @@ WORKLOAD_TEXT = {
 }
 
 
-# DRAM bytes read + written per GEMM launch (the micro-batch's GEMM launches averaged) from
-# an ncu capture of the current GEMM kernel; None until one is taken after its last change
-GEMM_DRAM_BYTES_PER_LAUNCH = None
+# DRAM bytes read + written per GEMM launch: dram__bytes_read.sum + dram__bytes_write.sum
+# averaged over the 588 GEMM launches (4 micro-batches x 147) of the ncu launch list in
+# profiles/gpt2_124m_step_launches.md (the same GEMM kernel as this build; the capture
+# command is given there). Set it back to None whenever the GEMM kernel changes.
+GEMM_DRAM_BYTES_PER_LAUNCH = 111.2e6
 
 
 def peaks():

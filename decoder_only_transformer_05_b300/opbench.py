@@ -68,7 +68,7 @@ def run_gemm(name, kind, N, K, epi, iters):
                     b_mn=True, epi="accum", accum=acc, ldo=K, scale=1.0, splits=0,
                     workspace=ws, workspace_bytes=ws.numel() * 4)
         gm, gn, gk = N, K, M
-    ms = _time(lambda: G.op_gemm(**args), iters)
+    ms = _time(lambda s: G.op_gemm(**args, stream=s), iters)
     return dict(op=name, ms=ms, tflops=2.0 * gm * gn * gk / (ms * 1e-3) / 1e12,
                 shape=[gm, gn, gk])
 
@@ -81,9 +81,10 @@ def run_attention(iters):
     dqkv = torch.empty_like(qkv)
     Dbuf = torch.empty(2, B, H, T, device="cuda")
     flops = 2 * 2 * B * H * (T * (T + 1) / 2) * (C // H)   # causal QK^T and PV
-    ms_f = _time(lambda: G.op_attention_forward("bf16", out, lse, qkv, B, T, C, H), iters)
-    ms_b = _time(lambda: G.op_attention_backward("bf16", dqkv, Dbuf, dout, out, qkv, lse, B, T,
-                                                 C, H), iters)
+    ms_f = _time(lambda s: G.op_attention_forward("bf16", out, lse, qkv, B, T, C, H, stream=s),
+                 iters)
+    ms_b = _time(lambda s: G.op_attention_backward("bf16", dqkv, Dbuf, dout, out, qkv, lse, B,
+                                                   T, C, H, stream=s), iters)
     return [dict(op="attention_fwd", ms=ms_f, tflops=flops / (ms_f * 1e-3) / 1e12),
             dict(op="attention_bwd", ms=ms_b, tflops=2.5 * flops / (ms_b * 1e-3) / 1e12)]
 
@@ -92,11 +93,12 @@ def run_layernorm(iters):
     x, w, b = _bf16(M, C), _bf16(C), _bf16(C)
     y = torch.empty_like(x)
     mean, rstd = torch.empty(M, device="cuda"), torch.empty(M, device="cuda")
-    ms_f = _time(lambda: G.op_layernorm_forward("bf16", y, mean, rstd, x, w, b, M, C), iters)
+    ms_f = _time(lambda s: G.op_layernorm_forward("bf16", y, mean, rstd, x, w, b, M, C, stream=s),
+                 iters)
     dres, dw, db = _bf16(M, C), torch.zeros(C, device="cuda"), torch.zeros(C, device="cuda")
     part = torch.empty(G.op_layernorm_partials_floats(M, C), device="cuda")
-    ms_b = _time(lambda: G.op_layernorm_backward("bf16", dres, 1, dw, db, y, x, w, mean, rstd,
-                                                 M, C, 1.0, part), iters)
+    ms_b = _time(lambda s: G.op_layernorm_backward("bf16", dres, 1, dw, db, y, x, w, mean, rstd,
+                                                   M, C, 1.0, part, stream=s), iters)
     return [dict(op="layernorm_fwd", ms=ms_f, gbs=(2 * M * C * 2 + 8 * M) / (ms_f * 1e-3) / 1e9),
             dict(op="layernorm_bwd", ms=ms_b,
                  gbs=(4 * M * C * 2 + 8 * M) / (ms_b * 1e-3) / 1e9)]
@@ -107,7 +109,8 @@ def run_classifier(iters):
     tgt = torch.randint(0, V, (M,), dtype=torch.int32, device="cuda")
     losses = torch.empty(M, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    ms = _time(lambda: G.op_classifier("bf16", logits, losses, tgt, M, V, Vp, err), iters)
+    ms = _time(lambda s: G.op_classifier("bf16", logits, losses, tgt, M, V, Vp, err, stream=s),
+               iters)
     return [dict(op="classifier", ms=ms, gbs=2 * M * Vp * 2 / (ms * 1e-3) / 1e9)]
 
 
@@ -120,12 +123,13 @@ def run_ce(iters):
     losses = torch.empty(M, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     scratch = torch.empty(G.op_lmhead_ce_scratch_bytes(M, Vp) // 4 + 4, device="cuda")
-    ms_fused = _time(lambda: G.op_lmhead_cross_entropy(M, C, V, Vp, x, wte, tgt, logits, losses,
-                                                       scratch, err), iters)
+    ms_fused = _time(lambda s: G.op_lmhead_cross_entropy(M, C, V, Vp, x, wte, tgt, logits,
+                                                         losses, scratch, err, stream=s), iters)
 
-    def unfused():
-        G.op_gemm("bf16", M, Vp, C, x, C, False, wte, C, False, "store", out=logits, ldo=Vp)
-        G.op_classifier("bf16", logits, losses, tgt, M, V, Vp, err)
+    def unfused(s):
+        G.op_gemm("bf16", M, Vp, C, x, C, False, wte, C, False, "store", out=logits, ldo=Vp,
+                  stream=s)
+        G.op_classifier("bf16", logits, losses, tgt, M, V, Vp, err, stream=s)
     ms_unfused = _time(unfused, iters)
     return [dict(op="lmhead_cross_entropy_fused", ms=ms_fused),
             dict(op="lmhead_then_classifier", ms=ms_unfused)]
@@ -164,14 +168,25 @@ def run_decode(iters):
 
 
 def _time(fn, iters):
-    for _ in range(2):
-        fn()
+    """Average device time of fn(stream) over `iters` back-to-back launches, replayed from a
+    CUDA graph so that the host-side cost of each call (argument marshalling, tensor-map
+    encoding) does not leave the GPU idle between short kernels."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            fn(s)
     torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
+        for _ in range(iters):
+            fn(s)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(iters):
-        fn()
-    e1.record()
+    with torch.cuda.stream(s):
+        g.replay()
+        e0.record()
+        g.replay()
+        e1.record()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / iters
 
