@@ -45,16 +45,18 @@ namespace tc {
 constexpr int BM = 128, BK = 64;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
-constexpr int STG_BYTES = 4096;   // per epilogue warp: 32 rows x 128 B
 
-template <int BN> struct Cfg {
+// XS: the epilogue has a second bf16 output or a TMA-loaded input, so each epilogue warp
+// stages 2 x 4 KB (and the operand ring has one stage fewer)
+template <int BN, bool XS> struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;         // 16 KB: this block's 128 rows of A
   static constexpr int B_BYTES = (BN / 2) * BK * 2;   // this block's half of the B tile
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 6 : 8;    // 192 KB of operands in flight
+  static constexpr int STAGES = BN == 256 ? (XS ? 5 : 6) : (XS ? 6 : 8);   // 144-192 KB in flight
+  static constexpr int STG = XS ? 8192 : 4096;        // per epilogue warp: 32 rows x 128 B (x 2)
   static constexpr int TMEM_COLS = 2 * BN;            // two accumulators
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = STAGES * STAGE + EPI_WARPS * STG_BYTES + 1024 + BAR_BYTES;
+  static constexpr int SMEM = STAGES * STAGE + EPI_WARPS * STG + 1024 + BAR_BYTES;
 };
 
 struct Params {
@@ -76,44 +78,83 @@ struct Params {
 };
 
 // ------------------------------------------------------------------ epilogue
-// One 32x32 chunk: this thread's row `row`, columns [col0, col0 + 32), accumulator v.
-// Results go to the warp's staging buffer `stg` (and `stg + 2048` for the GELU
-// pre-activation); lane 0 then stores the chunk with TMA.
+// One step of an epilogue warp: its 32 rows (thread = row0 + lane) x 64 columns
+// [col0, col0 + 64); `acc` holds the 64 accumulator values of the row (the tensor-memory load
+// complete). The two 32-column halves are handled in turn (bias, input rows, arithmetic on
+// packed fp32 pairs, staging); then lane 0 stores the step with one TMA store per output
+// (a 32 x 64 bf16 box, 128-byte rows), or, for gradient accumulation, two fp32 32 x 32
+// reduce-adds through the slot one after the other.
 struct EpiMaps {
-  CUtensorMap out;   // bf16 [M, N] (64-byte swizzle) or fp32 [M, N] / [splits, M, N] (128-byte)
+  CUtensorMap out;   // bf16 [M, N] (box 64 x 32, 128-byte swizzle) or fp32 [M, N] / [splits, M, N] (box 32 x 32)
   CUtensorMap pre;   // bf16 [M, N]: the second output of EPI_GELU_FWD / _FWD_U / _BWD_U
-  CUtensorMap in;    // bf16 [M, N] pre-activation, EPI_GELU_BWD only
+  CUtensorMap in;    // bf16 [M, N] gelu'(u) rows, EPI_GELU_BWD only
 };
 
-// `inp`: this thread's row of the chunk's input (residual or pre-activation), if any.
-__device__ __forceinline__ void epilogue_chunk(const Params& p, const EpiMaps& maps, int row0,
-                                               int col0, int split, uint32_t stg,
-                                               uint32_t taddr, const uint4 (&inp)[4],
-                                               float& ce_m, float& ce_s) {
+// 16-byte units 4h .. 4h+3 of row r of a 32 x 64 bf16 tile (128 B per row), laid out for a TMA
+// map with 128-byte swizzle: unit j of row r at unit j ^ (r & 7).
+__device__ __forceinline__ void stage_half_bf16(uint32_t buf, int r, int h, const uint32_t (&w)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    st_shared16(buf + r * 128 + (((4 * h + j) ^ (r & 7)) << 4),
+                make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]));
+}
+
+// stg: the warp's staging slot (out in the first 4 KB, the second output in the second).
+// inr: the row's 64 input values (residual, gelu'(u) or u; zeros if none) and bia: the 64
+// bias values, both loaded before the accumulator so that their latency overlaps it.
+__device__ __forceinline__ void epilogue_step(const Params& p, const EpiMaps& maps, int row0,
+                                              int col0, int split, uint32_t stg,
+                                              const uint32_t (&acc)[64], const uint32_t (&inr)[32],
+                                              const uint4 (&bia)[8], float& ce_m, float& ce_s) {
   const int lane = threadIdx.x & 31;
-  // bias first, so that its latency overlaps the tensor-memory load
-  uint4 bia[4];
-  if (p.bias && p.epi != EPI_ACCUM) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) bia[i] = __ldg(reinterpret_cast<const uint4*>(p.bias + col0) + i);
-  }
-  const bool src = p.epi == EPI_GELU_BWD || p.epi == EPI_GELU_BWD_U || (p.epi == EPI_STORE && p.resid);
-  // the accumulator as 16 column pairs (packed two-lane fp32 arithmetic below)
-  float2 v[16];
-  tmem_ld32(taddr, reinterpret_cast<float (&)[32]>(v));
-  if (p.bias && p.epi != EPI_ACCUM) {
-    const uint32_t* b = reinterpret_cast<const uint32_t*>(bia);
-#pragma unroll
-    for (int e = 0; e < 16; ++e) v[e] = __fadd2_rn(v[e], bf2_to_f2(b[e]));
-  }
-  if (lane == 0) bulk_wait_read();
-  __syncwarp();
   if (p.epi == EPI_ACCUM) {
-    stage_row_f32(stg, lane, reinterpret_cast<const float (&)[32]>(v),
-                  (p.splits == 1 || p.defer) ? p.scale : 1.0f);
-  } else {
+    const float s = (p.splits == 1 || p.defer) ? p.scale : 1.0f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (lane == 0) bulk_wait_read();   // the slot's previous stores have read it
+      __syncwarp();
+      float f[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(acc[32 * h + i]);
+      stage_row_f32(stg, lane, f, s);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        if (row0 < p.M) {   // stores start in range; TMA clips the rest
+          if (p.splits == 1) tma_reduce_add_2d(&maps.out, stg, col0 + 32 * h, row0);
+          else if (p.defer) tma_reduce_add_3d(&maps.out, stg, col0 + 32 * h, row0, split);
+          else tma_store_3d(&maps.out, stg, col0 + 32 * h, row0, split);
+        }
+        bulk_commit();
+      }
+    }
+    return;
+  }
+  const bool two = p.epi == EPI_GELU_FWD || p.epi == EPI_GELU_FWD_U || p.epi == EPI_GELU_BWD_U;
+  const bool src = p.epi == EPI_GELU_BWD || p.epi == EPI_GELU_BWD_U || (p.epi == EPI_STORE && p.resid);
+  if (lane == 0) bulk_wait_read();   // the slot's previous stores have read it
+  __syncwarp();
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int c0 = col0 + 32 * h;
+    float2 v[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      v[e] = make_float2(__uint_as_float(acc[32 * h + 2 * e]), __uint_as_float(acc[32 * h + 2 * e + 1]));
+    if (p.bias) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 b4 = bia[4 * h + i];
+        v[4 * i] = __fadd2_rn(v[4 * i], bf2_to_f2(b4.x));
+        v[4 * i + 1] = __fadd2_rn(v[4 * i + 1], bf2_to_f2(b4.y));
+        v[4 * i + 2] = __fadd2_rn(v[4 * i + 2], bf2_to_f2(b4.z));
+        v[4 * i + 3] = __fadd2_rn(v[4 * i + 3], bf2_to_f2(b4.w));
+      }
+    }
+    uint32_t in[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) in[e] = inr[16 * h + e];
     uint32_t w[16];
-    const uint32_t* in = reinterpret_cast<const uint32_t*>(inp);
     if (p.epi == EPI_STORE || p.epi == EPI_LOGITS_CE) {
       if (src) {
 #pragma unroll
@@ -122,18 +163,18 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const EpiMaps& m
 #pragma unroll
       for (int e = 0; e < 16; ++e) w[e] = pack2_bf16(v[e].x, v[e].y);
       if (p.epi == EPI_LOGITS_CE) {
-        // softmax statistics of the rounded logits of this chunk's columns < vocab, merged
+        // softmax statistics of the rounded logits of this half's columns < vocab, merged
         // into the running (ce_m, ce_s) of the thread's row (log2 domain); the column mask
-        // only in a chunk that reaches past vocab
+        // only in a half that reaches past vocab
         constexpr float L2E = 1.4426950408889634f;
         float2 z[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) z[e] = bf2_to_f2(w[e]);
-        if (col0 + 32 > p.vocab) {
+        if (c0 + 32 > p.vocab) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            if (col0 + 2 * e >= p.vocab) z[e].x = -INFINITY;
-            if (col0 + 2 * e + 1 >= p.vocab) z[e].y = -INFINITY;
+            if (c0 + 2 * e >= p.vocab) z[e].x = -INFINITY;
+            if (c0 + 2 * e + 1 >= p.vocab) z[e].y = -INFINITY;
           }
         }
         float zm0 = fmaxf(z[0].x, z[0].y), zm1 = fmaxf(z[1].x, z[1].y);
@@ -167,7 +208,7 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const EpiMaps& m
         u[e] = pack2_bf16(d.x, d.y);
         w[e] = pack2_bf16(g.x, g.y);
       }
-      stage_row_bf16(stg + 2048, lane, u);
+      stage_half_bf16(stg + 4096, lane, h, u);
     } else if (p.epi == EPI_GELU_FWD_U) {   // keep u itself for the recomputing backward
       uint32_t u[16];
 #pragma unroll
@@ -177,7 +218,7 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const EpiMaps& m
         u[e] = pack2_bf16(v[e].x, v[e].y);
         w[e] = pack2_bf16(g.x, g.y);
       }
-      stage_row_bf16(stg + 2048, lane, u);
+      stage_half_bf16(stg + 4096, lane, h, u);
     } else if (p.epi == EPI_GELU_BWD_U) {   // gelu'(u) and gelu(u) recomputed from u
       uint32_t gu[16];
 #pragma unroll
@@ -188,7 +229,7 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const EpiMaps& m
         w[e] = pack2_bf16(o.x, o.y);
         gu[e] = pack2_bf16(g.x, g.y);
       }
-      stage_row_bf16(stg + 2048, lane, gu);
+      stage_half_bf16(stg + 4096, lane, h, gu);
     } else {   // EPI_GELU_BWD
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
@@ -196,30 +237,25 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const EpiMaps& m
         w[e] = pack2_bf16(g.x, g.y);
       }
     }
-    stage_row_bf16(stg, lane, w);
+    stage_half_bf16(stg, lane, h, w);
   }
   fence_proxy_async();
   __syncwarp();
-  if (lane == 0 && row0 < p.M) {   // stores start in range; TMA clips the rest
-    if (p.epi == EPI_ACCUM) {
-      if (p.splits == 1) tma_reduce_add_2d(&maps.out, stg, col0, row0);
-      else if (p.defer) tma_reduce_add_3d(&maps.out, stg, col0, row0, split);
-      else tma_store_3d(&maps.out, stg, col0, row0, split);
-    } else {
+  if (lane == 0) {
+    if (row0 < p.M) {   // stores start in range; TMA clips the rest
       tma_store_2d(&maps.out, stg, col0, row0);
-      if (p.epi == EPI_GELU_FWD || p.epi == EPI_GELU_FWD_U || p.epi == EPI_GELU_BWD_U)
-        tma_store_2d(&maps.pre, stg + 2048, col0, row0);
+      if (two) tma_store_2d(&maps.pre, stg + 4096, col0, row0);
     }
     bulk_commit();
   }
 }
 
 // ------------------------------------------------------------------ kernel
-template <int BN, bool AMN, bool BMN>
+template <int BN, bool AMN, bool BMN, bool XS>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ EpiMaps maps, const Params p) {
-  using Cf = Cfg<BN>;
+  using Cf = Cfg<BN, XS>;
   // the pair MMA: M = 256 (128 rows per block), N = BN
   constexpr uint32_t IDESC = make_idesc(2 * BM, BN, AMN, BMN);
   constexpr uint16_t PAIR = 0x3;
@@ -228,8 +264,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
   const uint32_t staging = base + Cf::STAGES * Cf::STAGE;
-  const uint32_t bars = staging + EPI_WARPS * STG_BYTES;
-  uint8_t* bars_ptr = base_ptr + Cf::STAGES * Cf::STAGE + EPI_WARPS * STG_BYTES;
+  const uint32_t bars = staging + EPI_WARPS * Cf::STG;
+  uint8_t* bars_ptr = base_ptr + Cf::STAGES * Cf::STAGE + EPI_WARPS * Cf::STG;
   // barrier layout (the same in both blocks): full[S] empty[S] tfull[2] tempty[2] final,
   // then the tmem slot and the abort flag. full, tempty and final are used in the even
   // (MMA-issuing) block only.
@@ -377,41 +413,49 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
   } else {
     // ---------------- epilogue warps 2..9 of both blocks; warp % 4 selects the TMEM lane
-    // quarter, and warps w, w + 4 split the tile's 32-column chunks between them
+    // quarter, and warps w, w + 4 split the tile's 64-column steps between them
     const int q = warp & 3, ew = warp - 2, half = ew >> 2;
-    const uint32_t stg = staging + ew * STG_BYTES;
+    const uint32_t stg = staging + ew * Cf::STG;
     if ((p.epi == EPI_GELU_FWD || p.epi == EPI_GELU_FWD_U || p.epi == EPI_GELU_BWD_U) &&
         lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"((unsigned long long)&maps.pre) : "memory");
     }
-    // The GELU pre-activation rows of a chunk come by TMA into the second half of the warp's
-    // staging area, one chunk ahead: chunk k + 1's copy is issued as soon as chunk k's rows
-    // are in registers (measured: 5 % faster than per-thread loads for the fc-proj dgrad;
-    // for the residual of the short K = 768 forward GEMMs the per-thread loads stay faster).
-    const bool has_in = p.epi == EPI_GELU_BWD;
-    const uint32_t in_buf = stg + 2048, ibar = in_bar(ew);
+    // EPI_GELU_BWD: the gelu'(u) rows of a step come by TMA into the second half of the warp's
+    // staging slot, one step ahead: step k + 1's copy is issued as soon as step k's rows are
+    // in registers.
+    const bool has_in = XS && p.epi == EPI_GELU_BWD;
+    const uint32_t in_buf = stg + 4096, ibar = in_bar(ew);
     int n_in = 0;   // input copies consumed (their barrier phases)
     bool in_pending = false;
-    // the warp's chunk after (unit, c): (unit, c + 2) in the same tile, else the first of
-    // the next unit
-    auto next_chunk = [&](int& unit, int& c) -> bool {
+    const bf16* rsrc = p.epi == EPI_GELU_BWD_U ? p.aux : (p.epi == EPI_STORE ? p.resid : nullptr);
+    // the warp's step after (unit, c): (unit, c + 2) in the same tile, else the first of the
+    // next unit in which the warp has a step
+    auto next_step = [&](int& unit, int& c) -> bool {
       int mb, nb, sp;
       decode(unit, mb, nb, sp);
-      if (c + 2 < BN / 32 && nb * BN + (c + 2) * 32 < p.N) { c += 2; return true; }
-      unit += stride;
+      if (c + 2 < BN / 64 && nb * BN + (c + 2) * 64 < p.N) { c += 2; return true; }
       c = half;
-      return unit < units;
+      for (unit += stride; unit < units; unit += stride) {
+        decode(unit, mb, nb, sp);
+        if (nb * BN + half * 64 < p.N) return true;
+      }
+      return false;
     };
     auto issue_in = [&](int unit, int c) {
       int mb, nb, sp;
       decode(unit, mb, nb, sp);
       if (lane == 0) {
-        mbar_expect_tx(ibar, 2048);
-        tma_load_2d(in_buf, &maps.in, ibar, nb * BN + c * 32, mb * BM + q * 32);
+        mbar_expect_tx(ibar, 4096);
+        tma_load_2d(in_buf, &maps.in, ibar, nb * BN + c * 64, mb * BM + q * 32);
       }
       in_pending = true;
     };
-    if (has_in && first < units) issue_in(first, half);
+    if (has_in && first < units) {
+      int u0 = first, c0 = half;
+      int mb, nb, sp;
+      decode(u0, mb, nb, sp);
+      if (nb * BN + half * 64 < p.N || next_step(u0, c0)) issue_in(u0, c0);
+    }
     int tcount = 0;
     for (int unit = first; unit < units; unit += stride, ++tcount) {
       int mb, nb, sp;
@@ -426,38 +470,46 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       float ce_m = -INFINITY, ce_s = 0.f;   // EPI_LOGITS_CE: this row's stats over the tile half
 #pragma unroll 1
-      for (int c = half; c < BN / 32; c += 2) {
-        const int col0 = nb * BN + c * 32;
+      for (int c = half; c < BN / 64; c += 2) {
+        const int col0 = nb * BN + c * 64;
         if (col0 >= p.N) break;
-        uint4 inp[4];
+        uint4 bia[8];
+        if (p.bias && p.epi != EPI_ACCUM) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) bia[j] = __ldg(reinterpret_cast<const uint4*>(p.bias + col0) + j);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) bia[j] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        uint32_t inr[32];
         if (has_in) {
           ok = __all_sync(0xffffffffu, mbar_wait(ibar, (uint32_t)n_in & 1u, abort_flag, p.err, true, p.wait_ns));
           if (!ok) break;
           ++n_in;
           in_pending = false;
-          // row `lane` of the 32 x 32 chunk: 16-byte unit j at j ^ ((lane >> 1) & 3)
+          // row `lane` of the 32 x 64 tile, 128-byte swizzle: 16-byte unit j at j ^ (lane & 7)
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            inp[j] = ld_shared16(in_buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4));
+          for (int j = 0; j < 8; ++j) {
+            const uint4 t = ld_shared16(in_buf + lane * 128 + ((j ^ (lane & 7)) << 4));
+            inr[4 * j] = t.x; inr[4 * j + 1] = t.y; inr[4 * j + 2] = t.z; inr[4 * j + 3] = t.w;
+          }
           __syncwarp();
           fence_proxy_async();
           int nu = unit, nc = c;
-          if (next_chunk(nu, nc)) issue_in(nu, nc);
+          if (next_step(nu, nc)) issue_in(nu, nc);
+        } else if (rsrc && row0 + lane < p.M) {   // rows past M are computed, never stored
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 t = __ldg(reinterpret_cast<const uint4*>(rsrc + (size_t)(row0 + lane) * p.ldo + col0) + j);
+            inr[4 * j] = t.x; inr[4 * j + 1] = t.y; inr[4 * j + 2] = t.z; inr[4 * j + 3] = t.w;
+          }
         } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) inp[j] = make_uint4(0u, 0u, 0u, 0u);
-          // residual rows, or the pre-activation of EPI_GELU_BWD_U (whose second output
-          // needs the staging half that the TMA-prefetched input would use); rows past M are
-          // computed but never stored: TMA clips them
-          const bf16* rsrc = p.epi == EPI_GELU_BWD_U ? p.aux : (p.epi == EPI_STORE ? p.resid : nullptr);
-          if (rsrc && row0 + lane < p.M) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              inp[j] = __ldg(reinterpret_cast<const uint4*>(rsrc + (size_t)(row0 + lane) * p.ldo +
-                                                             col0) + j);
-          }
+          for (int j = 0; j < 32; ++j) inr[j] = 0u;
         }
-        epilogue_chunk(p, maps, row0, col0, sp, stg, taddr + c * 32, inp, ce_m, ce_s);
+        uint32_t r[64];
+        tmem_ld64(taddr + c * 64, r);
+        epilogue_step(p, maps, row0, col0, sp, stg, r, inr, bia, ce_m, ce_s);
       }
       if (!ok) break;
       if (p.epi == EPI_LOGITS_CE && row0 + lane < p.M)   // rows past M are never stored
@@ -467,7 +519,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty(acc), 0));
     }
-    // an input copy issued for a chunk the loop did not reach (abort) lands before exit
+    // an input copy issued for a step the loop did not reach (abort) lands before exit
     if (has_in && in_pending && lane == 0)
       mbar_wait(ibar, (uint32_t)n_in & 1u, abort_flag, nullptr, false);
     if (lane == 0) bulk_wait_all();
@@ -532,12 +584,12 @@ static bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint6
                   box_outer, swz);
 }
 
-template <int BN, bool AMN, bool BMN>
+template <int BN, bool AMN, bool BMN, bool XS>
 static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
-  using Cf = Cfg<BN>;
+  using Cf = Cfg<BN, XS>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, AMN, BMN>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, AMN, BMN, XS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
     if (e != cudaSuccess) return e;
     attr_done = true;
@@ -590,13 +642,11 @@ static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
                     (uint64_t)g.M * g.N);
   } else {
     if ((g.epi == EPI_GELU_BWD || g.epi == EPI_GELU_BWD_U) && !g.aux) return cudaErrorInvalidValue;
-    ok = make_map_bf16(&maps.out, g.out, g.N, g.M, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    ok = make_map_bf16(&maps.out, g.out, g.N, g.M, g.ldo, 64, 32);
     const void* in = g.epi == EPI_GELU_BWD ? g.aux : nullptr;
-    if (ok && in)
-      ok = make_map_bf16(&maps.in, in, g.N, g.M, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (ok && in) ok = make_map_bf16(&maps.in, in, g.N, g.M, g.ldo, 64, 32);
     if (ok && (g.epi == EPI_GELU_FWD || g.epi == EPI_GELU_FWD_U || g.epi == EPI_GELU_BWD_U))
-      ok = g.pre && make_map_bf16(&maps.pre, g.pre, g.N, g.M, g.ldo, 32, 32,
-                                  CU_TENSOR_MAP_SWIZZLE_64B);
+      ok = g.pre && make_map_bf16(&maps.pre, g.pre, g.N, g.M, g.ldo, 64, 32);
   }
   if (!ok) return cudaErrorInvalidValue;
   // clusters of two blocks; as many as can be resident at once (persistent)
@@ -614,13 +664,13 @@ static cudaError_t launch(const GemmArgs& g, int num_sms, cudaStream_t s) {
   static int max_clusters = 0;
   if (!max_clusters) {
     cfg.gridDim = dim3(2 * (num_sms / 2));
-    cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, gemm_kernel<BN, AMN, BMN>, &cfg);
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, gemm_kernel<BN, AMN, BMN, XS>, &cfg);
     if (e != cudaSuccess) return e;
     if (max_clusters <= 0) return cudaErrorInvalidConfiguration;
   }
   const int units = ceil_div(p.num_m, 2) * p.num_n * p.splits;
   cfg.gridDim = dim3(2 * std::min(units, max_clusters));
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel<BN, AMN, BMN>, ma, mb, maps, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel<BN, AMN, BMN, XS>, ma, mb, maps, p);
   count_launches(1);
   if (e != cudaSuccess) return e;
   if (p.splits > 1 && !p.defer)
@@ -673,13 +723,25 @@ cudaError_t gemm_bf16_tc(const GemmArgs& g, cudaStream_t s) {
   GemmArgs a = g;
   if (a.epi == EPI_ACCUM && a.splits <= 0) a.splits = gemm_tc_pick_splits(a.M, a.N, a.K, sms);
   const int bn = a.epi == EPI_LOGITS_CE ? 256 : pick_bn(a.N);
-#define GEMM_TC_DISPATCH(BN_)                                                  \
-  if (!a.a_mn && !a.b_mn) return tc::launch<BN_, false, false>(a, sms, s);     \
-  if (!a.a_mn && a.b_mn) return tc::launch<BN_, false, true>(a, sms, s);       \
-  if (a.a_mn && a.b_mn) return tc::launch<BN_, true, true>(a, sms, s);         \
-  return tc::launch<BN_, true, false>(a, sms, s);
-  if (bn == 256) { GEMM_TC_DISPATCH(256) }
-  GEMM_TC_DISPATCH(128)
+  // a second bf16 output (the GELU epilogues) or a TMA-loaded input needs the wide staging
+  const bool xs = a.epi == EPI_GELU_FWD || a.epi == EPI_GELU_FWD_U || a.epi == EPI_GELU_BWD ||
+                  a.epi == EPI_GELU_BWD_U;
+#define GEMM_TC_DISPATCH(BN_, XS_)                                                 \
+  if (!a.a_mn && !a.b_mn) return tc::launch<BN_, false, false, XS_>(a, sms, s);    \
+  if (!a.a_mn && a.b_mn) return tc::launch<BN_, false, true, XS_>(a, sms, s);      \
+  if (a.a_mn && a.b_mn) return tc::launch<BN_, true, true, XS_>(a, sms, s);        \
+  return tc::launch<BN_, true, false, XS_>(a, sms, s);
+  if (xs) {
+    if (a.a_mn) return cudaErrorInvalidValue;   // the GELU epilogues' A operand is K-major
+    if (bn == 256) {
+      if (a.b_mn) return tc::launch<256, false, true, true>(a, sms, s);
+      return tc::launch<256, false, false, true>(a, sms, s);
+    }
+    if (a.b_mn) return tc::launch<128, false, true, true>(a, sms, s);
+    return tc::launch<128, false, false, true>(a, sms, s);
+  }
+  if (bn == 256) { GEMM_TC_DISPATCH(256, false) }
+  GEMM_TC_DISPATCH(128, false)
 #undef GEMM_TC_DISPATCH
 }
 
