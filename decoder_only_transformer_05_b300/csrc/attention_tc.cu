@@ -379,27 +379,29 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
         }
-        // P = exp2(s sl2 - m) as bf16 pairs straight into tensor memory, 32 keys at a time;
-        // the row sum in four independent partials
-        float sp[4] = {0.f, 0.f, 0.f, 0.f};
+        // P = exp2(s sl2 - m) as bf16 pairs straight into tensor memory, 32 keys at a time
+        // (the scaling on packed fp32 pairs); the row sum in two packed partials
+        const float2 sl2x2 = make_float2(sl2, sl2), nm2 = make_float2(-m, -m);
+        float2 sp2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            float p0 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * e]), sl2, -m));
-            float p1 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * e + 1]), sl2, -m));
+            const float2 a = __ffma2_rn(make_float2(__uint_as_float(sr[c][2 * e]),
+                                                    __uint_as_float(sr[c][2 * e + 1])),
+                                        sl2x2, nm2);
+            float2 pv = make_float2(fast_exp2(a.x), fast_exp2(a.y));
             if (diag) {
-              if (c * 32 + 2 * e > r) p0 = 0.f;
-              if (c * 32 + 2 * e + 1 > r) p1 = 0.f;
+              if (c * 32 + 2 * e > r) pv.x = 0.f;
+              if (c * 32 + 2 * e + 1 > r) pv.y = 0.f;
             }
-            sp[(2 * e) & 3] += p0;
-            sp[(2 * e + 1) & 3] += p1;
-            pk[e] = pack2_bf16(p0, p1);
+            sp2[e & 1] = __fadd2_rn(sp2[e & 1], pv);
+            pk[e] = pack2_bf16(pv.x, pv.y);
           }
           tmem_st16(lane_base + p_col + c * 16, pk);
         }
-        l = l * alpha + ((sp[0] + sp[1]) + (sp[2] + sp[3]));
+        l = l * alpha + ((sp2[0].x + sp2[1].x) + (sp2[0].y + sp2[1].y));
         // a moved maximum rescales O (which holds the sum up to the previous block)
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
