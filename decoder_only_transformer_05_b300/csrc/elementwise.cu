@@ -23,8 +23,10 @@ long long& launch_counter() {
 template <typename T>
 __global__ void encoder_fwd_kernel(T* __restrict__ x, const int* __restrict__ tokens,
                                    const T* __restrict__ wte, const T* __restrict__ wpe,
-                                   int M, int T_, int C, int V, int* err, int pos0) {
+                                   int M, int T_, int C, int V, int* err, int pos0,
+                                   const int* __restrict__ pos_dev) {
   constexpr int VE = 16 / sizeof(T);
+  if (pos_dev) pos0 = *pos_dev;
   const int vpr = C / VE;
   long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)M * vpr) return;
@@ -45,16 +47,17 @@ __global__ void encoder_fwd_kernel(T* __restrict__ x, const int* __restrict__ to
 }
 
 cudaError_t encoder_forward(DType t, void* x, const int* tokens, const void* wte, const void* wpe,
-                            int B, int T_, int C, int V, int* err, cudaStream_t s, int pos0) {
+                            int B, int T_, int C, int V, int* err, cudaStream_t s, int pos0,
+                            const int* pos_dev) {
   int M = B * T_;
   if (t == DType::BF16) {
     long long n = (long long)M * (C / 8);
     encoder_fwd_kernel<bf16><<<ceil_div(n, 256), 256, 0, s>>>(
-        (bf16*)x, tokens, (const bf16*)wte, (const bf16*)wpe, M, T_, C, V, err, pos0); count_launches(1);
+        (bf16*)x, tokens, (const bf16*)wte, (const bf16*)wpe, M, T_, C, V, err, pos0, pos_dev); count_launches(1);
   } else {
     long long n = (long long)M * (C / 4);
     encoder_fwd_kernel<float><<<ceil_div(n, 256), 256, 0, s>>>(
-        (float*)x, tokens, (const float*)wte, (const float*)wpe, M, T_, C, V, err, pos0); count_launches(1);
+        (float*)x, tokens, (const float*)wte, (const float*)wpe, M, T_, C, V, err, pos0, pos_dev); count_launches(1);
   }
   return last();
 }
@@ -612,16 +615,27 @@ cudaError_t mean_loss(float* loss_out, const float* losses, int M, cudaStream_t 
   return last();
 }
 
-template <typename T>
+template <typename T, bool VEC>
 __global__ void argmax_kernel(int* out, const T* __restrict__ logits, int V, int Vp) {
+  // one block per row; thread i scans the 16-byte vectors i, i + blockDim, ... (single
+  // elements when the row pitch is not a multiple of 16 bytes; columns increase within a
+  // thread, so its first maximum is kept), then the lowest index among equal maxima wins
+  // across threads
+  constexpr int VE = VEC ? 16 / sizeof(T) : 1;
   __shared__ float sv[32];
   __shared__ int si[32];
   const T* z = logits + (size_t)blockIdx.x * Vp;
   float best = -INFINITY;
   int bi = 0x7fffffff;
-  for (int c = threadIdx.x; c < V; c += blockDim.x) {
-    float v = to_f32(z[c]);
-    if (v > best) { best = v; bi = c; }   // c increases per thread: first max kept
+  for (int c0 = threadIdx.x * VE; c0 < V; c0 += blockDim.x * VE) {
+    alignas(16) T a[VE];
+    if constexpr (VEC) *reinterpret_cast<uint4*>(a) = *reinterpret_cast<const uint4*>(z + c0);
+    else a[0] = z[c0];
+#pragma unroll
+    for (int e = 0; e < VE; ++e) {
+      const float v = to_f32(a[e]);
+      if (c0 + e < V && v > best) { best = v; bi = c0 + e; }
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -641,8 +655,16 @@ __global__ void argmax_kernel(int* out, const T* __restrict__ logits, int V, int
 
 cudaError_t argmax_rows(DType t, int* out, const void* logits, int M, int V, int Vp,
                         cudaStream_t s) {
-  if (t == DType::BF16) { argmax_kernel<bf16><<<M, 256, 0, s>>>(out, (const bf16*)logits, V, Vp); count_launches(1); }
-  else { argmax_kernel<float><<<M, 256, 0, s>>>(out, (const float*)logits, V, Vp); count_launches(1); }
+  // rows as 16-byte vectors where the row pitch keeps them aligned
+  const bool al = ((uintptr_t)logits & 15u) == 0;
+  if (t == DType::BF16) {
+    if (al && Vp % 8 == 0) argmax_kernel<bf16, true><<<M, 1024, 0, s>>>(out, (const bf16*)logits, V, Vp);
+    else argmax_kernel<bf16, false><<<M, 1024, 0, s>>>(out, (const bf16*)logits, V, Vp);
+  } else {
+    if (al && Vp % 4 == 0) argmax_kernel<float, true><<<M, 1024, 0, s>>>(out, (const float*)logits, V, Vp);
+    else argmax_kernel<float, false><<<M, 1024, 0, s>>>(out, (const float*)logits, V, Vp);
+  }
+  count_launches(1);
   return last();
 }
 

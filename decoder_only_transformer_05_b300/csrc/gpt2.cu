@@ -163,6 +163,12 @@ struct gpt2 {
   std::vector<MicroGraph> graphs;
   bool graph_mode = true;
   cudaStream_t cap_stream = nullptr;
+  // gpt2_decode_step: the position on the device (read by the replayed kernels) and one
+  // CUDA graph of the step for the current decode batch
+  int* d_pos = nullptr;
+  cudaGraphExec_t dec_exec = nullptr;
+  int dec_exec_B = 0;
+  long long dec_exec_launches = 0;
 
   // state
   int last_B = 0, last_T = 0;
@@ -373,7 +379,11 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   size_t o_lnf = plan(M * C * es), o_lnfm = plan(M * 4), o_lnfr = plan(M * 4);
   size_t o_logits = plan(M * (size_t)h->Vp * es), o_losses = plan(M * 4), o_argmax = plan(M * 4);
   size_t o_dres = plan(M * C * es), o_dln = plan(M * C * es), o_datt = plan(M * C * es);
-  size_t o_dqkv = plan(M * 3 * C * es), o_dfch = plan(M * 4 * C * es), o_D = plan(2 * BHT * 4);
+  size_t o_dqkv = plan(M * 3 * C * es), o_dfch = plan(M * 4 * C * es);
+  // the attention backward's -D, -lse log2e rows; greedy decoding's attention partials
+  size_t o_D = plan(std::max((size_t)(2 * BHT * 4),
+                             attention_decode_scratch_floats((int)h->Bmax, (int)h->H, (int)h->T,
+                                                             (int)(C / h->H)) * 4));
   // split-K workspace for a tied lm_head gradient that needed one (it does not at these
   // shapes; the per-layer weight gradients use the deferred buffers below)
   size_t ws = 0;
@@ -385,7 +395,7 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   size_t o_np = plan((size_t)norm_partials_count() * 4);
   size_t o_enc = plan(encoder_backward_scratch_bytes((int)M, h->Vp));
   size_t o_err = plan(64), o_loss = plan(64), o_norm = plan(64);
-  size_t o_mbtok = plan(M * 4), o_mbtgt = plan(M * 4);
+  size_t o_mbtok = plan(M * 4), o_mbtgt = plan(M * 4), o_pos = plan(256);
   size_t o_kv = plan(L * M * 2 * C * es);
   const size_t ce_parts = h->is_bf16 ? (size_t)gemm_ce_parts(h->Vp) : 0;
   size_t o_cep = plan(ce_parts * M * 8 + 16), o_cel = plan(M * 4);
@@ -416,6 +426,7 @@ extern "C" int gpt2_create(const gpt2_config* cfg_in, gpt2_handle* out) {
   h->enc_scratch = a + o_enc;
   h->d_err = (int*)(a + o_err); h->d_loss = (float*)(a + o_loss); h->d_norm = (float*)(a + o_norm);
   h->mb_tok = (int32_t*)(a + o_mbtok); h->mb_tgt = (int32_t*)(a + o_mbtgt);
+  h->d_pos = (int*)(a + o_pos);
   h->kvcache = a + o_kv;
   h->ce_part = (float*)(a + o_cep); h->ce_lse = (float*)(a + o_cel);
 
@@ -527,6 +538,7 @@ extern "C" void gpt2_destroy(gpt2_handle h) {
   if (!h) return;
   for (auto& p : h->prof) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
   for (auto& g : h->graphs) cudaGraphExecDestroy(g.exec);
+  if (h->dec_exec) cudaGraphExecDestroy(h->dec_exec);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   if (h->dmem) cudaFree(h->dmem);
   if (h->amem) cudaFree(h->amem);
@@ -570,7 +582,8 @@ static cudaError_t run_gemm(gpt2* h, GemmArgs g, const gpt2::DefWgrad* def = nul
         g.workspace = h->splitk_ws;
       }
     }
-    e = gemm_bf16_tc(g, h->stream);
+    // a handful of rows (the decode step) streams the weights instead of filling 128-row tiles
+    e = g.M <= 16 && gemv_rows_supported(g) ? gemv_rows(g, h->stream) : gemm_bf16_tc(g, h->stream);
   } else {
     e = gemm_f32(g, h->stream);
   }
@@ -941,32 +954,31 @@ extern "C" int gpt2_prefill(gpt2_handle h, const int32_t* tokens, int32_t B, int
   for (int l = 0; l < h->L; ++l)
     CKL(kv_cache_store(h->dt, h->kv(l), h->qkv[l], B, T0, 0, T0, h->T, h->C, s));
   CKL(gather_last(next, h->argmax, B, T0, s));
+  CKL(decode_position(h->d_pos, T0, 0, s));
   h->dec_B = B;
   h->dec_len = T0;
   return GPT2_OK;
 }
 
-extern "C" int gpt2_decode_step(gpt2_handle h, const int32_t* tokens, int32_t B, int32_t* next) {
-  if (!h || !tokens || !next) return fail(GPT2_ERR_ARG, "null argument");
-  if (h->dec_len <= 0) return fail(GPT2_ERR_STATE, "decode_step needs a prefill first");
-  if (B != h->dec_B) return fail(GPT2_ERR_ARG, "B=%d differs from the prefill's B=%d", B, h->dec_B);
-  const int t = h->dec_len;
-  if (t >= h->T) return fail(GPT2_ERR_SEQ_TOO_LONG, "position %d >= block_size %d", t, h->T);
+// The launches of one decode step for B rows at position t: the new tokens come from
+// mb_tok, the position from d_pos (incremented at the end), so that the same launches,
+// recorded once, serve every later position.
+static int decode_launches(gpt2* h, int B, int t) {
   const int C = h->C, L = h->L, Vp = h->Vp;
   const DType dt = h->dt;
   cudaStream_t s = h->stream;
-  h->have_targets = false;
-  h->last_B = B; h->last_T = 1; h->last_tokens = tokens;
   // the new position's activations use rows 0..B-1 of the forward's buffers
-  CKL(encoder_forward(dt, h->x[0], tokens, h->pw(T_WTE), h->pw(T_WPE), B, 1, C, h->V, h->d_err, s, t));
+  CKL(encoder_forward(dt, h->x[0], h->mb_tok, h->pw(T_WTE), h->pw(T_WPE), B, 1, C, h->V,
+                      h->d_err, s, t, h->d_pos));
   for (int l = 0; l < L; ++l) {
     CKL(layernorm_forward(dt, h->ln1[l], h->ln1_mean[l], h->ln1_rstd[l], h->x[l],
                           h->pw(T_LN1W, l), h->pw(T_LN1B, l), B, C, s));
     GemmArgs g = linear_fwd(B, 3 * C, C, h->ln1[l], h->pw(T_QKVW, l), h->qkv[l]);
     if (h->bias) g.bias = h->pw(T_QKVB, l);
     CKL(run_gemm(h, g));
-    CKL(kv_cache_store(dt, h->kv(l), h->qkv[l], B, 1, t, 1, h->T, C, s));
-    CKL(attention_decode(dt, h->att[l], h->qkv[l], h->kv(l), B, t, h->T, C, h->H, s));
+    CKL(kv_cache_store(dt, h->kv(l), h->qkv[l], B, 1, t, 1, h->T, C, s, h->d_pos));
+    CKL(attention_decode(dt, h->att[l], h->qkv[l], h->kv(l), B, t, h->T, C, h->H, s, h->d_pos,
+                         h->Dbuf));
     g = linear_fwd(B, C, C, h->att[l], h->pw(T_ATTPROJW, l), h->xmid[l]);
     if (h->bias) g.bias = h->pw(T_ATTPROJB, l);
     g.resid = h->x[l];
@@ -987,6 +999,59 @@ extern "C" int gpt2_decode_step(gpt2_handle h, const int32_t* tokens, int32_t B,
                         h->pw(T_LNFB), B, C, s));
   CKL(run_gemm(h, linear_fwd(B, Vp, C, h->lnf, h->pw(T_WTE), h->logits)));
   CKL(argmax_rows(dt, h->argmax, h->logits, B, h->V, Vp, s));
+  CKL(decode_position(h->d_pos, -1, 1, s));
+  return GPT2_OK;
+}
+
+static int decode_capture(gpt2* h, int B, int t) {
+  if (!h->cap_stream) CK(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
+  const long long n0 = launch_counter();
+  cudaStream_t user = h->stream;
+  h->stream = h->cap_stream;
+  CK(cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
+  const int rc = decode_launches(h, B, t);   // recorded, not executed
+  cudaGraph_t graph = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(h->cap_stream, &graph);
+  h->stream = user;
+  const long long launches = launch_counter() - n0;
+  launch_counter() = n0;
+  if (rc || e != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    if (rc) return rc;
+    return fail(GPT2_ERR_CUDA, "stream capture of the decode step failed: %s",
+                cudaGetErrorString(e));
+  }
+  cudaGraphExec_t exec = nullptr;
+  const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (ei != cudaSuccess)
+    return fail(GPT2_ERR_CUDA, "cudaGraphInstantiate: %s", cudaGetErrorString(ei));
+  if (h->dec_exec) cudaGraphExecDestroy(h->dec_exec);
+  h->dec_exec = exec;
+  h->dec_exec_B = B;
+  h->dec_exec_launches = launches;
+  return GPT2_OK;
+}
+
+extern "C" int gpt2_decode_step(gpt2_handle h, const int32_t* tokens, int32_t B, int32_t* next) {
+  if (!h || !tokens || !next) return fail(GPT2_ERR_ARG, "null argument");
+  if (h->dec_len <= 0) return fail(GPT2_ERR_STATE, "decode_step needs a prefill first");
+  if (B != h->dec_B) return fail(GPT2_ERR_ARG, "B=%d differs from the prefill's B=%d", B, h->dec_B);
+  const int t = h->dec_len;
+  if (t >= h->T) return fail(GPT2_ERR_SEQ_TOO_LONG, "position %d >= block_size %d", t, h->T);
+  cudaStream_t s = h->stream;
+  CK(cudaMemcpyAsync(h->mb_tok, tokens, (size_t)B * sizeof(int32_t), cudaMemcpyDefault, s));
+  if (h->graph_mode && !h->prof_mask && h->dec_exec && h->dec_exec_B == B) {
+    CK(cudaGraphLaunch(h->dec_exec, s));
+    count_launches((int)h->dec_exec_launches);
+  } else {
+    int rc = decode_launches(h, B, t);
+    // the first step for this batch runs eagerly, then is recorded for the later ones
+    if (!rc && h->graph_mode && !h->prof_mask) rc = decode_capture(h, B, t);
+    if (rc) return rc;
+  }
+  h->have_targets = false;
+  h->last_B = B; h->last_T = 1; h->last_tokens = h->mb_tok;
   CK(cudaMemcpyAsync(next, h->argmax, (size_t)B * sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
   h->dec_len = t + 1;
   return GPT2_OK;
@@ -1004,6 +1069,9 @@ extern "C" int gpt2_set_graph_mode(gpt2_handle h, int enabled) {
   if (!h->graph_mode) {
     for (auto& g : h->graphs) cudaGraphExecDestroy(g.exec);
     h->graphs.clear();
+    if (h->dec_exec) cudaGraphExecDestroy(h->dec_exec);
+    h->dec_exec = nullptr;
+    h->dec_exec_B = 0;
   }
   return GPT2_OK;
 }

@@ -84,9 +84,10 @@ int gemm_ce_parts(int N);
 void gemm_tc_debug_waits(long long wait_limit_ns, int drop_first_signal);
 
 // ---------------------------------------------------------------- elementwise
-// x[b, t] = wte[tokens[b, t]] + wpe[pos0 + t]
+// x[b, t] = wte[tokens[b, t]] + wpe[pos0 + t]; pos0 read from pos_dev on the device if given
 cudaError_t encoder_forward(DType t, void* x, const int* tokens, const void* wte, const void* wpe,
-                            int B, int T, int C, int V, int* err, cudaStream_t s, int pos0 = 0);
+                            int B, int T, int C, int V, int* err, cudaStream_t s, int pos0 = 0,
+                            const int* pos_dev = nullptr);
 // Deterministic embedding backward: counting sort of positions by token id, then a
 // per-id segmented sum in position order. scratch: encoder_backward_scratch_bytes(M, Vp).
 size_t encoder_backward_scratch_bytes(int M, int Vp);
@@ -164,15 +165,27 @@ cudaError_t attention_backward_tc(void* dqkv, float* Dbuf, const void* dout, con
 
 // ---------------------------------------------------------------- inference (KV cache)
 // cache [Bmax][Tmax][2C] (K then V of each position): rows i < n of batch b of qkv
-// ([B * Trows, 3C]) go to positions pos0 + i of the cache
+// ([B * Trows, 3C]) go to positions pos0 + i of the cache (pos0 read from pos_dev on the
+// device if given; the host pos0 is then the value it will hold, for the bounds check)
 cudaError_t kv_cache_store(DType t, void* cache, const void* qkv, int B, int Trows, int pos0,
-                           int n, int Tmax, int C, cudaStream_t s);
+                           int n, int Tmax, int C, cudaStream_t s, const int* pos_dev = nullptr);
 // One query per (batch, head) at position t: q from qkv row b ([B, 3C], Q third), keys and
 // values of positions 0..t from the cache; out [B, C] (heads concatenated); head size <= 128.
+// t read from t_dev on the device if given (t_pos: the value it will hold, for the check).
+// scratch: attention_decode_scratch_floats(B, H, Tmax, C / H) floats (the per-split partials).
 cudaError_t attention_decode(DType t, void* out, const void* qkv, const void* cache, int B,
-                             int t_pos, int Tmax, int C, int H, cudaStream_t s);
+                             int t_pos, int Tmax, int C, int H, cudaStream_t s,
+                             const int* t_dev, float* scratch);
+size_t attention_decode_scratch_floats(int B, int H, int Tmax, int hs);
 // out[b] = in[b * T + T - 1]
 cudaError_t gather_last(int* out, const int* in, int B, int T, cudaStream_t s);
+// bf16 Y = X W^T (+ bias, + residual, tanh-GELU epilogues) for at most 16 rows: the decode
+// step's linear layers, streaming each weight once (gemv_rows_supported says which GemmArgs
+// it takes: K-major operands, N and ldo even, K % 8 == 0, epilogues store / GELU forward)
+bool gemv_rows_supported(const GemmArgs& g);
+cudaError_t gemv_rows(const GemmArgs& g, cudaStream_t s);
+// the device copy of the decode position: *pos_dev = set if set >= 0, else *pos_dev += add
+cudaError_t decode_position(int* pos_dev, int set, int add, cudaStream_t s);
 
 // ---------------------------------------------------------------- optimiser
 // partials: norm_partials_count() floats; out[0] = ||g||, out[1] = clip coefficient

@@ -129,3 +129,31 @@ def test_decode_errors():
         m.decode_step(tok[:1].contiguous(), nxt)     # B differs from the prefill's
     assert e.value.name == "ARG"
     m.close()
+
+
+@pytest.mark.parametrize("name,B", [("char-bf16", 2), ("gpt2-124m-micro", 12)])
+def test_replayed_decode_steps_match_eager_ones(name, B):
+    """After its first step for a batch, gpt2_decode_step replays a recorded graph whose
+    kernels read the position from device memory; the tokens and logits it produces are
+    bit-identical to those of the same steps run eagerly (graph mode off)."""
+    w = S.WORKLOADS[name]
+    T0, n_new = 40, 12
+    prompt, _ = S.batch(w["tok_seed"], 13, B, T0, w["V"], w["dist"], w["s"])
+    runs = []
+    for graph in (True, False):
+        m, params, cfg, w = make(name, B)
+        m.set_graph_mode(graph)
+        nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+        m.prefill(torch.tensor(prompt).cuda(), nxt)
+        toks, logits = [], []
+        for i in range(n_new):
+            m.decode_step(nxt.clone(), nxt)
+            toks.append(nxt.cpu().numpy().copy())
+            logits.append(m.read_region("logits", np.uint16 if w["precision"] != "fp32" else np.float32,
+                                        count=B * w["Vp"]).copy())
+        runs.append((toks, logits))
+        m.close()
+    for a, b in zip(runs[0][0], runs[1][0]):
+        assert np.array_equal(a, b)
+    for a, b in zip(runs[0][1], runs[1][1]):
+        assert np.array_equal(a, b)
