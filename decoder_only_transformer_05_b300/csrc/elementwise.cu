@@ -528,20 +528,44 @@ cudaError_t classifier(DType t, void* logits, float* losses, const int* targets,
 }
 
 // ------------------------------------------------------------------ cross-entropy from the
-// lm_head's softmax statistics (EPI_LOGITS_CE): one thread per row merges the row's partials
-// (float2 (m, s) at ce_part[part * M + row], log2 domain) in part order into lse2 = m +
-// log2(s); then one block per row writes the loss and the dlogits in a single streaming pass.
-__global__ void ce_combine_kernel(float* __restrict__ lse2_out, const float2* __restrict__ part,
-                                  int nparts, int M) {
-  const int row = blockIdx.x * blockDim.x + threadIdx.x;
-  if (row >= M) return;
+// lm_head's softmax statistics (EPI_LOGITS_CE): the row's partials (float2 (m, s) at
+// ce_part[part * M + row], log2 domain) merged into lse2 = m + log2(s). Block: 32 rows (the
+// lanes, so every load of a warp is 32 consecutive rows) x 8 warps; warp g merges the parts
+// g, g + 8, ... in order, then the 8 results are merged in warp order. Then one block per row
+// writes the loss and the dlogits in a single streaming pass.
+constexpr int CEC_WARPS = 8;
+__global__ void __launch_bounds__(32 * CEC_WARPS)
+ce_combine_kernel(float* __restrict__ lse2_out, const float2* __restrict__ part, int nparts,
+                  int M) {
+  __shared__ float sm[CEC_WARPS][32], ss[CEC_WARPS][32];
+  const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
+  const int row = blockIdx.x * 32 + lane;
   float m = -INFINITY, s = 0.f;
-  for (int k = 0; k < nparts; ++k) {
-    const float2 v = part[(size_t)k * M + row];
-    if (v.x == -INFINITY) continue;   // a part with no column < V
-    online_merge(m, s, v.x, v.y);
+  if (row < M) {
+    int k = g;
+    for (; k + 3 * CEC_WARPS < nparts; k += 4 * CEC_WARPS) {   // four loads in flight
+      float2 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = part[(size_t)(k + i * CEC_WARPS) * M + row];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (v[i].x != -INFINITY) online_merge(m, s, v[i].x, v[i].y);   // -inf: no column < V
+    }
+    for (; k < nparts; k += CEC_WARPS) {
+      const float2 v = part[(size_t)k * M + row];
+      if (v.x != -INFINITY) online_merge(m, s, v.x, v.y);
+    }
   }
-  lse2_out[row] = m + __log2f(s);
+  sm[g][lane] = m;
+  ss[g][lane] = s;
+  __syncthreads();
+  if (g == 0 && row < M) {
+    float mm = -INFINITY, sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < CEC_WARPS; ++w)
+      if (sm[w][lane] != -INFINITY) online_merge(mm, sum, sm[w][lane], ss[w][lane]);
+    lse2_out[row] = mm + __log2f(sum);
+  }
 }
 
 template <typename T>
@@ -589,7 +613,8 @@ cudaError_t ce_from_partials(DType t, void* logits, float* losses, const float* 
                              int nparts, const int* targets, int M, int V, int Vp, float* lse_tmp,
                              int* err, cudaStream_t s) {
   if (t != DType::BF16 || M <= 0 || nparts <= 0) return cudaErrorInvalidValue;
-  ce_combine_kernel<<<ceil_div(M, 256), 256, 0, s>>>(lse_tmp, (const float2*)ce_part, nparts, M);
+  ce_combine_kernel<<<ceil_div(M, 32), 32 * CEC_WARPS, 0, s>>>(lse_tmp, (const float2*)ce_part,
+                                                                nparts, M);
   count_launches(1);
   ce_finish_kernel<bf16><<<M, CLS_THREADS, 0, s>>>((bf16*)logits, losses, lse_tmp, targets, V, Vp,
                                                   1.0f / (float)M, err);
