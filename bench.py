@@ -42,11 +42,11 @@ WORKLOAD_TEXT = {
 }
 
 
-# DRAM bytes read + written per GEMM launch: dram__bytes_read.sum + dram__bytes_write.sum
-# averaged over the 588 GEMM launches (4 micro-batches x 147) of the ncu launch list in
-# profiles/gpt2_124m_step_launches.md (the same GEMM kernel as this build; the capture
-# command is given there). Set it back to None whenever the GEMM kernel changes.
-GEMM_DRAM_BYTES_PER_LAUNCH = 109.7e6
+# DRAM bytes read + written per GEMM launch: dram__bytes_read.sum + dram__bytes_write.sum of
+# each GEMM shape taken on single-op cases (profiles/gemm_tc_124m.md gives the command and the
+# per-shape figures), weighted by the 147 GEMM launches of a micro-batch (12 of each layer
+# shape, one of each lm_head shape). Set it back to None whenever the GEMM kernel changes.
+GEMM_DRAM_BYTES_PER_LAUNCH = 103.6e6
 
 
 def peaks():
@@ -359,6 +359,9 @@ def run_ours(args, w):
                          "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
                          "frac": gemm_tflops / pk["bf16_sustained"] if gemm_tflops else None,
                          "peak_kind": f"bf16 sustained ({pk['source']})",
+                         # the same against the burst figure (the sustained one was measured
+                         # at a lower clock than the step runs at)
+                         "frac_of_burst": gemm_tflops / pk["bf16"] if gemm_tflops else None,
                          "launches": g_n, "avg_launch_ms": g_ms / g_n if g_n else None,
                          "timed_launches": "every GEMM of each timed step's first micro-batch",
                          "traffic": GEMM_DRAM_BYTES_PER_LAUNCH},
