@@ -20,12 +20,13 @@
 //               cuts the shared-memory operand bytes per FLOP by a third against one block
 //               per tile.
 //   warps 2..9  epilogue (both blocks): warp w reads TMEM lanes 32*(w%4).. (the rows of its
-//               quarter), warps w and w+4 take alternate 32-column chunks of the tile. Per
-//               chunk: tcgen05.ld, the epilogue arithmetic on packed fp32 pairs, the result
-//               into a swizzled shared-memory staging buffer, then one TMA bulk-tensor store
-//               (or, for gradient accumulation, a TMA bulk-tensor reduce-add) of the 32x32
-//               chunk. The epilogue warps of both blocks arrive on the even block's barrier
-//               when an accumulator is free again.
+//               quarter), warps w and w+4 take alternate 64-column steps of the tile. Per
+//               step: the bias and input rows (loaded first), one tcgen05.ld of 64 columns,
+//               the epilogue arithmetic on packed fp32 pairs in two 32-column halves, the
+//               result into a swizzled shared-memory staging slot (128-byte rows), then one
+//               TMA bulk-tensor store per output (for gradient accumulation, two 32-column
+//               TMA bulk-tensor reduce-adds). The epilogue warps of both blocks arrive on
+//               the even block's barrier when an accumulator is free again.
 // Every mbarrier wait is bounded: on timeout the block records DEV_ERR_TIMEOUT, stops
 // issuing work, waits for its own copies and MMAs and frees its tensor memory.
 #include <cuda.h>
@@ -716,7 +717,7 @@ int gemm_tc_pick_splits(int M, int N, int K, int num_sms) {
 }
 
 cudaError_t gemm_bf16_tc(const GemmArgs& g, cudaStream_t s) {
-  // N: whole 64-column epilogue chunk pairs. Any K: a K that is not a multiple of 64 ends in
+  // N: whole 64-column epilogue steps. Any K: a K that is not a multiple of 64 ends in
   // a block that reads zeros past K (the tensor maps check the 16-byte row pitches).
   if (g.M <= 0 || g.N <= 0 || g.K <= 0 || g.N % 64) return cudaErrorInvalidValue;
   const int sms = gemm_tc_num_sms();
