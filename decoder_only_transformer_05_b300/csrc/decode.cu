@@ -188,16 +188,81 @@ cudaError_t attention_decode(DType t, void* out, const void* qkv, const void* ca
 // vectors l, l + 32, ... of their two weight rows, and the M dot products per column are
 // finished with warp reductions. Epilogues: store, tanh-GELU (gelu(u) to out and gelu'(u),
 // or u itself, to pre).
+//
+// Fused forms for the decode step (GemvFuse): with ln_x set, x is LayerNorm(ln_x; ln_w, ln_b)
+// computed here, one warp per row with the lane-to-vector mapping and the operation order of
+// ln_fwd_kernel (so the values equal that kernel's bf16 output); with kv_cache set, the
+// output columns [C, 3C) of the qkv projection (the new position's keys and values) also go
+// to the cache row of position *kv_pos.
 template <int MM>
 __global__ void __launch_bounds__(256)
 gemv_rows_kernel(bf16* __restrict__ out, bf16* __restrict__ pre, const bf16* __restrict__ x,
                  const bf16* __restrict__ W, const bf16* __restrict__ bias,
-                 const bf16* __restrict__ resid, int M, int N, int K, long long ldo, int epi) {
+                 const bf16* __restrict__ resid, int M, int N, int K, long long ldo, int epi,
+                 GemvFuse f) {
   extern __shared__ __align__(16) uint8_t gv_smem[];
   uint4* sx = reinterpret_cast<uint4*>(gv_smem);   // [M][K / 8]
   const int kv = K / 8;
-  for (int i = threadIdx.x; i < M * kv; i += blockDim.x)
-    sx[i] = reinterpret_cast<const uint4*>(x + (size_t)(i / kv) * K)[i % kv];
+  if (f.ln_x) {
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    for (int m = w; m < M; m += 8) {
+      const uint4* xr = reinterpret_cast<const uint4*>((const bf16*)f.ln_x + (size_t)m * K);
+      float2 v[12][4];   // up to 12 vectors of 8 per lane (K <= 3072)
+      float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 12; ++j) {
+        const int c = j * 32 + l;
+        if (c < kv) {
+          const uint4 a = xr[c];
+          v[j][0] = bf2_to_f2(a.x); v[j][1] = bf2_to_f2(a.y);
+          v[j][2] = bf2_to_f2(a.z); v[j][3] = bf2_to_f2(a.w);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v[j][q] = make_float2(0.f, 0.f);
+        }
+        if ((j + 1) * 32 <= kv + 31) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) s2 = __fadd2_rn(s2, v[j][q]);
+        }
+      }
+      const float mu = warp_sum(s2.x + s2.y) / K;
+      const float2 nmu = make_float2(-mu, -mu);
+      float2 q2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 12; ++j) {
+        if (j * 32 + l < kv) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 d = __fadd2_rn(v[j][q], nmu);
+            q2 = __ffma2_rn(d, d, q2);
+          }
+        }
+      }
+      const float rs = rsqrtf(warp_sum(q2.x + q2.y) / K + 1e-5f);
+      const float2 rs2 = make_float2(rs, rs);
+#pragma unroll
+      for (int j = 0; j < 12; ++j) {
+        const int c = j * 32 + l;
+        if (c < kv) {
+          const uint4 wq = reinterpret_cast<const uint4*>(f.ln_w)[c];
+          const uint4 bq = reinterpret_cast<const uint4*>(f.ln_b)[c];
+          const uint32_t ww[4] = {wq.x, wq.y, wq.z, wq.w}, bw[4] = {bq.x, bq.y, bq.z, bq.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 sw = __fmul2_rn(rs2, bf2_to_f2(ww[q]));
+            const float2 sh = __ffma2_rn(nmu, sw, bf2_to_f2(bw[q]));
+            const float2 r = __ffma2_rn(v[j][q], sw, sh);
+            o[q] = pack2_bf16_rn(r.x, r.y);
+          }
+          sx[m * kv + c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < M * kv; i += blockDim.x)
+      sx[i] = reinterpret_cast<const uint4*>(x + (size_t)(i / kv) * K)[i % kv];
+  }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = 2 * (blockIdx.x * 8 + warp);
@@ -243,7 +308,11 @@ gemv_rows_kernel(bf16* __restrict__ out, bf16* __restrict__ pre, const bf16* __r
     u = __fadd2_rn(u, bf2_to_f2(*reinterpret_cast<const uint32_t*>(resid + (size_t)m * ldo + n0)));
   uint32_t* o = reinterpret_cast<uint32_t*>(out + (size_t)m * ldo + n0);
   if (epi == EPI_STORE) {
-    *o = pack2_bf16_rn(u.x, u.y);
+    const uint32_t pk = pack2_bf16_rn(u.x, u.y);
+    *o = pk;
+    if (f.kv_cache && n0 >= f.kv_C)   // row m = batch element m, at position *kv_pos
+      *reinterpret_cast<uint32_t*>((bf16*)f.kv_cache +
+                                   ((size_t)m * f.kv_Tmax + *f.kv_pos) * 2 * f.kv_C + (n0 - f.kv_C)) = pk;
   } else {
     float2 d;
     const float2 g = gelu_tanh_and_grad_fast2(u, d);
@@ -254,7 +323,7 @@ gemv_rows_kernel(bf16* __restrict__ out, bf16* __restrict__ pre, const bf16* __r
 }
 
 template <int MM>
-static cudaError_t gemv_launch(const GemmArgs& g, cudaStream_t s) {
+static cudaError_t gemv_launch(const GemmArgs& g, const GemvFuse& f, cudaStream_t s) {
   const size_t smem = (size_t)g.M * g.K * 2;
   static size_t attr = 48 * 1024;
   if (smem > attr) {
@@ -265,7 +334,7 @@ static cudaError_t gemv_launch(const GemmArgs& g, cudaStream_t s) {
   }
   gemv_rows_kernel<MM><<<ceil_div(g.N, 16), 256, smem, s>>>(
       (bf16*)g.out, (bf16*)g.pre, (const bf16*)g.A, (const bf16*)g.B, (const bf16*)g.bias,
-      (const bf16*)g.resid, g.M, g.N, g.K, g.ldo, g.epi);
+      (const bf16*)g.resid, g.M, g.N, g.K, g.ldo, g.epi, f);
   count_launches(1);
   return last();
 }
@@ -277,13 +346,18 @@ bool gemv_rows_supported(const GemmArgs& g) {
          (g.epi == EPI_STORE || g.pre) && ((uintptr_t)g.A & 15u) == 0 && ((uintptr_t)g.B & 15u) == 0;
 }
 
-cudaError_t gemv_rows(const GemmArgs& g, cudaStream_t s) {
+cudaError_t gemv_rows(const GemmArgs& g, cudaStream_t s, const GemvFuse& f) {
   if (!gemv_rows_supported(g)) return cudaErrorInvalidValue;
-  if (g.M <= 1) return gemv_launch<1>(g, s);
-  if (g.M <= 2) return gemv_launch<2>(g, s);
-  if (g.M <= 4) return gemv_launch<4>(g, s);
-  if (g.M <= 8) return gemv_launch<8>(g, s);
-  return gemv_launch<16>(g, s);
+  if (f.ln_x && (!f.ln_w || !f.ln_b || g.K > 12 * 256 || ((uintptr_t)f.ln_x & 15u) ||
+                 ((uintptr_t)f.ln_w & 15u) || ((uintptr_t)f.ln_b & 15u)))
+    return cudaErrorInvalidValue;
+  if (f.kv_cache && (!f.kv_pos || g.epi != EPI_STORE || g.N != 3 * f.kv_C || f.kv_C % 2))
+    return cudaErrorInvalidValue;
+  if (g.M <= 1) return gemv_launch<1>(g, f, s);
+  if (g.M <= 2) return gemv_launch<2>(g, f, s);
+  if (g.M <= 4) return gemv_launch<4>(g, f, s);
+  if (g.M <= 8) return gemv_launch<8>(g, f, s);
+  return gemv_launch<16>(g, f, s);
 }
 
 __global__ void gather_last_kernel(int* out, const int* in, int B, int T) {

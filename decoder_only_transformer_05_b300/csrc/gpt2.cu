@@ -970,26 +970,42 @@ static int decode_launches(gpt2* h, int B, int t) {
   // the new position's activations use rows 0..B-1 of the forward's buffers
   CKL(encoder_forward(dt, h->x[0], h->mb_tok, h->pw(T_WTE), h->pw(T_WPE), B, 1, C, h->V,
                       h->d_err, s, t, h->d_pos));
+  // bf16, at most 16 rows: the weight-streaming kernel also computes LN1 / LN2 itself and
+  // writes the new keys and values into the cache (fewer dependent launches per layer)
+  const bool fuse = h->is_bf16 && B <= 16;
   for (int l = 0; l < L; ++l) {
-    CKL(layernorm_forward(dt, h->ln1[l], h->ln1_mean[l], h->ln1_rstd[l], h->x[l],
-                          h->pw(T_LN1W, l), h->pw(T_LN1B, l), B, C, s));
     GemmArgs g = linear_fwd(B, 3 * C, C, h->ln1[l], h->pw(T_QKVW, l), h->qkv[l]);
     if (h->bias) g.bias = h->pw(T_QKVB, l);
-    CKL(run_gemm(h, g));
-    CKL(kv_cache_store(dt, h->kv(l), h->qkv[l], B, 1, t, 1, h->T, C, s, h->d_pos));
+    if (fuse) {
+      GemvFuse f;
+      f.ln_x = h->x[l]; f.ln_w = h->pw(T_LN1W, l); f.ln_b = h->pw(T_LN1B, l);
+      f.kv_cache = h->kv(l); f.kv_Tmax = h->T; f.kv_C = C; f.kv_pos = h->d_pos;
+      CKL(gemv_rows(g, s, f));
+    } else {
+      CKL(layernorm_forward(dt, h->ln1[l], h->ln1_mean[l], h->ln1_rstd[l], h->x[l],
+                            h->pw(T_LN1W, l), h->pw(T_LN1B, l), B, C, s));
+      CKL(run_gemm(h, g));
+      CKL(kv_cache_store(dt, h->kv(l), h->qkv[l], B, 1, t, 1, h->T, C, s, h->d_pos));
+    }
     CKL(attention_decode(dt, h->att[l], h->qkv[l], h->kv(l), B, t, h->T, C, h->H, s, h->d_pos,
                          h->Dbuf));
     g = linear_fwd(B, C, C, h->att[l], h->pw(T_ATTPROJW, l), h->xmid[l]);
     if (h->bias) g.bias = h->pw(T_ATTPROJB, l);
     g.resid = h->x[l];
     CKL(run_gemm(h, g));
-    CKL(layernorm_forward(dt, h->ln2[l], h->ln2_mean[l], h->ln2_rstd[l], h->xmid[l],
-                          h->pw(T_LN2W, l), h->pw(T_LN2B, l), B, C, s));
     g = linear_fwd(B, 4 * C, C, h->ln2[l], h->pw(T_FCW, l), h->fcg[l]);
     if (h->bias) g.bias = h->pw(T_FCB, l);
     g.epi = h->recompute ? EPI_GELU_FWD_U : EPI_GELU_FWD;
     g.pre = h->fch[l];
-    CKL(run_gemm(h, g));
+    if (fuse) {
+      GemvFuse f;
+      f.ln_x = h->xmid[l]; f.ln_w = h->pw(T_LN2W, l); f.ln_b = h->pw(T_LN2B, l);
+      CKL(gemv_rows(g, s, f));
+    } else {
+      CKL(layernorm_forward(dt, h->ln2[l], h->ln2_mean[l], h->ln2_rstd[l], h->xmid[l],
+                            h->pw(T_LN2W, l), h->pw(T_LN2B, l), B, C, s));
+      CKL(run_gemm(h, g));
+    }
     g = linear_fwd(B, C, 4 * C, h->fcg[l], h->pw(T_FCPROJW, l), h->x[l + 1]);
     if (h->bias) g.bias = h->pw(T_FCPROJB, l);
     g.resid = h->xmid[l];

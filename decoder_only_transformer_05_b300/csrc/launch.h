@@ -183,7 +183,14 @@ cudaError_t gather_last(int* out, const int* in, int B, int T, cudaStream_t s);
 // step's linear layers, streaming each weight once (gemv_rows_supported says which GemmArgs
 // it takes: K-major operands, N and ldo even, K % 8 == 0, epilogues store / GELU forward)
 bool gemv_rows_supported(const GemmArgs& g);
-cudaError_t gemv_rows(const GemmArgs& g, cudaStream_t s);
+// Optional fusions of the decode step: ln_x set -> X = LayerNorm(ln_x; ln_w, ln_b) (eps 1e-5)
+// computed inside (K <= 3072); kv_cache set (qkv projection, EPI_STORE, N = 3 kv_C) -> the
+// K and V columns also go to cache[(m Tmax + *kv_pos) 2C + (n - C)].
+struct GemvFuse {   // bf16 pointers
+  const void* ln_x = nullptr; const void* ln_w = nullptr; const void* ln_b = nullptr;
+  void* kv_cache = nullptr; int kv_Tmax = 0; int kv_C = 0; const int* kv_pos = nullptr;
+};
+cudaError_t gemv_rows(const GemmArgs& g, cudaStream_t s, const GemvFuse& f = GemvFuse());
 // the device copy of the decode position: *pos_dev = set if set >= 0, else *pos_dev += add
 cudaError_t decode_position(int* pos_dev, int set, int add, cudaStream_t s);
 
