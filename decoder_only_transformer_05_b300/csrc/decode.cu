@@ -1,6 +1,9 @@
 // Forward-only inference with a KV cache (greedy decoding, one new token per sequence per
-// step): the cache store, the one-query attention over the cached keys and values, and a
-// gather of the prompt's last positions. The model and the causal scaled softmax attention
+// step): the cache store, the one-query attention over the cached keys and values (split over
+// key blocks, then combined), the weight-streaming linear layers of the step's few rows (with
+// LayerNorm and the cache store fused in), the device-side position counter that lets a
+// recorded step be replayed, and a gather of the prompt's last positions. The model and the
+// causal scaled softmax attention
 // are those of 「从零实现一个最小GPT：代码讲解 + 知识点全解」 (二.3 Head, 三.3); its 三.8
 // generation loop re-runs the whole prefix for each new token, whereas here each layer's
 // keys and values of earlier positions are kept and only the new position is computed.
