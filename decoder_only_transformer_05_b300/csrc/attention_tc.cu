@@ -343,7 +343,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
         const bool diag = (j == qblk);
         uint32_t sr[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32_nowait(lane_base + s_col + c * 32, sr[c]);
+        tmem_ld64_nowait(lane_base + s_col, *reinterpret_cast<uint32_t (*)[64]>(&sr[0][0]));
+        tmem_ld64_nowait(lane_base + s_col + 64, *reinterpret_cast<uint32_t (*)[64]>(&sr[2][0]));
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -425,8 +426,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       uint32_t o[2][32];
-      tmem_ld32_nowait(lane_base + o_col, o[0]);
-      tmem_ld32_nowait(lane_base + o_col + 32, o[1]);
+      tmem_ld64_nowait(lane_base + o_col, *reinterpret_cast<uint32_t (*)[64]>(&o[0][0]));
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
@@ -682,10 +682,8 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant
         // second load), each chunk stored as soon as it is computed; the mask (causal on
         // the diagonal block, past T on the last) only in the blocks that need it
         uint32_t sv[2][32], dv[2][32];
-        tmem_ld32_nowait(lane_base + COL_S + c0, sv[0]);
-        tmem_ld32_nowait(lane_base + COL_DP + c0, dv[0]);
-        tmem_ld32_nowait(lane_base + COL_S + c0 + 32, sv[1]);
-        tmem_ld32_nowait(lane_base + COL_DP + c0 + 32, dv[1]);
+        tmem_ld64_nowait(lane_base + COL_S + c0, *reinterpret_cast<uint32_t (*)[64]>(&sv[0][0]));
+        tmem_ld64_nowait(lane_base + COL_DP + c0, *reinterpret_cast<uint32_t (*)[64]>(&dv[0][0]));
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -1027,10 +1025,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant_
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         uint32_t sv[2][32], dv[2][32];
-        tmem_ld32_nowait(lane_base + COL_S + c0, sv[0]);
-        tmem_ld32_nowait(lane_base + COL_DP + c0, dv[0]);
-        tmem_ld32_nowait(lane_base + COL_S + c0 + 32, sv[1]);
-        tmem_ld32_nowait(lane_base + COL_DP + c0 + 32, dv[1]);
+        tmem_ld64_nowait(lane_base + COL_S + c0, *reinterpret_cast<uint32_t (*)[64]>(&sv[0][0]));
+        tmem_ld64_nowait(lane_base + COL_DP + c0, *reinterpret_cast<uint32_t (*)[64]>(&dv[0][0]));
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
