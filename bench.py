@@ -43,9 +43,9 @@ WORKLOAD_TEXT = {
 
 
 # DRAM bytes read + written per GEMM launch: dram__bytes_read.sum + dram__bytes_write.sum of
-# each GEMM shape taken on single-op cases (profiles/gemm_tc_124m.md gives the command and the
-# per-shape figures), weighted by the 147 GEMM launches of a micro-batch (12 of each layer
-# shape, one of each lm_head shape). Set it back to None whenever the GEMM kernel changes.
+# each GEMM shape, from an ncu capture of `opbench --ops gemm --iters 1` (single-op cases),
+# weighted by the 147 GEMM launches of a micro-batch (12 of each layer shape, one of each
+# lm_head shape). Set it back to None whenever the GEMM kernel changes.
 GEMM_DRAM_BYTES_PER_LAUNCH = 103.6e6
 
 
