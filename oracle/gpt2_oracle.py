@@ -20,7 +20,7 @@ What it follows (cited by page title and section):
   * 「4.1 GPT-2 (124M) 复现」 section 2.3: gradient accumulation and the 6e-4 -> 6e-5
     learning-rate range with 2000 warmup steps.
 
-Readings where the pages are silent or disagree (each is listed in the design notes):
+Readings where the pages are silent or disagree:
   * fused QKV: one [3C, C] weight whose rows are the Q, K, V thirds, each third
     holding the heads in order; equal to the per-head Linears stacked.
   * the lm_head is tied to the token embedding; logits cover the first V (unpadded)
