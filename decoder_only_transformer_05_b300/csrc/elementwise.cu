@@ -132,14 +132,79 @@ __device__ int block_exclusive_scan(int v, int* sh, int* total) {
 }
 
 __global__ void __launch_bounds__(SORT_THREADS, 1)
-encoder_sort_kernel(const int* __restrict__ tokens, int M, int Vp, EncScratch sc) {
+encoder_sort_kernel(const int* __restrict__ tokens, int M, int Vp, EncScratch sc, int packed) {
   __shared__ int hist[256][SORT_WARPS + 1];
   __shared__ int scan_sh[40];
+  extern __shared__ uint32_t srt[];   // packed: [2][M] of (key << 16 | position)
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int per_warp = (M + SORT_WARPS - 1) / SORT_WARPS;
   const int lo = min(M, w * per_warp), hi = min(M, lo + per_warp);
+  if (packed) {
+    // M <= 65536 and Vp <= 65536: key and position share one word and both radix passes run
+    // in shared memory (the same stable per-warp counting, scan and scatter as below)
+    uint32_t* a = srt;
+    uint32_t* b = srt + M;
+    for (int i = threadIdx.x; i < M; i += blockDim.x) {
+      int t = tokens[i];
+      t = t < 0 ? 0 : (t >= Vp ? Vp - 1 : t);
+      a[i] = ((uint32_t)t << 16) | (uint32_t)i;
+    }
+    int kbits = 0;
+    while ((1 << kbits) < Vp) kbits += 8;
+    for (int shift = 16; shift < 16 + kbits; shift += 8) {
+      for (int i = threadIdx.x; i < 256 * (SORT_WARPS + 1); i += blockDim.x)
+        (&hist[0][0])[i] = 0;
+      __syncthreads();
+      for (int base = lo; base < hi; base += 32) {
+        const int i = base + lane;
+        const bool valid = i < hi;
+        const int d = valid ? (int)((a[i] >> shift) & 255u) : -1 - lane;
+        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        if (valid && lane == __ffs(peers) - 1) hist[d][w] += __popc(peers);
+        __syncwarp();
+      }
+      __syncthreads();
+      {
+        const int cells = 256 * SORT_WARPS;
+        const int per = cells / SORT_THREADS;
+        const int c0 = threadIdx.x * per;
+        int local = 0;
+        for (int j = 0; j < per; ++j) { const int c = c0 + j; local += hist[c / SORT_WARPS][c % SORT_WARPS]; }
+        int total;
+        int run = block_exclusive_scan(local, scan_sh, &total);
+        for (int j = 0; j < per; ++j) {
+          const int c = c0 + j;
+          const int v = hist[c / SORT_WARPS][c % SORT_WARPS];
+          hist[c / SORT_WARPS][c % SORT_WARPS] = run;
+          run += v;
+        }
+      }
+      __syncthreads();
+      for (int base = lo; base < hi; base += 32) {
+        const int i = base + lane;
+        const bool valid = i < hi;
+        const uint32_t k = valid ? a[i] : 0u;
+        const int d = valid ? (int)((k >> shift) & 255u) : -1 - lane;
+        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        const int leader = __ffs(peers) - 1;
+        const int basepos = valid ? hist[d][w] : 0;
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (valid) b[basepos + rank] = k;
+        __syncwarp();
+        if (valid && lane == leader) hist[d][w] = basepos + __popc(peers);
+        __syncwarp();
+      }
+      __syncthreads();
+      uint32_t* t = a; a = b; b = t;
+    }
+    for (int i = threadIdx.x; i < M; i += blockDim.x) {
+      sc.key0[i] = (int)(a[i] >> 16);
+      sc.pos0[i] = (int)(a[i] & 0xffffu);
+    }
+    __syncthreads();
+  }
   // load keys (clamped ids) and positions
-  for (int i = threadIdx.x; i < M; i += blockDim.x) {
+  for (int i = threadIdx.x; !packed && i < M; i += blockDim.x) {
     int t = tokens[i];
     t = t < 0 ? 0 : (t >= Vp ? Vp - 1 : t);
     sc.key0[i] = t;
@@ -147,7 +212,7 @@ encoder_sort_kernel(const int* __restrict__ tokens, int M, int Vp, EncScratch sc
   }
   __syncthreads();
   int bits = 0;
-  while ((1 << bits) < Vp) bits += 8;
+  while (!packed && (1 << bits) < Vp) bits += 8;   // packed: already sorted
   int* kin = sc.key0; int* pin = sc.pos0; int* kout = sc.key1; int* pout = sc.pos1;
   for (int shift = 0; shift < bits; shift += 8) {
     for (int i = threadIdx.x; i < 256 * (SORT_WARPS + 1); i += blockDim.x)
@@ -408,7 +473,19 @@ cudaError_t encoder_backward(DType t, float* dwte, float* dwpe, const void* dx, 
                              cudaStream_t s) {
   const int M = B * T_;
   EncScratch sc = enc_scratch(scratch, M);
-  encoder_sort_kernel<<<1, SORT_THREADS, 0, s>>>(tokens, M, Vp, sc);
+  // keys and positions packed in one word and sorted in shared memory where they fit
+  const int packed = M <= 65536 && Vp <= 65536 && (size_t)M * 8 <= 180 * 1024;
+  const size_t smem = packed ? (size_t)M * 8 : 0;
+  if (packed) {
+    static size_t attr = 0;
+    if (smem > attr) {
+      cudaError_t e = cudaFuncSetAttribute(encoder_sort_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      attr = smem;
+    }
+  }
+  encoder_sort_kernel<<<1, SORT_THREADS, smem, s>>>(tokens, M, Vp, sc, packed);
   count_launches(1);
   // MAXV 16-byte vectors per lane cover the row: 8 bf16 or 4 fp32 each, 32 lanes
   if (t == DType::BF16) {
